@@ -1,0 +1,346 @@
+/*
+ * CPU oracle for the W4A16 group-quantized matmul and the Q4 block-32 GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, scalar, obviously-correct
+ * restatement of what the pages define. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it. The CUDA library never calls it and
+ * shares no code with it.
+ *
+ * Build: gcc -O1 -ffp-contract=off -fPIC -shared (no fast-math, no FMA
+ * contraction), so that every fp32 step below is one IEEE-754 operation rounded
+ * to nearest-even, exactly as written.
+ *
+ * Sources (page title, section):
+ *   [P1] "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured",
+ *        Step 2 (group-128 scale/min, q = round((w-min)/scale), 8 nibbles per
+ *        int32 along K, K/8 x N packed matrix, K/128 x N scales and minimums;
+ *        the Triton listing's unpack "row 8r+j = nibble j of word r" and its
+ *        dequantize "q*s + m").
+ *   [P2] "Why My 4-Bit CUDA Kernel Wasn't Faster", sections "Why fewer bytes
+ *        should have helped" and "Loading the same bytes differently" (18-byte
+ *        block of 32 codes + 2-byte FP16 scale; decode = code minus bias, times
+ *        scale; low nibble is the even weight, high nibble the odd one).
+ *   [P3] "Quantization and GEMV", section "W4A16: dequantizing in registers"
+ *        (first element in the low 4 bits) and "The quantization formulas".
+ *
+ * Readings where the pages are silent (each also listed in the design doc):
+ *   - round() is round-half-to-even (IEEE default; PyTorch's torch.round).
+ *   - s and min are rounded to BF16 first; q is computed against the stored
+ *     BF16 values, in fp32: t = (w - min_bf16) / s_bf16, then RNE, then clamp
+ *     to [0, 15].
+ *   - scale = bf16_rne(fp32((max - min) / 15)) (fp32 subtract, fp32 divide).
+ *   - A group whose BF16 scale is zero stores q = 0 (so w_hat = min).
+ *   - Q4: scale = fp16_rne(fp32(max|w| / 8)); q = clamp(rne(w / s) + 8, 0, 15);
+ *     a zero scale stores q = 8 (w_hat = 0).
+ *   - Weights are finite.
+ *
+ * Parity pins (tests/test_oracle_pins.py): rounding helpers against PyTorch's
+ * own conversions; hand-worked groups in tests/golden/; 4.25 bits/weight and
+ * the pages' byte counts; round trips for on-grid weights; one-hot x; constant
+ * groups; brute force at N,K <= 64 against exact rational arithmetic; the
+ * fp64 matmul against torch.matmul; the pages' ~10 % quantization error band.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* IEEE conversions, written from the format definitions.                    */
+/* ------------------------------------------------------------------------ */
+
+/* Round a finite double to an integer, ties to even, without relying on the
+ * current floating-point environment. */
+static double round_half_even(double v) {
+  double f = floor(v);
+  double frac = v - f; /* exact for |v| < 2^52 */
+  if (frac > 0.5) return f + 1.0;
+  if (frac < 0.5) return f;
+  /* exact tie: pick the even neighbour */
+  return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* Convert an fp32 value to a binary format with `mbits` explicit mantissa bits,
+ * exponent bias `bias` and largest exponent `emax` (of a finite value), rounding
+ * to nearest, ties to even. Returns the bit pattern (sign at bit 15). */
+static uint16_t to_small_float(float f, int mbits, int bias, int emax) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  int ebits = 15 - mbits;
+  uint16_t exp_all_ones = (uint16_t)(((1u << ebits) - 1u) << mbits);
+  if (isnan(f)) return (uint16_t)(sign | exp_all_ones | (1u << (mbits - 1)));
+  double a = fabs((double)f);
+  if (isinf(f)) return (uint16_t)(sign | exp_all_ones);
+  if (a == 0.0) return sign;
+  int emin = 1 - bias; /* exponent of the smallest normal */
+  int e;
+  frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+  e -= 1;       /* a = 1.xxx * 2^e */
+  if (e < emin) {
+    /* subnormal range: units of 2^(emin - mbits) */
+    double q = round_half_even(ldexp(a, mbits - emin));
+    /* q == 2^mbits is the smallest normal; the encoding below is continuous */
+    return (uint16_t)(sign | (uint16_t)q);
+  }
+  double sig = round_half_even(ldexp(a, mbits - e)); /* in [2^mbits, 2^(mbits+1)] */
+  if (sig == ldexp(1.0, mbits + 1)) {
+    sig = ldexp(1.0, mbits);
+    e += 1;
+  }
+  if (e > emax) return (uint16_t)(sign | exp_all_ones); /* overflow -> inf */
+  uint16_t biased = (uint16_t)(e + bias);
+  return (uint16_t)(sign | (uint16_t)(biased << mbits) |
+                    (uint16_t)((uint32_t)sig - (1u << mbits)));
+}
+
+uint16_t oracle_bf16_rne(float f) { return to_small_float(f, 7, 127, 127); }
+uint16_t oracle_fp16_rne(float f) { return to_small_float(f, 10, 15, 15); }
+
+float oracle_bf16_to_float(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+float oracle_fp16_to_float(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int m = h & 0x3ff;
+  double v;
+  if (e == 0x1f) {
+    v = m ? NAN : INFINITY;
+  } else if (e == 0) {
+    v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+  } else {
+    v = ldexp((double)(m + 1024), e - 15 - 10);
+  }
+  return (float)(sign ? -v : v);
+}
+
+/* Array forms of the conversions (same arithmetic, one call per array). */
+void oracle_bf16_rne_array(const float* in, uint16_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = oracle_bf16_rne(in[i]);
+}
+void oracle_fp16_rne_array(const float* in, uint16_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = oracle_fp16_rne(in[i]);
+}
+void oracle_fp16_to_float_array(const uint16_t* in, float* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = oracle_fp16_to_float(in[i]);
+}
+
+/* Round an fp32 value to the nearest integer, ties to even (the reading of
+ * "round" in [P1] Step 2). */
+static float rne_int(float t) { return (float)round_half_even((double)t); }
+
+/* ------------------------------------------------------------------------ */
+/* W4A16: quantize, pack, dequantize, matmul ([P1] Step 2).                  */
+/* ------------------------------------------------------------------------ */
+
+/* w: fp32 [N, K] row-major (one output feature per row, K contiguous).
+ * codes: u8 [N, K] (one 4-bit code per byte).
+ * scales, mins: bf16 bit patterns [K/G, N] (group-major, N contiguous).
+ * Per group of G consecutive weights along K: scale = (max - min) / 15 and
+ * q = round((w - min) / scale), 0..15. */
+void oracle_w4a16_quantize(const float* w, int N, int K, int G, uint8_t* codes,
+                           uint16_t* scales, uint16_t* mins) {
+  int groups = K / G;
+  for (int n = 0; n < N; ++n) {
+    for (int g = 0; g < groups; ++g) {
+      const float* wg = w + (size_t)n * K + (size_t)g * G;
+      float lo = wg[0], hi = wg[0];
+      for (int i = 1; i < G; ++i) {
+        if (wg[i] < lo) lo = wg[i];
+        if (wg[i] > hi) hi = wg[i];
+      }
+      volatile float range = hi - lo;        /* one fp32 subtraction */
+      volatile float s32 = range / 15.0f;    /* one fp32 division */
+      uint16_t s_b = oracle_bf16_rne(s32);
+      uint16_t m_b = oracle_bf16_rne(lo);
+      scales[(size_t)g * N + n] = s_b;
+      mins[(size_t)g * N + n] = m_b;
+      float s = oracle_bf16_to_float(s_b);
+      float m = oracle_bf16_to_float(m_b);
+      for (int i = 0; i < G; ++i) {
+        int q;
+        if (s == 0.0f) {
+          q = 0;
+        } else {
+          volatile float diff = wg[i] - m; /* fp32 subtraction */
+          volatile float t = diff / s;     /* fp32 division */
+          float r = rne_int(t);
+          q = r < 0.0f ? 0 : (r > 15.0f ? 15 : (int)r);
+        }
+        codes[(size_t)n * K + (size_t)g * G + i] = (uint8_t)q;
+      }
+    }
+  }
+}
+
+/* Pack 8 codes per 32-bit word along K: word (r, n) holds k = 8r + j in bits
+ * 4j..4j+3, first element in the low nibble ([P1] Step 2 listing comment
+ * "row 8r + j = nibble j of word r"; [P3] "first element in the low 4 bits").
+ * qw: int32 [K/8, N], N contiguous. */
+void oracle_w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw) {
+  for (int r = 0; r < K / 8; ++r) {
+    for (int n = 0; n < N; ++n) {
+      uint32_t word = 0;
+      for (int j = 0; j < 8; ++j) {
+        uint32_t q = codes[(size_t)n * K + (size_t)r * 8 + j] & 0xFu;
+        word |= q << (4 * j);
+      }
+      qw[(size_t)r * N + n] = (int32_t)word;
+    }
+  }
+}
+
+/* Code of weight (n, k) read back from the packed matrix. */
+static int unpack_code(const int32_t* qw, int N, int n, int k) {
+  uint32_t word = (uint32_t)qw[(size_t)(k / 8) * N + n];
+  return (int)((word >> (4 * (k % 8))) & 0xFu);
+}
+
+/* w_hat[n, k] = q * s + min in fp64 ([P1] Step 2: "q * s + m"). The product of
+ * a 4-bit integer and a BF16 scale is exact in fp64, and so is the sum with a
+ * BF16 minimum unless their exponents differ by more than ~40. */
+void oracle_w4a16_dequant(const int32_t* qw, const uint16_t* scales, const uint16_t* mins,
+                          int N, int K, int G, double* w_hat) {
+  for (int n = 0; n < N; ++n) {
+    for (int k = 0; k < K; ++k) {
+      int g = k / G;
+      double s = (double)oracle_bf16_to_float(scales[(size_t)g * N + n]);
+      double m = (double)oracle_bf16_to_float(mins[(size_t)g * N + n]);
+      w_hat[(size_t)n * K + k] = (double)unpack_code(qw, N, n, k) * s + m;
+    }
+  }
+}
+
+/* y_ref[m, n] = sum_k x[m, k] * w_hat[n, k] in fp64, and
+ * abs_ref[m, n] = sum_k |x[m, k] * w_hat[n, k]| (the scale of the rounding
+ * error allowed to a BF16/fp32 implementation).
+ * x: bf16 bit patterns [M, K]; result arrays [M, N]. */
+void oracle_w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                         const uint16_t* mins, int M, int N, int K, int G, double* y_ref,
+                         double* abs_ref) {
+  for (int m = 0; m < M; ++m) {
+    for (int n = 0; n < N; ++n) {
+      double acc = 0.0, acc_abs = 0.0;
+      for (int k = 0; k < K; ++k) {
+        int g = k / G;
+        double s = (double)oracle_bf16_to_float(scales[(size_t)g * N + n]);
+        double mn = (double)oracle_bf16_to_float(mins[(size_t)g * N + n]);
+        double w_hat = (double)unpack_code(qw, N, n, k) * s + mn;
+        double xv = (double)oracle_bf16_to_float(x[(size_t)m * K + k]);
+        acc += xv * w_hat;
+        acc_abs += fabs(xv * w_hat);
+      }
+      y_ref[(size_t)m * N + n] = acc;
+      if (abs_ref) abs_ref[(size_t)m * N + n] = acc_abs;
+    }
+  }
+}
+
+/* Same as oracle_w4a16_matmul but only for the listed output columns
+ * (cols[i] for i < ncols); results are [M, ncols]. Used to check full-size
+ * launches on a sample of outputs. */
+void oracle_w4a16_matmul_cols(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                              const uint16_t* mins, int M, int N, int K, int G,
+                              const int32_t* cols, int ncols, double* y_ref,
+                              double* abs_ref) {
+  for (int m = 0; m < M; ++m) {
+    for (int i = 0; i < ncols; ++i) {
+      int n = cols[i];
+      double acc = 0.0, acc_abs = 0.0;
+      for (int k = 0; k < K; ++k) {
+        int g = k / G;
+        double s = (double)oracle_bf16_to_float(scales[(size_t)g * N + n]);
+        double mn = (double)oracle_bf16_to_float(mins[(size_t)g * N + n]);
+        double w_hat = (double)unpack_code(qw, N, n, k) * s + mn;
+        double xv = (double)oracle_bf16_to_float(x[(size_t)m * K + k]);
+        acc += xv * w_hat;
+        acc_abs += fabs(xv * w_hat);
+      }
+      y_ref[(size_t)m * ncols + i] = acc;
+      if (abs_ref) abs_ref[(size_t)m * ncols + i] = acc_abs;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q4 block-32 ([P2]): 32 codes + one FP16 scale, w_hat = (q - 8) * s.       */
+/* ------------------------------------------------------------------------ */
+
+/* w: fp32 [N, K]; codes: u8 [N, K/2] (= [N, K/32, 16]; byte j of a block holds
+ * weight 2j in the low nibble and weight 2j+1 in the high nibble);
+ * scales: fp16 bit patterns [N, K/32]. */
+void oracle_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales) {
+  int blocks = K / 32;
+  for (int n = 0; n < N; ++n) {
+    for (int b = 0; b < blocks; ++b) {
+      const float* wb = w + (size_t)n * K + (size_t)b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        float a = fabsf(wb[i]);
+        if (a > amax) amax = a;
+      }
+      volatile float s32 = amax / 8.0f; /* one fp32 division */
+      uint16_t s_h = oracle_fp16_rne(s32);
+      scales[(size_t)n * blocks + b] = s_h;
+      float s = oracle_fp16_to_float(s_h);
+      int q[32];
+      for (int i = 0; i < 32; ++i) {
+        if (s == 0.0f) {
+          q[i] = 8;
+        } else {
+          volatile float t = wb[i] / s; /* fp32 division */
+          float r = rne_int(t) + 8.0f;
+          q[i] = r < 0.0f ? 0 : (r > 15.0f ? 15 : (int)r);
+        }
+      }
+      uint8_t* cb = codes + (size_t)n * (K / 2) + (size_t)b * 16;
+      for (int j = 0; j < 16; ++j) cb[j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+    }
+  }
+}
+
+static int q4_code(const uint8_t* codes, int K, int n, int k) {
+  uint8_t byte = codes[(size_t)n * (K / 2) + (size_t)(k / 2)];
+  return (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+}
+
+/* w_hat[n, k] = (q - 8) * s in fp64 (exact). */
+void oracle_q4b32_dequant(const uint8_t* codes, const uint16_t* scales, int N, int K,
+                          double* w_hat) {
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) {
+      double s = (double)oracle_fp16_to_float(scales[(size_t)n * (K / 32) + k / 32]);
+      w_hat[(size_t)n * K + k] = (double)(q4_code(codes, K, n, k) - 8) * s;
+    }
+}
+
+/* y_ref[n] = sum_b s[n, b] * sum_j (q[n, b, j] - 8) * x[32 b + j], in fp64;
+ * abs_ref[n] = sum_k |x[k] * w_hat[n, k]|. x: fp16 bit patterns [K]. Only the
+ * listed rows (rows[i], i < nrows) are computed; pass rows = NULL for all N. */
+void oracle_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                       int N, int K, const int32_t* rows, int nrows, double* y_ref,
+                       double* abs_ref) {
+  int count = rows ? nrows : N;
+  for (int i = 0; i < count; ++i) {
+    int n = rows ? rows[i] : i;
+    double acc = 0.0, acc_abs = 0.0;
+    for (int b = 0; b < K / 32; ++b) {
+      double s = (double)oracle_fp16_to_float(scales[(size_t)n * (K / 32) + b]);
+      double block = 0.0;
+      for (int j = 0; j < 32; ++j) {
+        int k = 32 * b + j;
+        double xv = (double)oracle_fp16_to_float(x[k]);
+        double qv = (double)(q4_code(codes, K, n, k) - 8);
+        block += qv * xv;
+        acc_abs += fabs(qv * s * xv);
+      }
+      acc += s * block;
+    }
+    y_ref[i] = acc;
+    if (abs_ref) abs_ref[i] = acc_abs;
+  }
+}

@@ -1,0 +1,345 @@
+"""Pins for the CPU oracle: checks against facts fixed by the pages and by
+mathematics, never against the oracle itself or the CUDA path.
+
+Every pin is a function ``pin_xxx() -> None`` that raises AssertionError when the
+oracle (whatever build ``oracle`` currently routes to) disagrees with the fact.
+``tests/test_oracle_pins.py`` runs them against the real oracle and
+``tests/test_oracle_mutants.py`` checks that each planted mistake in the oracle
+source is caught by at least one of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------- #
+# fixture readers
+# --------------------------------------------------------------------------- #
+
+def _records(name):
+    """Parse a golden file into a list of (tag, {key: [tokens]}) records."""
+    recs, cur = [], None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key in ("group", "block"):
+                cur = (vals[0], {})
+                recs.append(cur)
+            elif key == "codes":
+                cur = ("pack", {"codes": vals})
+                recs.append(cur)
+            else:
+                cur[1][key] = vals
+    return recs
+
+
+def _page_sizes():
+    out = {}
+    with open(os.path.join(GOLDEN, "page_sizes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                out[k] = float(v)
+    return out
+
+
+def _weights_from(rec):
+    if "w_hex" in rec:
+        bits = np.array([int(t, 16) for t in rec["w_hex"]], dtype=np.uint32)
+        return bits.view(np.float32)
+    return np.array([float(t) for t in rec["w_dec"]], dtype=np.float32)
+
+
+def _bf16(bits):
+    return float(torch.tensor([int(bits) & 0xFFFF], dtype=torch.int32).to(torch.int16)
+                 .view(torch.bfloat16).float())
+
+
+def _fp16(bits):
+    return float(torch.tensor([int(bits) & 0xFFFF], dtype=torch.int32).to(torch.int16)
+                 .view(torch.float16).float())
+
+
+def _torch_bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------- #
+# pins
+# --------------------------------------------------------------------------- #
+
+def pin_rounding_helpers_match_pytorch():
+    """bf16/fp16 round-to-nearest-even against PyTorch's own conversions (a library
+    routine), on special values, exact ties and 2^20 random bit patterns."""
+    g = np.random.default_rng(123)
+    rnd = g.integers(0, 2**32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    specials = np.array([0x00000000, 0x80000000, 0x3F800000, 0x7F7FFFFF, 0xFF7FFFFF,
+                         0x7F800000, 0xFF800000, 0x00000001, 0x807FFFFF, 0x3F808000,
+                         0x3F818000, 0x3F80C000, 0x477FE000, 0x477FF000, 0x477FEFFF,
+                         0x33000000, 0x33000001, 0x33800000, 0x387FE000, 0x38800000],
+                        dtype=np.uint32)
+    bits = np.concatenate([rnd, specials])
+    f = bits.view(np.float32)
+    f = f[~np.isnan(f)]
+    t = torch.from_numpy(f.copy())
+    np.testing.assert_array_equal(oracle.bf16_rne(f), _torch_bits(t.to(torch.bfloat16)))
+    np.testing.assert_array_equal(oracle.fp16_rne(f), _torch_bits(t.to(torch.float16)))
+    all16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    fin = ((all16 >> 10) & 0x1F) != 0x1F
+    got = oracle.fp16_to_float(all16[fin])
+    ref = torch.from_numpy(all16[fin].view(np.int16).copy()).view(torch.float16).float().numpy()
+    np.testing.assert_array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def pin_quantize_hand_worked_groups():
+    """Hand-worked groups (tests/golden/w4a16_quantize_groups.txt)."""
+    for tag, rec in _records("w4a16_quantize_groups.txt"):
+        w = _weights_from(rec).reshape(1, -1)
+        codes, scales, mins = oracle.w4a16_quantize(w, group=w.shape[1])
+        assert int(scales[0, 0]) == int(rec["scale"][0], 16), (tag, hex(scales[0, 0]))
+        assert int(mins[0, 0]) == int(rec["min"][0], 16), (tag, hex(mins[0, 0]))
+        assert codes[0].tolist() == [int(v) for v in rec["q"]], (tag, codes[0].tolist())
+
+
+def pin_pack_hand_worked_words():
+    """Hand-worked packed words (tests/golden/w4a16_pack_words.txt)."""
+    for _, rec in _records("w4a16_pack_words.txt"):
+        codes = np.array([int(v) for v in rec["codes"]], dtype=np.uint8).reshape(1, -1)
+        qw = oracle.w4a16_pack(codes)
+        got = [int(v) & 0xFFFFFFFF for v in qw[:, 0]]
+        assert got == [int(v, 16) for v in rec["words"]], [hex(v) for v in got]
+    # layout: word (r, n) at qw[r, n] -- a 3-column matrix with distinct rows
+    codes = np.array([[c] * 16 for c in (1, 2, 3)], dtype=np.uint8)
+    qw = oracle.w4a16_pack(codes).view(np.uint32)
+    assert qw.shape == (2, 3)
+    assert qw[0].tolist() == [0x11111111, 0x22222222, 0x33333333]
+
+
+def pin_sizes_printed_on_pages():
+    """4.25 bits/weight, 3.76x, 31.2 MB, the 4 KB vs 16 KB tile, 18-byte Q4 blocks,
+    3.56x and 144 MiB, all computed from the array sizes the oracle produces."""
+    p = _page_sizes()
+    N, K, G = 64, 256, 128
+    codes, s, m = oracle.w4a16_quantize(workloads.weights(N, K, seed=1).numpy(), group=G)
+    qw = oracle.w4a16_pack(codes)
+    bits = 8.0 * (qw.nbytes + s.nbytes + m.nbytes) / (N * K)
+    assert bits == p["w4a16_bits_per_weight"]
+    assert round(16.0 / bits, 2) == p["w4a16_speedup_cap"]
+    # the Llama up-projection: bytes per weight from the small case, scaled
+    n_w = int(p["w4a16_llama_up_N"] * p["w4a16_llama_up_K"])
+    total = n_w * (qw.nbytes + s.nbytes + m.nbytes) // (N * K)
+    assert total == 31_195_136 and round(total / 1e6, 1) == p["w4a16_llama_up_mb"]
+    # a 128 (K) x 64 (N) tile of packed words vs BF16
+    tk, tn = int(p["w4a16_tile_K"]), int(p["w4a16_tile_N"])
+    tile_q = oracle.w4a16_pack(np.zeros((tn, tk), dtype=np.uint8))
+    assert tile_q.nbytes == p["w4a16_tile_packed_bytes"]
+    assert tk * tn * 2 == p["w4a16_tile_bf16_bytes"]
+    # Q4: 16 code bytes + 2 scale bytes per 32 weights
+    qc, qs = oracle.q4b32_quantize(workloads.weights(4, 64, seed=2).numpy())
+    per_block = (qc.nbytes + qs.nbytes) / (4 * 64 / 32)
+    assert per_block == p["q4_block_bytes"]
+    assert round(p["q4_block_fp16_bytes"] / per_block, 2) == p["q4_ratio"]
+    n2 = int(p["q4_square_N"]) ** 2
+    assert n2 // 32 * per_block == p["q4_square_mib"] * 2**20
+
+
+def pin_round_trip_on_grid():
+    """Weights already on the 16-level grid (q*s + min exact, q = 0 and 15 present
+    in every group) quantize back to exactly (q, s, min) and rebuild bit for bit."""
+    rng = np.random.default_rng(7)
+    N, K, G = 24, 256, 32
+    groups = K // G
+    s_b = oracle.bf16_rne(2.0 ** rng.uniform(-10, -5, size=(groups, N)))
+    m_b = oracle.bf16_rne(rng.uniform(-0.5, 0.0, size=(groups, N)))
+    q = rng.integers(0, 16, size=(N, K))
+    q[:, ::G] = 0
+    q[:, 1::G] = 15
+    w = np.empty((N, K), dtype=np.float64)
+    for n in range(N):
+        for k in range(K):
+            w[n, k] = q[n, k] * _bf16(s_b[k // G, n]) + _bf16(m_b[k // G, n])
+    w32 = w.astype(np.float32)
+    assert np.array_equal(w32.astype(np.float64), w), "grid values must be exact in fp32"
+    codes, s2, m2 = oracle.w4a16_quantize(w32, group=G)
+    np.testing.assert_array_equal(s2, s_b)
+    np.testing.assert_array_equal(m2, m_b)
+    np.testing.assert_array_equal(codes, q.astype(np.uint8))
+    w_hat = oracle.w4a16_dequant(oracle.w4a16_pack(codes), s2, m2, group=G)
+    np.testing.assert_array_equal(w_hat, w)
+
+
+def pin_quantize_nearest_grid_point():
+    """For random groups, every code is a nearest grid point to w in exact arithmetic
+    (ties to the even code), unless the clamp applies or the exact quotient lies within
+    fp32 rounding of a tie; and the stored scale is the BF16 rounding of (max-min)/15."""
+    w = workloads.weights(16, 256, seed=11).numpy()
+    G = 64
+    codes, s, m = oracle.w4a16_quantize(w, group=G)
+    for n in range(w.shape[0]):
+        for g in range(w.shape[1] // G):
+            grp = w[n, g * G:(g + 1) * G]
+            sf, mf = Fraction(_bf16(s[g, n])), Fraction(_bf16(m[g, n]))
+            exact_s = (Fraction(float(grp.max())) - Fraction(float(grp.min()))) / 15
+            assert abs(sf - exact_s) <= exact_s / 2**8, "scale must be bf16(range/15)"
+            assert abs(mf - Fraction(float(grp.min()))) <= abs(Fraction(float(grp.min()))) / 2**8
+            for i, wv in enumerate(grp):
+                t = (Fraction(float(wv)) - mf) / sf
+                q = int(codes[n, g * G + i])
+                best = min(range(16), key=lambda c: (abs(t - c), c % 2))
+                if q != best:
+                    near_tie = abs(abs(t - math.floor(t)) - Fraction(1, 2)) < Fraction(1, 2**18)
+                    assert near_tie, (n, g, i, float(t), q, best)
+
+
+def pin_one_hot_activation():
+    """x = e_k gives y[n] = w_hat[n, k] = q*s + min exactly: pins nibble order, the
+    [K/8, N] layout and the group index of the scale/min."""
+    N, K, G = 40, 384, 128
+    codes, s, m = oracle.w4a16_quantize(workloads.weights(N, K, seed=3).numpy(), group=G)
+    qw = oracle.w4a16_pack(codes)
+    one = _torch_bits(torch.tensor([1.0], dtype=torch.bfloat16))[0]
+    for k in (0, 1, 7, 8, 127, 128, 200, 383):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = one
+        y, a = oracle.w4a16_matmul(x, qw, s, m, group=G)
+        for n in range(N):
+            want = int(codes[n, k]) * _bf16(s[k // G, n]) + _bf16(m[k // G, n])
+            assert y[0, n] == want and a[0, n] == abs(want), (k, n)
+
+
+def pin_constant_codes():
+    """All codes equal c in a group: y = sum_g (c*s_g + min_g) * sum_{k in g} x_k, summed
+    exactly with rationals."""
+    N, K, G = 6, 256, 128
+    rng = np.random.default_rng(5)
+    for c in (0, 9, 15):
+        codes = np.full((N, K), c, dtype=np.uint8)
+        s = oracle.bf16_rne(rng.uniform(0.001, 0.01, size=(K // G, N)))
+        mn = oracle.bf16_rne(rng.uniform(-0.05, 0.0, size=(K // G, N)))
+        x = workloads.bits16(workloads.activations_bf16(2, K, seed=c))
+        y, _ = oracle.w4a16_matmul(x, oracle.w4a16_pack(codes), s, mn, group=G)
+        for r in range(2):
+            for n in range(N):
+                tot = Fraction(0)
+                for g in range(K // G):
+                    sx = sum(Fraction(_bf16(v)) for v in x[r, g * G:(g + 1) * G])
+                    tot += (c * Fraction(_bf16(s[g, n])) + Fraction(_bf16(mn[g, n]))) * sx
+                assert abs(Fraction(y[r, n]) - tot) <= Fraction(1, 2**40), (c, r, n)
+
+
+def pin_brute_force_small():
+    """N, K <= 64, groups 8..64: y from the packed path equals the exact rational triple
+    loop over the unpacked codes to fp64 rounding."""
+    rng = np.random.default_rng(9)
+    for (M, N, K, G) in ((1, 8, 64, 8), (3, 17, 64, 16), (2, 64, 64, 32), (4, 33, 64, 64),
+                         (1, 64, 32, 32)):
+        w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        codes, s, mn = oracle.w4a16_quantize(w, group=G)
+        x = workloads.bits16(workloads.activations_bf16(M, K, seed=N + K))
+        y, a = oracle.w4a16_matmul(x, oracle.w4a16_pack(codes), s, mn, group=G)
+        for r in range(M):
+            for n in range(N):
+                exact = sum(Fraction(_bf16(x[r, k])) *
+                            (int(codes[n, k]) * Fraction(_bf16(s[k // G, n])) +
+                             Fraction(_bf16(mn[k // G, n]))) for k in range(K))
+                assert abs(Fraction(y[r, n]) - exact) <= Fraction(a[r, n]) * Fraction(1, 2**45), \
+                    (M, N, K, G, r, n)
+
+
+def pin_matches_library_matmul():
+    """The fp64 sum equals torch.matmul (fp64) on the rebuilt weights to ~1e-12."""
+    N, K, G, M = 96, 512, 128, 3
+    codes, s, mn = oracle.w4a16_quantize(workloads.weights(N, K, seed=4).numpy(), group=G)
+    qw = oracle.w4a16_pack(codes)
+    x = workloads.bits16(workloads.activations_bf16(M, K, seed=4))
+    y, a = oracle.w4a16_matmul(x, qw, s, mn, group=G)
+    sv = torch.from_numpy(s.view(np.int16).copy()).view(torch.bfloat16).double()
+    mv = torch.from_numpy(mn.view(np.int16).copy()).view(torch.bfloat16).double()
+    w_hat = (torch.from_numpy(codes.astype(np.float64)) * sv.repeat_interleave(G, 0).T
+             + mv.repeat_interleave(G, 0).T)
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double()
+    ref = (xv @ w_hat.T).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    # sampled-column entry point agrees with the full one
+    cols = np.array([0, 5, 95, 17], dtype=np.int32)
+    y2, a2 = oracle.w4a16_matmul(x, qw, s, mn, group=G, cols=cols)
+    np.testing.assert_array_equal(y2, y[:, cols])
+    np.testing.assert_array_equal(a2, a[:, cols])
+
+
+def pin_quantization_error_band():
+    """Rounding N(0, 0.02^2) weights to 16 levels per group of 128 gives ~10 % output
+    error against the original weights (the pages report 10 %); accept 6-14 %."""
+    N, K, G = 256, 2048, 128
+    w = workloads.weights(N, K, seed=0).numpy()
+    codes, s, mn = oracle.w4a16_quantize(w, group=G)
+    w_hat = oracle.w4a16_dequant(oracle.w4a16_pack(codes), s, mn, group=G)
+    x = workloads.activations_bf16(4, K, seed=0).double().numpy()
+    y_q = x @ w_hat.T
+    y_o = x @ w.astype(np.float64).T
+    rel = np.linalg.norm(y_q - y_o) / np.linalg.norm(y_o)
+    assert 0.06 < rel < 0.14, rel
+    # every rebuilt weight lies within half a step of the original (no clamp at this scale)
+    step = np.repeat(torch.from_numpy(s.view(np.int16).copy()).view(torch.bfloat16).double()
+                     .numpy(), G, axis=0).T
+    assert np.all(np.abs(w_hat - w) <= 0.5 * step * (1 + 2**-7) + 2**-9 * np.abs(w))
+
+
+def pin_q4_hand_worked_blocks():
+    """Hand-worked Q4 blocks (tests/golden/q4b32_blocks.txt)."""
+    recs = _records("q4b32_blocks.txt")
+    w = np.stack([_weights_from(r) for _, r in recs])
+    codes, scales = oracle.q4b32_quantize(w)
+    for i, (tag, rec) in enumerate(recs):
+        assert int(scales[i, 0]) == int(rec["scale"][0], 16), tag
+        assert codes[i].tolist() == [int(v, 16) for v in rec["bytes"]], (tag, codes[i].tolist())
+
+
+def pin_q4_round_trip_and_gemv():
+    """On-grid Q4 blocks round-trip; the GEMV equals the exact rational sum, and a
+    one-hot x picks (q - 8) * s."""
+    rng = np.random.default_rng(21)
+    N, K = 12, 128
+    q = rng.integers(1, 16, size=(N, K))
+    q[:, ::32] = 0              # -8 * s sets max|w| = 8 s
+    s_h = oracle.fp16_rne(2.0 ** rng.uniform(-12, -6, size=(N, K // 32)))
+    w = np.empty((N, K), dtype=np.float64)
+    for n in range(N):
+        for k in range(K):
+            w[n, k] = (q[n, k] - 8) * _fp16(s_h[n, k // 32])
+    codes, s2 = oracle.q4b32_quantize(w.astype(np.float32))
+    np.testing.assert_array_equal(s2, s_h)
+    np.testing.assert_array_equal(oracle.q4b32_dequant(codes, s2), w)
+    x = workloads.bits16(workloads.activations_fp16(K, seed=3))
+    y, a = oracle.q4b32_gemv(x, codes, s2)
+    for n in range(N):
+        exact = sum((q[n, k] - 8) * Fraction(_fp16(s_h[n, k // 32])) * Fraction(_fp16(x[k]))
+                    for k in range(K))
+        assert abs(Fraction(y[n]) - exact) <= Fraction(a[n]) * Fraction(1, 2**45)
+    one = _torch_bits(torch.tensor([1.0], dtype=torch.float16))[0]
+    for k in (0, 1, 31, 32, 127):
+        xo = np.zeros(K, dtype=np.uint16)
+        xo[k] = one
+        y, _ = oracle.q4b32_gemv(xo, codes, s2)
+        assert np.array_equal(y, w[:, k]), k
+    rows = np.array([3, 0, 11], dtype=np.int32)
+    y_full, _ = oracle.q4b32_gemv(x, codes, s2)
+    y_rows, _ = oracle.q4b32_gemv(x, codes, s2, rows=rows)
+    np.testing.assert_array_equal(y_rows, y_full[rows])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

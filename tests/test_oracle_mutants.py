@@ -1,0 +1,77 @@
+"""Each plausible mistake planted in (a temporary copy of) the oracle source must make
+at least one pin fail. The mistakes are planted in the oracle, on the CPU; nothing
+here touches the CUDA library."""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
+
+# (id, text in the oracle source, replacement, occurrence index or None for all)
+MUTANTS = [
+    ("pack_nibble_order_reversed", "word |= q << (4 * j);", "word |= q << (4 * (7 - j));", None),
+    ("unpack_nibble_order_reversed", "(word >> (4 * (k % 8)))", "(word >> (4 * (7 - k % 8)))", None),
+    ("matmul_drops_min_term", "double w_hat = (double)unpack_code(qw, N, n, k) * s + mn;",
+     "double w_hat = (double)unpack_code(qw, N, n, k) * s;", None),
+    ("scale_divides_by_16", "range / 15.0f", "range / 16.0f", None),
+    ("scale_from_max_not_range", "volatile float range = hi - lo;", "volatile float range = hi;", None),
+    ("round_half_away", "static float rne_int(float t) { return (float)round_half_even((double)t); }",
+     "static float rne_int(float t) { return roundf(t); }", None),
+    ("q_against_fp32_min", "volatile float diff = wg[i] - m;", "volatile float diff = wg[i] - lo;", None),
+    ("no_clamp_at_15", "q = r < 0.0f ? 0 : (r > 15.0f ? 15 : (int)r);", "q = r < 0.0f ? 0 : (int)r;", 0),
+    ("degenerate_group_code_8", "if (s == 0.0f) {\n          q = 0;", "if (s == 0.0f) {\n          q = 8;", None),
+    ("scale_layout_transposed_in_matmul",
+     "double s = (double)oracle_bf16_to_float(scales[(size_t)g * N + n]);\n"
+     "        double mn = (double)oracle_bf16_to_float(mins[(size_t)g * N + n]);\n"
+     "        double w_hat = (double)unpack_code(qw, N, n, k) * s + mn;\n"
+     "        double xv = (double)oracle_bf16_to_float(x[(size_t)m * K + k]);\n"
+     "        acc += xv * w_hat;",
+     "double s = (double)oracle_bf16_to_float(scales[(size_t)n * (K / G) + g]);\n"
+     "        double mn = (double)oracle_bf16_to_float(mins[(size_t)n * (K / G) + g]);\n"
+     "        double w_hat = (double)unpack_code(qw, N, n, k) * s + mn;\n"
+     "        double xv = (double)oracle_bf16_to_float(x[(size_t)m * K + k]);\n"
+     "        acc += xv * w_hat;", 0),
+    ("matmul_sign_error", "acc += xv * w_hat;", "acc -= xv * w_hat;", None),
+    ("x_index_transposed", "x[(size_t)m * K + k]", "x[(size_t)k * M + m]", None),
+    ("bf16_truncates", "double sig = round_half_even(ldexp(a, mbits - e));",
+     "double sig = floor(ldexp(a, mbits - e));", None),
+    ("q4_bias_7", "float r = rne_int(t) + 8.0f;", "float r = rne_int(t) + 7.0f;", None),
+    ("q4_nibble_pair_swapped", "cb[j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));",
+     "cb[j] = (uint8_t)(q[2 * j + 1] | (q[2 * j] << 4));", None),
+    ("q4_decode_bias_7", "double qv = (double)(q4_code(codes, K, n, k) - 8);",
+     "double qv = (double)(q4_code(codes, K, n, k) - 7);", None),
+    ("q4_scale_divides_by_7", "volatile float s32 = amax / 8.0f;", "volatile float s32 = amax / 7.0f;", None),
+    ("q4_zero_block_code_0", "if (s == 0.0f) {\n          q[i] = 8;", "if (s == 0.0f) {\n          q[i] = 0;", None),
+]
+
+
+def _mutate(text, old, new, occurrence):
+    assert old in text, f"mutation anchor not found: {old!r}"
+    if occurrence is None:
+        return text.replace(old, new)
+    parts = text.split(old)
+    return old.join(parts[:occurrence + 1]) + new + old.join(parts[occurrence + 1:])
+
+
+@pytest.mark.parametrize("mid,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(mid, old, new, occ, tmp_path):
+    with open(SRC) as f:
+        text = f.read()
+    mutated = _mutate(text, old, new, occ)
+    assert mutated != text
+    src = tmp_path / f"{mid}.c"
+    src.write_text(mutated)
+    lib = oracle.compile_to(str(src), str(tmp_path / f"{mid}.so"))
+    caught = []
+    with oracle.use_library(lib):
+        for pin in pins.ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, IndexError, ValueError):
+                caught.append(pin.__name__)
+                break
+    assert caught, f"mutant {mid} passed every pin"
