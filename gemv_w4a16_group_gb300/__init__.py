@@ -1,0 +1,208 @@
+"""GB300 (sm_103a) W4A16 group-quantized matmul and Q4 block-32 GEMV.
+
+Thin Python binding over the C ABI declared in ``include/w4a16.h``: every function
+checks tensor dtypes, shapes and devices, allocates outputs with PyTorch when the caller
+passes none, and hands raw device pointers plus the current CUDA stream to the library.
+All arithmetic runs in the library's CUDA kernels; there is no CPU fallback, and this
+module raises ImportError when the compiled library is missing (build it with
+``python -m gemv_w4a16_group_gb300.build``).
+
+Formats ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2;
+"Why My 4-Bit CUDA Kernel Wasn't Faster"):
+  * W4A16: codes uint8 [N, K]; packed ``qw`` int32 [K/8, N] (word (r, n) holds k = 8r + j
+    in bits 4j..4j+3); ``scales`` and ``mins`` bfloat16 [K/128, N]; x bfloat16 [M, K];
+    y bfloat16 [M, N]; w_hat = q * scale + min.
+  * Q4 block-32: codes uint8 [N, K/2] (low nibble = even k); scales float16 [N, K/32];
+    x float16 [K]; y float16 [N]; w_hat = (q - 8) * scale.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "W4A16Error", "library_path", "w4a16_quantize", "w4a16_pack", "w4a16_matmul",
+    "w4a16_matmul_workspace_bytes", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
+    "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
+    "testing_set_q4_variant",
+]
+
+STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
+                3: "W4A16_ERR_MISALIGNED", 4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT",
+                6: "W4A16_ERR_WORKSPACE"}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"the GB300 kernel library is not built ({LIB_PATH} missing); run "
+            "`python -m gemv_w4a16_group_gb300.build` on a machine with nvcc")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S, U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
+    sigs = {
+        "w4a16_quantize": [P, I, I, I, P, P, P, P],
+        "w4a16_pack": [P, I, I, P, P],
+        "w4a16_matmul": [P, P, P, P, P, I, I, I, I, P, S, P],
+        "q4b32_quantize": [P, I, I, P, P, P],
+        "q4b32_gemv": [P, P, P, P, I, I, P],
+        "w4a16_device_status": [P],
+        "w4a16_selftest_bounded_wait": [U32, P],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.w4a16_matmul_workspace_bytes.argtypes = [I, I, I, I]
+    lib.w4a16_matmul_workspace_bytes.restype = S
+    lib.w4a16_status_string.argtypes = [I]
+    lib.w4a16_status_string.restype = ctypes.c_char_p
+    for name in ("w4a16_testing_force_kernel", "w4a16_testing_set_gemv_max_m",
+                 "w4a16_testing_set_q4_variant"):
+        getattr(lib, name).argtypes = [I]
+        getattr(lib, name).restype = I
+    return lib
+
+
+_lib = _load()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _check(name: str, status: int):
+    if status != 0:
+        raise W4A16Error(name, status)
+
+
+def w4a16_quantize(w: torch.Tensor, group: int = 128, codes=None, scales=None, mins=None,
+                   stream=None):
+    """fp32 [N, K] -> (codes uint8 [N, K], scales bf16 [K/group, N], mins bf16 [K/group, N])."""
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((K // group, N), dtype=torch.bfloat16, device=w.device)
+    if mins is None:
+        mins = torch.empty((K // group, N), dtype=torch.bfloat16, device=w.device)
+    _check("w4a16_quantize", _lib.w4a16_quantize(
+        _dev(w, "w", torch.float32), N, K, group, _dev(codes, "codes", torch.uint8, (N, K)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)), _stream(stream)))
+    return codes, scales, mins
+
+
+def w4a16_pack(codes: torch.Tensor, qw=None, stream=None) -> torch.Tensor:
+    """uint8 codes [N, K] -> int32 [K/8, N]."""
+    N, K = codes.shape
+    if qw is None:
+        qw = torch.empty((K // 8, N), dtype=torch.int32, device=codes.device)
+    _check("w4a16_pack", _lib.w4a16_pack(_dev(codes, "codes", torch.uint8), N, K,
+                                         _dev(qw, "qw", torch.int32, (K // 8, N)),
+                                         _stream(stream)))
+    return qw
+
+
+def w4a16_matmul_workspace_bytes(M: int, N: int, K: int, group: int = 128) -> int:
+    return int(_lib.w4a16_matmul_workspace_bytes(M, N, K, group))
+
+
+def w4a16_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, mins: torch.Tensor,
+                 group: int = 128, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] (bf16) = x [M, K] (bf16) . w_hat^T."""
+    M, K = x.shape
+    N = qw.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("w4a16_matmul", _lib.w4a16_matmul(
+        _dev(x, "x", torch.bfloat16), _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)),
+        _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
+    return y
+
+
+def q4b32_quantize(w: torch.Tensor, codes=None, scales=None, stream=None):
+    """fp32 [N, K] -> (codes uint8 [N, K/2], scales fp16 [N, K/32])."""
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 32), dtype=torch.float16, device=w.device)
+    _check("q4b32_quantize", _lib.q4b32_quantize(
+        _dev(w, "w", torch.float32), N, K, _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.float16, (N, K // 32)), _stream(stream)))
+    return codes, scales
+
+
+def q4b32_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y=None,
+               stream=None) -> torch.Tensor:
+    """y [N] (fp16) = W_hat [N, K] . x [K] (fp16)."""
+    N = codes.shape[0]
+    K = codes.shape[1] * 2
+    if y is None:
+        y = torch.empty((N,), dtype=torch.float16, device=x.device)
+    _check("q4b32_gemv", _lib.q4b32_gemv(
+        _dev(x, "x", torch.float16, (K,)), _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.float16, (N, K // 32)), _dev(y, "y", torch.float16, (N,)),
+        N, K, _stream(stream)))
+    return y
+
+
+def w4a16_device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status (0 = OK, 5 = a wait expired)."""
+    return int(_lib.w4a16_device_status(_stream(stream)))
+
+
+def w4a16_selftest_bounded_wait(limit_us: int, stream=None) -> int:
+    return int(_lib.w4a16_selftest_bounded_wait(limit_us, _stream(stream)))
+
+
+def testing_force_kernel(kernel: int) -> int:
+    """0 = by M, 1/2 = CUDA-core GEMV (fp32x2 / mixed BF16 inner product), 3 = tcgen05."""
+    return int(_lib.w4a16_testing_force_kernel(kernel))
+
+
+def testing_set_gemv_max_m(m: int) -> int:
+    return int(_lib.w4a16_testing_set_gemv_max_m(m))
+
+
+def testing_set_q4_variant(v: int) -> int:
+    return int(_lib.w4a16_testing_set_q4_variant(v))

@@ -1,0 +1,179 @@
+// C ABI of the library: host-side argument validation, kernel choice by batch size and
+// the per-device status word. No entry point allocates memory.
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+#include "w4a16.h"
+#include "w4a16_testing.h"
+
+namespace {
+
+// Status word written by kernels that detect a failure themselves (an expired bounded
+// wait). One per device; read and cleared by w4a16_device_status.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_status_word for the current device (looked up once per device).
+uint32_t* status_word_ptr() {
+  static uint32_t* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+// Kernel choice for w4a16_matmul: 0 = by M (default), 1 = CUDA-core GEMV (fp32x2 inner
+// product), 2 = CUDA-core GEMV (mixed-precision inner product), 3 = tensor-core kernel.
+int g_force_kernel = 0;
+// M at or below which the CUDA-core GEMV runs when the choice is by M.
+int g_gemv_max_m = 4;
+
+uint64_t g_wait_limit_ns = w4k::kDefaultWaitLimitNs;
+
+}  // namespace
+
+extern "C" {
+
+const char* w4a16_status_string(w4a16_status status) {
+  switch (status) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG";
+    case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+    case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+    case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+    case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+  }
+  return "W4A16_ERR_UNKNOWN";
+}
+
+w4a16_status w4a16_quantize(const float* w, int N, int K, int group, uint8_t* codes,
+                            uint16_t* scales, uint16_t* mins, w4a16_stream_t stream) {
+  if (!w || !codes || !scales || !mins) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 128) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(mins))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w4a16_quantize(w, N, K, codes, scales, mins,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw, w4a16_stream_t stream) {
+  if (!codes || !qw) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 8 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(qw)) return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w4a16_pack(codes, N, K, reinterpret_cast<uint32_t*>(qw),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
+  (void)M;
+  (void)N;
+  (void)K;
+  (void)group;
+  return 0;
+}
+
+w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                          const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
+                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  if (!x || !qw || !scales || !mins || !y) return W4A16_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 128 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(mins) || !aligned16(y))
+    return W4A16_ERR_MISALIGNED;
+  if ((workspace == nullptr) != (workspace_bytes == 0)) return W4A16_ERR_WORKSPACE;
+  if (workspace != nullptr && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(qw);
+  int kernel = g_force_kernel;
+  if (kernel == 0) kernel = (M <= g_gemv_max_m) ? 1 : 3;
+  if (kernel == 1 || kernel == 2)
+    return from_cuda(w4k::launch_w4a16_gemv(x, q, scales, mins, y, M, N, K, kernel - 1, s));
+  uint32_t* status = status_word_ptr();
+  if (status == nullptr) return W4A16_ERR_CUDA;
+  const int bm = w4k::tc_block_m(M);
+  w4k::TcMaps maps;
+  cudaError_t e = w4k::make_tc_maps(x, q, scales, mins, M, N, K, bm, &maps);
+  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  return from_cuda(w4k::launch_w4a16_tc(maps, y, M, N, K, bm, status, g_wait_limit_ns, s));
+}
+
+w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                            w4a16_stream_t stream) {
+  if (!w || !codes || !scales) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales)) return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_q4b32_quantize(w, N, K, codes, scales,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int g_q4_variant = 0;
+
+w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                        uint16_t* y, int N, int K, w4a16_stream_t stream) {
+  if (!x || !codes || !scales || !y) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_q4b32_gemv(x, codes, scales, y, N, K, g_q4_variant,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_device_status(w4a16_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  uint32_t* p = status_word_ptr();
+  if (p == nullptr) return W4A16_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+  }
+  return (word & w4k::kStatusTimeout) ? W4A16_ERR_TIMEOUT : W4A16_OK;
+}
+
+w4a16_status w4a16_selftest_bounded_wait(uint32_t limit_us, w4a16_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return W4A16_ERR_INVALID_ARG;
+  uint32_t* p = status_word_ptr();
+  if (p == nullptr) return W4A16_ERR_CUDA;
+  return from_cuda(w4k::launch_bounded_wait_selftest(
+      p, static_cast<uint64_t>(limit_us) * 1000ull, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Test and benchmark hooks (declared in w4a16_testing.h, not part of the public header).
+int w4a16_testing_force_kernel(int kernel) {
+  if (kernel < 0 || kernel > 3) return -1;
+  const int prev = g_force_kernel;
+  g_force_kernel = kernel;
+  return prev;
+}
+
+int w4a16_testing_set_gemv_max_m(int m) {
+  const int prev = g_gemv_max_m;
+  if (m >= 0) g_gemv_max_m = m;
+  return prev;
+}
+
+int w4a16_testing_set_q4_variant(int v) {
+  const int prev = g_q4_variant;
+  if (v == 0 || v == 1) g_q4_variant = v;
+  return prev;
+}
+
+}  // extern "C"

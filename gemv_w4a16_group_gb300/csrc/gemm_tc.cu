@@ -1,0 +1,341 @@
+// W4A16 tensor-core kernel for sm_103a: TMA + tcgen05.mma with accumulators in tensor
+// memory (TMEM).
+//
+// What it computes is the pages' tile GEMM ("Low-Precision Kernels: INT4, INT8 and FP8
+// Matmuls, Measured", Step 2): per k-block, load packed words and this group's scale and
+// minimum, rebuild w_hat = q * s + min as BF16 in registers, multiply on BF16 tensor
+// cores with fp32 sums, store BF16. The BF16 weights never reach global memory.
+//
+// GB300 design (not the Triton kernel's):
+//   * Roles: warp 4 issues TMA loads (x tile, packed-word tile, scale and min rows) into
+//     a 4-stage shared-memory ring; warps 0-3 rebuild the weight tile and write it into
+//     TMEM with tcgen05.st (each warp owns the 32 TMEM lanes of its quadrant); warp 5
+//     issues tcgen05.mma from one thread; warps 0-3 then drain the accumulator.
+//   * The weight tile is the MMA's A operand straight from TMEM (128 weight columns =
+//     128 TMEM lanes, 16 k = 8 columns of BF16 pairs), so the dequantised tile costs no
+//     shared-memory bandwidth; x is the B operand (K-major, 128-byte swizzle) from
+//     shared memory. The accumulator is y^T: lane = weight column n, column = row m.
+//   * One MMA is 128 (n) x BM (m) x 16 (k); BM = 16..256 follows M, so small batches
+//     use a narrow tile rather than padding M to 128.
+//   * Every mbarrier wait is bounded; an expired wait latches a status bit, stops the
+//     pipeline, waits (bounded) for this CTA's copies and MMAs in flight, frees TMEM and
+//     returns.
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4k {
+namespace {
+
+constexpr int kBN = 128;  // weight columns per CTA (MMA M)
+constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row of BF16)
+constexpr int kStages = 4;
+constexpr int kDequantWarps = 4;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kPkBytes = kBK / 8 * kBN * 4;  // 8 rows x 128 words = 4 KB
+constexpr uint32_t kRowBytes = kBN * 2;           // one scale (or min) row = 256 B
+
+template <int BM>
+struct Smem {
+  static constexpr uint32_t x_bytes = BM * 128;
+  static constexpr uint32_t x_off = 0;
+  static constexpr uint32_t pk_off = x_off + kStages * x_bytes;
+  static constexpr uint32_t sc_off = pk_off + kStages * kPkBytes;
+  static constexpr uint32_t mn_off = sc_off + kStages * kRowBytes;
+  static constexpr uint32_t bar_off = mn_off + kStages * kRowBytes;
+  static constexpr uint32_t nbars = 3 * kStages + 2;  // full, empty, afull, accfull, drain
+  static constexpr uint32_t misc_off = bar_off + nbars * 8;
+  static constexpr uint32_t total = misc_off + 16;
+  static constexpr uint32_t alloc = total + 1024;  // slack to align the base to 1024 B
+  static constexpr uint32_t tx_bytes = x_bytes + kPkBytes + 2 * kRowBytes;
+  // TMEM: accumulator columns [0, BM), weight stages from a 32-column boundary after it;
+  // the allocation is a power of two.
+  static constexpr uint32_t a_col0 = BM < 32 ? 32u : static_cast<uint32_t>(BM);
+  static constexpr uint32_t tmem_cols = (a_col0 + kStages * 32 <= 256) ? 256u : 512u;
+  static_assert(a_col0 + kStages * 32 <= 512, "TMEM overflow");
+  static_assert(x_bytes % 1024 == 0, "x stage must keep 1024-byte alignment");
+};
+
+template <int BM>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_tc_kernel(const __grid_constant__ TcMaps maps, uint16_t* __restrict__ y, int M, int N,
+                    int K, uint32_t* __restrict__ status, uint64_t limit_ns) {
+  using L = Smem<BM>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sx = smem + L::x_off;
+  uint32_t* spk = reinterpret_cast<uint32_t*>(smem + L::pk_off);
+  uint16_t* ssc = reinterpret_cast<uint16_t*>(smem + L::sc_off);
+  uint16_t* smn = reinterpret_cast<uint16_t*>(smem + L::mn_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
+  uint64_t* full = bars;                 // TMA bytes landed (count 1 + tx)
+  uint64_t* empty = bars + kStages;      // MMAs reading the stage are done (commit)
+  uint64_t* afull = bars + 2 * kStages;  // weight stage written to TMEM (4 warps)
+  uint64_t* accfull = bars + 3 * kStages;
+  uint64_t* drain = bars + 3 * kStages + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * BM;
+  const int KB = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&afull[s], kDequantWarps);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_holder, L::tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&maps.x);
+    tma_prefetch_desc(&maps.qw);
+    tma_prefetch_desc(&maps.scales);
+    tma_prefetch_desc(&maps.mins);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1u;
+        if (kb >= kStages && !mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, status, limit_ns))
+          break;
+        mbar_arrive_expect_tx(&full[s], L::tx_bytes);
+        tma_load_2d(sx + s * L::x_bytes, &maps.x, &full[s], kb * kBK, m0);
+        tma_load_2d(spk + s * (kPkBytes / 4), &maps.qw, &full[s], n0, kb * (kBK / 8));
+        tma_load_2d(ssc + s * kBN, &maps.scales, &full[s], n0, kb / 2);
+        tma_load_2d(smn + s * kBN, &maps.mins, &full[s], n0, kb / 2);
+        ++issued;
+      }
+      if (*abort_flag) {
+        // Let this CTA's copies in flight land before the CTA can exit.
+        for (int s = 0; s < kStages && s < issued; ++s) {
+          const int last = issued - 1 - ((issued - 1 - s) % kStages);  // last fill of stage s
+          volatile uint32_t no_abort = 0u;
+          mbar_wait_bounded(&full[s], (last / kStages) & 1u, &no_abort, status, limit_ns);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBN, BM);
+      bool ok = true;
+      for (int kb = 0; kb < KB && ok; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1u;
+        ok = mbar_wait_bounded(&afull[s], ph, abort_flag, status, limit_ns) &&
+             mbar_wait_bounded(&full[s], ph, abort_flag, status, limit_ns);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t xs = smem_addr(sx + s * L::x_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          tc_mma_a_tmem(tmem, tmem + L::a_col0 + s * 32 + kk * 8,
+                        smem_desc_kmajor_sw128(xs + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+      }
+      if (ok) tc_commit(accfull);
+      // Whatever happened, wait until every MMA issued here has completed.
+      tc_commit(drain);
+      volatile uint32_t no_abort = 0u;
+      mbar_wait_bounded(drain, 0u, &no_abort, status, limit_ns);
+    }
+  } else if (warp < kDequantWarps) {
+    const int row = warp * 32 + lane;  // TMEM lane = weight column n0 + row
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t b128 = 0x43004300u;  // BF16 (128, 128)
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1u;
+      if (!mbar_wait_bounded(&full[s], ph, abort_flag, status, limit_ns)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sb = ssc[s * kBN + row], mb = smn[s * kBN + row];
+      const uint32_t s2u = sb | (sb << 16), m2u = mb | (mb << 16);
+      const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+      const __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&m2u);
+      const __nv_bfloat162 off = *reinterpret_cast<const __nv_bfloat162*>(&b128);
+      uint32_t out[32];
+#pragma unroll
+      for (int c = 0; c < kBK / 8; ++c) {
+        const uint32_t w = spk[s * (kPkBytes / 4) + c * kBN + row];
+        uint32_t p[4];
+        codes_to_bf16x2_consecutive(w, p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p[i]), off);
+          const __nv_bfloat162 wv = __hfma2(q2, s2, m2);  // q*s + min, one rounding
+          out[4 * c + i] = *reinterpret_cast<const uint32_t*>(&wv);
+        }
+      }
+      tmem_st_32cols(lane_base + L::a_col0 + s * 32, out);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);
+    }
+    // Epilogue: accumulator lane `row` holds y[m0 + j, n0 + row] in column j.
+    if (ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns)) {
+      tc_fence_after_sync();
+      const int n = n0 + row;
+#pragma unroll 1
+      for (int c = 0; c < BM / 32 || (BM < 32 && c == 0); ++c) {
+        uint32_t v[32];
+        if (BM >= 32) {
+          tmem_ld_32cols(lane_base + c * 32, v);
+        } else {
+          tmem_ld_32cols(lane_base, v);  // columns >= BM hold no rows; never stored
+        }
+        tmem_ld_wait();
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c * 32 + j;
+            if (j < BM && m < M)
+              y[static_cast<size_t>(m) * N + n] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::tmem_cols);
+  }
+}
+
+__global__ void bounded_wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the wait must give up after limit_ns.
+    mbar_wait_bounded(&bar, 0u, &abort_flag, status, limit_ns);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BM>
+cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint32_t* status,
+                      uint64_t limit_ns, cudaStream_t stream) {
+  using L = Smem<BM>;
+  auto kern = w4a16_tc_kernel<BM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L::alloc));
+  if (e != cudaSuccess) return e;
+  dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  kern<<<grid, kThreads, L::alloc, stream>>>(maps, y, M, N, K, status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_block_m(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
+                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps) {
+  cudaError_t e;
+  e = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
+                static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kBK,
+                static_cast<uint32_t>(bm), CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = encode_2d(&maps->qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
+                static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, kBN, kBK / 8,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  e = encode_2d(&maps->scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, static_cast<uint64_t>(N),
+                static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kBN, 1,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  return encode_2d(&maps->mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins, static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kBN, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
+                            uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  switch (bm) {
+    case 16: return launch_bm<16>(maps, y, M, N, K, status, limit_ns, stream);
+    case 32: return launch_bm<32>(maps, y, M, N, K, status, limit_ns, stream);
+    case 64: return launch_bm<64>(maps, y, M, N, K, status, limit_ns, stream);
+    case 128: return launch_bm<128>(maps, y, M, N, K, status, limit_ns, stream);
+    case 256: return launch_bm<256>(maps, y, M, N, K, status, limit_ns, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace w4k

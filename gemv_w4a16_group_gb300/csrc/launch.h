@@ -1,0 +1,54 @@
+// Internal interface between the C ABI layer (api.cu) and the kernel files. Each
+// launcher assumes its arguments were validated by the caller and returns the launch
+// error (cudaGetLastError) without synchronizing.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace w4k {
+
+// Bits of the per-device status word (read and cleared by w4a16_device_status).
+constexpr uint32_t kStatusTimeout = 1u;
+
+// Default limit of a bounded wait (nanoseconds of %globaltimer).
+constexpr uint64_t kDefaultWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+cudaError_t launch_w4a16_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                                  uint16_t* mins, cudaStream_t stream);
+cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
+                              cudaStream_t stream);
+cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                                  cudaStream_t stream);
+
+// CUDA-core GEMV for small M (dequantization in registers). `variant` selects the
+// inner product: 0 = packed fp32 FMA on offset codes, 1 = mixed BF16 x BF16 -> fp32 FMA.
+int gemv_max_rows();
+cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
+                              const uint16_t* mins, uint16_t* y, int M, int N, int K, int variant,
+                              cudaStream_t stream);
+
+// TMA + tcgen05 kernel: y^T tile = W_hat tile (tensor memory) x x^T tile (shared memory).
+struct TcMaps {
+  CUtensorMap x;       // bf16 [M, K], box {64, BM}, 128-byte swizzle
+  CUtensorMap qw;      // int32 [K/8, N], box {128, 8}
+  CUtensorMap scales;  // bf16 [K/128, N], box {128, 1}
+  CUtensorMap mins;    // bf16 [K/128, N], box {128, 1}
+};
+int tc_block_m(int M);
+cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
+                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps);
+cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
+                            uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
+
+// Q4 block-32 GEMV.
+cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                              uint16_t* y, int N, int K, int variant, cudaStream_t stream);
+
+// Bounded-wait self test: waits on a barrier nothing arrives at.
+cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace w4k

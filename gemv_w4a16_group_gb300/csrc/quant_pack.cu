@@ -1,0 +1,149 @@
+// Offline weight preparation on the GPU: group-128 asymmetric 4-bit quantization, packing
+// eight codes per int32 along K, and Q4 block-32 quantization.
+//
+// W4A16 format ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2):
+// each group of 128 consecutive weights along K gets scale = (max - min) / 15 and a
+// minimum, both stored as BF16; each weight becomes q = round((w - min) / scale) in
+// 0..15; eight codes are packed into one 32-bit word along K, giving a K/8 x N matrix.
+// Q4 format ("Why My 4-Bit CUDA Kernel Wasn't Faster"): 32 weights share one FP16
+// scale; 16 bytes of codes, low nibble = even weight, decode (q - 8) * s.
+//
+// Every step is an IEEE fp32 operation rounded to nearest even (__fsub_rn, __fdiv_rn,
+// rintf, __float2bfloat16_rn, __float2half_rn), so the GPU result is bit-identical to a
+// scalar fp32 reference taking the same steps. All three kernels are bound by HBM.
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4k {
+
+// One warp per (row n, group g) of 128 weights: 4 consecutive weights per lane.
+__global__ void __launch_bounds__(256)
+w4a16_quantize_kernel(const float* __restrict__ w, int N, int K, uint8_t* __restrict__ codes,
+                      uint16_t* __restrict__ scales, uint16_t* __restrict__ mins) {
+  const int groups = K >> 7;
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (gw >= static_cast<long long>(groups) * N) return;
+  const int lane = threadIdx.x & 31;
+  const int g = static_cast<int>(gw / N);
+  const int n = static_cast<int>(gw % N);  // consecutive warps: consecutive n, same g
+  const size_t off = static_cast<size_t>(n) * K + static_cast<size_t>(g) * 128 + lane * 4;
+  const float4 v = __ldcs(reinterpret_cast<const float4*>(w + off));
+  float lo = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
+  float hi = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const __nv_bfloat16 s_b = __float2bfloat16_rn(s32);
+  const __nv_bfloat16 m_b = __float2bfloat16_rn(lo);
+  const float s = __bfloat162float(s_b);
+  const float m = __bfloat162float(m_b);
+  auto code = [&](float x) -> uint32_t {
+    if (s == 0.0f) return 0u;
+    const float r = rintf(__fdiv_rn(__fsub_rn(x, m), s));
+    return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 15.0f));
+  };
+  const uint32_t packed = code(v.x) | (code(v.y) << 8) | (code(v.z) << 16) | (code(v.w) << 24);
+  *reinterpret_cast<uint32_t*>(codes + off) = packed;
+  if (lane == 0) {
+    scales[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(s_b);
+    mins[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(m_b);
+  }
+}
+
+// Pack: tile of 64 rows (n) x 64 words (r) through shared memory so that both the
+// byte reads along K and the word writes along N are coalesced.
+__global__ void __launch_bounds__(256)
+w4a16_pack_kernel(const uint8_t* __restrict__ codes, int N, int K, uint32_t* __restrict__ qw) {
+  __shared__ uint32_t tile[64][65];
+  const int R = K >> 3;
+  const int n0 = blockIdx.y * 64, r0 = blockIdx.x * 64;
+  const int tid = threadIdx.x;
+  {
+    const int rl = tid & 63;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int nl = (tid >> 6) + 4 * i;
+      const int n = n0 + nl, r = r0 + rl;
+      uint32_t word = 0;
+      if (n < N && r < R) {
+        const uint2 b = *reinterpret_cast<const uint2*>(codes + static_cast<size_t>(n) * K + 8 * r);
+        // byte j of the 8 holds code k = 8r + j; nibble j of the word
+        const uint32_t lo = b.x & 0x0F0F0F0Fu, hi = b.y & 0x0F0F0F0Fu;
+        // spread: codes 0..3 from lo bytes, 4..7 from hi bytes
+        word = (lo & 0xFu) | ((lo >> 4) & 0xF0u) | ((lo >> 8) & 0xF00u) | ((lo >> 12) & 0xF000u) |
+               ((hi & 0xFu) << 16) | ((hi << 12) & 0xF00000u) | ((hi << 8) & 0xF000000u) |
+               ((hi << 4) & 0xF0000000u);
+      }
+      tile[rl][nl] = word;
+    }
+  }
+  __syncthreads();
+  {
+    const int nl = tid & 63;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int rl = (tid >> 6) + 4 * i;
+      const int n = n0 + nl, r = r0 + rl;
+      if (n < N && r < R) qw[static_cast<size_t>(r) * N + n] = tile[rl][nl];
+    }
+  }
+}
+
+// Q4: 8 lanes per block of 32 weights, 4 weights per lane.
+__global__ void __launch_bounds__(256)
+q4b32_quantize_kernel(const float* __restrict__ w, int N, int K, uint8_t* __restrict__ codes,
+                      uint16_t* __restrict__ scales) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(N) * (K >> 2);  // float4 units
+  const bool ok = i < total;
+  const long long e = ok ? i * 4 : 0;  // element index n*K + k
+  const float4 v = ok ? __ldcs(reinterpret_cast<const float4*>(w + e)) : make_float4(0, 0, 0, 0);
+  float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const __half s_h = __float2half_rn(__fdiv_rn(a, 8.0f));
+  const float s = __half2float(s_h);
+  auto code = [&](float x) -> uint32_t {
+    if (s == 0.0f) return 8u;
+    const float r = rintf(__fdiv_rn(x, s)) + 8.0f;
+    return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 15.0f));
+  };
+  if (!ok) return;
+  const uint32_t b0 = code(v.x) | (code(v.y) << 4);
+  const uint32_t b1 = code(v.z) | (code(v.w) << 4);
+  *reinterpret_cast<uint16_t*>(codes + e / 2) = static_cast<uint16_t>(b0 | (b1 << 8));
+  if ((threadIdx.x & 7) == 0) scales[e / 32] = __half_as_ushort(s_h);
+}
+
+cudaError_t launch_w4a16_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                                  uint16_t* mins, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(K >> 7) * N;
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  w4a16_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, codes, scales,
+                                                                            mins);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
+                              cudaStream_t stream) {
+  const int R = K >> 3;
+  dim3 grid((R + 63) / 64, (N + 63) / 64);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  w4a16_pack_kernel<<<grid, 256, 0, stream>>>(codes, N, K, qw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                                  cudaStream_t stream) {
+  const long long total = static_cast<long long>(N) * (K >> 2);
+  const long long blocks = (total + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  q4b32_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, codes, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace w4k

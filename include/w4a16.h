@@ -1,0 +1,153 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 group-quantized matmul library.
+ *
+ * What it computes
+ *   y = x . W_hat^T with x BF16 [M, K] activations and W_hat [N, K] rebuilt from
+ *   4-bit codes as w_hat = q * s + min, one BF16 scale s = (max - min) / 15 and one
+ *   BF16 minimum per group of 128 weights along K (4.25 bits per weight); eight codes
+ *   are packed per int32 along K into a K/8 x N matrix ("Low-Precision Kernels: INT4,
+ *   INT8 and FP8 Matmuls, Measured", Step 2). A second format is the 18-byte Q4 block
+ *   of 32 codes plus an FP16 scale, w_hat = (q - 8) * s ("Why My 4-Bit CUDA Kernel
+ *   Wasn't Faster", "Why fewer bytes should have helped").
+ *
+ * Conventions shared by every entry point
+ *   - Every array pointer is DEVICE memory owned by the caller. The library keeps no
+ *     pointer after a call returns and allocates nothing per call.
+ *   - BF16 and FP16 arrays are passed as uint16_t bit patterns.
+ *   - Every array is dense row-major (C order) with the shape given below; base
+ *     pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Arguments are validated on the host before anything is launched; a
+ *     call that returns an error status launched nothing.
+ *   - W4A16_ERR_CUDA means a CUDA runtime call failed (the sticky or launch error is
+ *     not cleared). Device-side faults the kernels detect themselves (a bounded wait
+ *     that expired) are latched in a per-device status word that
+ *     w4a16_device_status() reads and clears.
+ *   - Weights must be finite.
+ */
+#ifndef W4A16_GB300_H
+#define W4A16_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* w4a16_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1, /* null pointer, non-positive or inconsistent size */
+  W4A16_ERR_UNSUPPORTED = 2, /* valid for the format but not by these kernels    */
+  W4A16_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned                */
+  W4A16_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
+  W4A16_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (device status) */
+  W4A16_ERR_WORKSPACE = 6    /* workspace pointer/size does not meet the query  */
+} w4a16_status;
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* w4a16_status_string(w4a16_status status);
+
+/*
+ * w4a16_quantize -- fp32 weights to 4-bit codes with a BF16 scale and minimum per
+ * group ("Low-Precision Kernels ...", Step 2: "each group of 128 consecutive weights
+ * along the input dimension K gets scale = (max - min) / 15, and each weight becomes
+ * an integer q = round((w - min) / scale) from 0 to 15").
+ *   w      fp32 [N, K]        (one output feature per row, K contiguous)
+ *   codes  uint8 [N, K]       (one code 0..15 per byte)
+ *   scales bf16 [K/group, N]  s = bf16_rne(fp32(max - min) / 15)
+ *   mins   bf16 [K/group, N]  min = bf16_rne(min)
+ * Per weight: q = clamp(rint((w - min_bf16) / s_bf16), 0, 15) in fp32 with
+ * round-half-to-even; a group whose BF16 scale is 0 stores q = 0.
+ * Requires N > 0, K > 0, group == 128, K % group == 0.
+ */
+w4a16_status w4a16_quantize(const float* w, int N, int K, int group, uint8_t* codes,
+                            uint16_t* scales, uint16_t* mins, w4a16_stream_t stream);
+
+/*
+ * w4a16_pack -- eight codes per int32 along K ("Low-Precision Kernels ...", Step 2:
+ * "an N x K weight becomes a K/8 x N packed matrix"; its listing: "row 8r + j =
+ * nibble j of word r"; "Quantization and GEMV": first element in the low 4 bits).
+ *   codes uint8 [N, K] (values 0..15; higher bits are ignored)
+ *   qw    int32 [K/8, N]: word (r, n) = sum_j codes[n, 8r + j] << 4j
+ * Requires N > 0, K > 0, K % 8 == 0.
+ */
+w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw,
+                        w4a16_stream_t stream);
+
+/*
+ * w4a16_matmul -- y = x . W_hat^T with w_hat[n, k] = q * s + min rebuilt in registers
+ * ("Low-Precision Kernels ...", Step 2 and "Where the time goes at M = 1").
+ *   x      bf16 [M, K]
+ *   qw     int32 [K/8, N]  (as written by w4a16_pack)
+ *   scales bf16 [K/group, N], mins bf16 [K/group, N]
+ *   y      bf16 [M, N]     (fp32 accumulation, rounded to nearest even)
+ * Kernel choice is by M: a CUDA-core GEMV for small M, a TMA + tcgen05 tensor-core
+ * kernel otherwise. Accuracy: |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k|
+ * per output, y_ref the exact product on the same 4-bit weights. Results are
+ * deterministic (no floating-point atomics).
+ *   workspace / workspace_bytes: optional caller-owned device scratch that lets small-N
+ *   shapes split K across thread blocks; size it with w4a16_matmul_workspace_bytes().
+ *   NULL (with 0 bytes) is always accepted. The workspace must be zero-filled before
+ *   its first use and not shared by calls that may run concurrently; the kernels
+ *   leave it zeroed again when they finish.
+ * Requires M > 0, N > 0, K > 0, group == 128, K % group == 0, N % 8 == 0.
+ */
+w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                          const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
+                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
+/* Bytes of workspace that let w4a16_matmul split K for this shape (0 = no benefit). */
+size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);
+
+/*
+ * q4b32_quantize -- fp32 weights to Q4 blocks of 32 ("Why My 4-Bit CUDA Kernel Wasn't
+ * Faster": 16 bytes of codes plus a 2-byte scale the 32 weights share).
+ *   w      fp32 [N, K]
+ *   codes  uint8 [N, K/2]  byte j of block b holds weight 32b+2j in its low nibble
+ *                          and weight 32b+2j+1 in its high nibble
+ *   scales fp16 [N, K/32]  s = fp16_rne(fp32(max|w| / 8))
+ * Per weight: q = clamp(rint(w / s) + 8, 0, 15) (round-half-to-even); a block whose
+ * FP16 scale is 0 stores q = 8. Requires N > 0, K > 0, K % 32 == 0.
+ */
+w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
+                            w4a16_stream_t stream);
+
+/*
+ * q4b32_gemv -- y[n] = sum_b s[n, b] * sum_j (q[n, b, j] - 8) * x[32 b + j]
+ * ("Why My 4-Bit CUDA Kernel Wasn't Faster": pull the code, subtract the bias,
+ * multiply by the scale; codes and scales in separate arrays).
+ *   x fp16 [K]; codes uint8 [N, K/2]; scales fp16 [N, K/32]; y fp16 [N]
+ * fp32 accumulation, y rounded to nearest even; the same tolerance as w4a16_matmul.
+ * Requires N > 0, K > 0, K % 32 == 0.
+ */
+w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                        uint16_t* y, int N, int K, w4a16_stream_t stream);
+
+/*
+ * w4a16_device_status -- synchronizes `stream`, then reads and clears the current
+ * device's status word. Returns W4A16_ERR_TIMEOUT if any kernel of this library gave
+ * up a bounded wait since the last query, W4A16_ERR_CUDA if the synchronization
+ * failed, W4A16_OK otherwise. (The pages have no counterpart; this is the library's
+ * failure-detection hook.)
+ */
+w4a16_status w4a16_device_status(w4a16_stream_t stream);
+
+/*
+ * w4a16_selftest_bounded_wait -- launches one tiny kernel that waits on a shared-memory
+ * barrier nothing ever arrives at, with the same bounded-wait helper the tensor-core
+ * kernel uses, limited to `limit_us` microseconds (1..1000000). The kernel then
+ * records the expiry in the status word and returns, so a correct build makes the
+ * following w4a16_device_status() return W4A16_ERR_TIMEOUT. It holds no tensor
+ * memory and issues no copies. (No counterpart on the pages: a failure-detection
+ * test hook.)
+ */
+w4a16_status w4a16_selftest_bounded_wait(uint32_t limit_us, w4a16_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_GB300_H */

@@ -1,0 +1,35 @@
+/*
+ * w4a16_testing.h -- test and benchmark hooks of the GB300 W4A16 library.
+ *
+ * Not part of the stable API (w4a16.h). They change process-global choices that
+ * w4a16_matmul and q4b32_gemv read on the host before each launch, so they must not be
+ * called while another host thread is issuing those calls. The pages have no
+ * counterpart: they exist so that tests can check every kernel at every shape and the
+ * benchmark can compare the kernels.
+ */
+#ifndef W4A16_GB300_TESTING_H
+#define W4A16_GB300_TESTING_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Kernel w4a16_matmul uses: 0 = chosen by M (default), 1 = CUDA-core GEMV with the
+ * packed fp32 inner product, 2 = CUDA-core GEMV with the mixed BF16 inner product,
+ * 3 = TMA + tcgen05 tensor-core kernel. Returns the previous choice, or -1 if `kernel`
+ * is out of range (nothing changes then). */
+int w4a16_testing_force_kernel(int kernel);
+
+/* Largest M that the by-M choice sends to the CUDA-core GEMV (default 4). A negative
+ * value only queries. Returns the previous value. */
+int w4a16_testing_set_gemv_max_m(int m);
+
+/* Inner product of q4b32_gemv: 0 = packed fp32 (default), 1 = mixed FP16. Other values
+ * only query. Returns the previous value. */
+int w4a16_testing_set_q4_variant(int v);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_GB300_TESTING_H */

@@ -1,0 +1,111 @@
+"""The C-ABI library without a GPU: it loads, exports every function the public headers
+declare, and rejects invalid arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("w4a16.h", "w4a16_testing.h")]
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, TIMEOUT, WORKSPACE = range(7)
+A = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+B = 0x20000
+
+
+def _declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(\w+)\s*\([^;]*\)\s*;", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib(cuda_lib):
+    lib = ctypes.CDLL(cuda_lib)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4a16_matmul.argtypes = [P, P, P, P, P, I, I, I, I, P, S, P]
+    lib.w4a16_quantize.argtypes = [P, I, I, I, P, P, P, P]
+    lib.w4a16_pack.argtypes = [P, I, I, P, P]
+    lib.q4b32_quantize.argtypes = [P, I, I, P, P, P]
+    lib.q4b32_gemv.argtypes = [P, P, P, P, I, I, P]
+    lib.w4a16_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
+    lib.w4a16_status_string.argtypes = [I]
+    lib.w4a16_status_string.restype = ctypes.c_char_p
+    lib.w4a16_matmul_workspace_bytes.argtypes = [I, I, I, I]
+    lib.w4a16_matmul_workspace_bytes.restype = S
+    return lib
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("w4a16_quantize", "w4a16_pack", "w4a16_matmul", "q4b32_gemv",
+                     "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
+                     "w4a16_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["W4A16_OK", "W4A16_ERR_INVALID_ARG", "W4A16_ERR_UNSUPPORTED",
+                                 "W4A16_ERR_MISALIGNED", "W4A16_ERR_CUDA", "W4A16_ERR_TIMEOUT",
+                                 "W4A16_ERR_WORKSPACE"]):
+        assert lib.w4a16_status_string(code).decode() == name
+    assert lib.w4a16_status_string(99).decode() == "W4A16_ERR_UNKNOWN"
+
+
+def test_matmul_rejects_bad_arguments_on_host(lib):
+    m = lib.w4a16_matmul
+    good = (A, A, A, A, B)
+    assert m(None, A, A, A, B, 1, 256, 512, 128, None, 0, None) == INVALID
+    assert m(*good, 0, 256, 512, 128, None, 0, None) == INVALID          # M = 0
+    assert m(*good, 1, 0, 512, 128, None, 0, None) == INVALID            # N = 0
+    assert m(*good, 1, 256, -128, 128, None, 0, None) == INVALID         # K < 0
+    assert m(*good, 1, 256, 500, 128, None, 0, None) == INVALID          # K % group
+    assert m(*good, 1, 256, 512, 64, None, 0, None) == UNSUPPORTED       # group 64
+    assert m(*good, 1, 260, 512, 128, None, 0, None) == UNSUPPORTED      # N % 8
+    assert m(A + 2, A, A, A, B, 1, 256, 512, 128, None, 0, None) == MISALIGNED
+    assert m(A, A, A, A, B + 8, 1, 256, 512, 128, None, 0, None) == MISALIGNED
+    assert m(*good, 1, 256, 512, 128, A, 0, None) == WORKSPACE           # ptr without size
+    assert m(*good, 1, 256, 512, 128, None, 64, None) == WORKSPACE       # size without ptr
+    assert m(*good, 1, 256, 512, 128, A + 4, 64, None) == MISALIGNED
+
+
+def test_quantize_pack_q4_reject_bad_arguments_on_host(lib):
+    assert lib.w4a16_quantize(A, 4, 256, 128, None, A, A, None) == INVALID
+    assert lib.w4a16_quantize(A, 4, 250, 128, A, A, A, None) == INVALID
+    assert lib.w4a16_quantize(A, 4, 256, 32, A, A, A, None) == UNSUPPORTED
+    assert lib.w4a16_quantize(A + 4, 4, 256, 128, A, A, A, None) == MISALIGNED
+    assert lib.w4a16_pack(A, 4, 12, A, None) == INVALID
+    assert lib.w4a16_pack(A, 0, 16, A, None) == INVALID
+    assert lib.w4a16_pack(A + 1, 4, 16, A, None) == MISALIGNED
+    assert lib.q4b32_quantize(A, 4, 48, A, A, None) == INVALID
+    assert lib.q4b32_quantize(A, 4, 64, A, A + 2, None) == MISALIGNED
+    assert lib.q4b32_gemv(A, A, A, None, 4, 64, None) == INVALID
+    assert lib.q4b32_gemv(A, A, A, B, 4, 40, None) == INVALID
+    assert lib.q4b32_gemv(A, A, A + 8, B, 4, 64, None) == MISALIGNED
+    assert lib.w4a16_selftest_bounded_wait(0, None) == INVALID
+    assert lib.w4a16_selftest_bounded_wait(2_000_000, None) == INVALID
+
+
+def test_workspace_query_is_host_only(lib):
+    assert lib.w4a16_matmul_workspace_bytes(1, 14336, 4096, 128) >= 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+
+    import gemv_w4a16_group_gb300 as w4
+
+    x = torch.zeros(1, 256, dtype=torch.bfloat16)
+    qw = torch.zeros(32, 64, dtype=torch.int32)
+    s = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        w4.w4a16_matmul(x, qw, s, s)

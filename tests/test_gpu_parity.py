@@ -1,0 +1,285 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on seeded inputs.
+
+Quantize and pack must match bit for bit; matmul and Q4 outputs must satisfy
+|y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k| per output. Full-size launches are
+checked on every output where the oracle is fast enough, else on sampled columns.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+GEMV_F32X2, GEMV_MIXED, TCGEN05 = 1, 2, 3
+KERNELS = {"gemv_f32x2": GEMV_F32X2, "gemv_mixed": GEMV_MIXED, "tcgen05": TCGEN05}
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemv_w4a16_group_gb300 as mod
+
+    return mod
+
+
+@pytest.fixture
+def force_kernel(w4):
+    prev = []
+
+    def set_kernel(k):
+        prev.append(w4.testing_force_kernel(k))
+
+    yield set_kernel
+    w4.testing_force_kernel(0)
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def quantized(N, K, seed=0, outliers=0.0):
+    """CPU weights and their oracle quantization, packed."""
+    w = workloads.weights(N, K, seed=seed, outlier_frac=outliers)
+    codes, s, m = oracle.w4a16_quantize(w.numpy())
+    return w, codes, s, m, oracle.w4a16_pack(codes)
+
+
+def to_dev_params(codes, s, m, qw):
+    dev = "cuda"
+    return (torch.from_numpy(qw).to(dev),
+            torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(dev),
+            torch.from_numpy(m.view(np.int16)).view(torch.bfloat16).to(dev))
+
+
+def check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m, cols=None):
+    y = w4.w4a16_matmul(x.cuda(), qw, s, m)
+    torch.cuda.synchronize()
+    yv = y.float().cpu().numpy()
+    y_ref, a_ref = oracle.w4a16_matmul(bits(x), qw_np, s_np, m_np, cols=cols)
+    if cols is not None:
+        yv = yv[:, cols]
+    ok = oracle.within_tolerance(yv, y_ref, a_ref)
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        detail = [(int(i), int(j), float(yv[i, j]), float(y_ref[i, j])) for i, j in bad]
+        raise AssertionError(f"{int((~ok).sum())}/{ok.size} outputs out of tolerance: {detail}")
+    return y
+
+
+# --------------------------------------------------------------------------- #
+# quantize / pack: bit-exact
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("N,K,outliers", [(256, 512, 0.0), (72, 384, 0.0), (1000, 1280, 0.001),
+                                          (14336, 4096, 0.0), (14336, 4096, 0.001)])
+def test_quantize_pack_bit_exact(w4, N, K, outliers):
+    w, codes, s, m, qw = quantized(N, K, seed=N + K, outliers=outliers)
+    gc, gs, gm = w4.w4a16_quantize(w.cuda())
+    gq = w4.w4a16_pack(gc)
+    torch.cuda.synchronize()
+    assert np.array_equal(gc.cpu().numpy(), codes)
+    assert np.array_equal(bits(gs), s)
+    assert np.array_equal(bits(gm), m)
+    assert np.array_equal(gq.cpu().numpy(), qw)
+
+
+def test_quantize_on_grid_and_degenerate_groups(w4):
+    """Constant groups (scale 0), on-grid groups and exact ties, bit-exact."""
+    N, K = 16, 512
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[0, :128] = 0.3                      # constant group -> scale 0, q = 0
+    w[1, 128:256] = -1.5                  # constant negative
+    q = rng.integers(0, 16, size=128)
+    q[0], q[1] = 0, 15
+    w[2, 256:384] = (-0.75 + 0.25 * q).astype(np.float32)           # on the grid
+    w[3, 384:512] = (-0.75 + 0.25 * (q + 0.5)).astype(np.float32)   # exact ties
+    w[3, 384], w[3, 385] = -0.75, 3.0
+    codes, s, m = oracle.w4a16_quantize(w)
+    gc, gs, gm = w4.w4a16_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(gc.cpu().numpy(), codes)
+    assert np.array_equal(bits(gs), s) and np.array_equal(bits(gm), m)
+
+
+@pytest.mark.parametrize("N,K", [(8, 8), (64, 512), (100, 520), (333, 1024), (4096, 4104)])
+def test_pack_bit_exact_with_high_bits(w4, N, K):
+    rng = np.random.default_rng(N)
+    codes = rng.integers(0, 256, size=(N, K), dtype=np.uint8)  # high nibble must be ignored
+    ref = oracle.w4a16_pack(codes)
+    got = w4.w4a16_pack(torch.from_numpy(codes).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+# --------------------------------------------------------------------------- #
+# matmul: tolerance, every kernel
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (1, 8, 128), (2, 264, 384), (3, 136, 1536),
+                                   (4, 1536, 1536), (5, 256, 640), (8, 520, 256),
+                                   (13, 256, 512), (16, 384, 1024), (17, 256, 512),
+                                   (32, 640, 768), (64, 256, 1536), (100, 392, 512),
+                                   (128, 256, 512), (200, 264, 640), (256, 384, 384),
+                                   (300, 256, 256)])
+def test_matmul_small_shapes(w4, force_kernel, kernel, M, N, K):
+    if kernel != "tcgen05" and M > 64:
+        pytest.skip("CUDA-core GEMV is only meant for small M")
+    force_kernel(KERNELS[kernel])
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=M * 7 + N)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(M, K, seed=M + K)
+    check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096])
+def test_batch_sweep_full_size(w4, M):
+    """Llama-3-8B up-projection shape with 0.1 % outliers x10, automatic kernel choice;
+    every column at M <= 16, sampled columns above."""
+    cfg = workloads.BATCH_SWEEP
+    N, K = cfg["N"], cfg["K"]
+    w, codes, s_np, m_np, qw_np = _sweep_weights()
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(M, K, seed=M)
+    cols = None if M <= 16 else workloads.sample_indices(N, 48 if M <= 256 else 12, seed=M).numpy()
+    check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m, cols=cols)
+
+
+_SWEEP = {}
+
+
+def _sweep_weights():
+    if "w" not in _SWEEP:
+        cfg = workloads.BATCH_SWEEP
+        _SWEEP["w"] = quantized(cfg["N"], cfg["K"], seed=0, outliers=cfg["outlier_frac"])
+    return _SWEEP["w"]
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_llama_up_proj_m1_every_output(w4, force_kernel, kernel):
+    cfg = workloads.LLAMA_UP
+    force_kernel(KERNELS[kernel])
+    w, codes, s_np, m_np, qw_np = quantized(cfg["N"], cfg["K"], seed=0)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(1, cfg["K"], seed=0)
+    check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m)
+
+
+@pytest.mark.parametrize("name,N,K", [(n, N, K) for n, N, K in workloads.QWEN_BLOCK])
+def test_qwen_stack_shapes_m1(w4, name, N, K):
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=hash(name) % 1000)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(1, K, seed=K)
+    check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m)
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_matmul_special_inputs(w4, force_kernel, kernel):
+    """x = 0 gives exactly 0; one-hot x gives w_hat[n, k] to BF16 rounding; constant
+    groups; deterministic results (same bits twice)."""
+    force_kernel(KERNELS[kernel])
+    N, K = 256, 512
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=5)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x0 = torch.zeros(3, K, dtype=torch.bfloat16)
+    y0 = w4.w4a16_matmul(x0.cuda(), qw, s, m)
+    assert torch.count_nonzero(y0).item() == 0
+    w_hat = oracle.w4a16_dequant(qw_np, s_np, m_np)
+    for k in (0, 127, 128, 511):
+        x1 = torch.zeros(1, K, dtype=torch.bfloat16)
+        x1[0, k] = 1.0
+        y1 = w4.w4a16_matmul(x1.cuda(), qw, s, m).float().cpu().numpy()[0]
+        ref = w_hat[:, k]
+        assert np.all(np.abs(y1 - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30), k
+    x = workloads.activations_bf16(4, K, seed=9).cuda()
+    a = w4.w4a16_matmul(x, qw, s, m)
+    b = w4.w4a16_matmul(x, qw, s, m)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_matmul_guard_bands(w4, force_kernel, kernel):
+    """The kernels write exactly y[M, N]: sentinels around it stay untouched."""
+    force_kernel(KERNELS[kernel])
+    M, N, K = 3, 264, 384
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=11)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345, dtype=torch.int16, device="cuda")
+    y = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    x = workloads.activations_bf16(M, K, seed=1)
+    w4.w4a16_matmul(x.cuda(), qw, s, m, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345)
+    y_ref, a_ref = oracle.w4a16_matmul(bits(x), qw_np, s_np, m_np)
+    assert oracle.within_tolerance(y.float().cpu().numpy(), y_ref, a_ref).all()
+
+
+def test_matmul_rejects_misaligned_views(w4):
+    N, K = 256, 512
+    w, codes, s_np, m_np, qw_np = quantized(N, K)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    xbuf = torch.zeros(K + 1, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(w4.W4A16Error, match="MISALIGNED"):
+        w4.w4a16_matmul(xbuf[1:].view(1, K), qw, s, m)
+
+
+# --------------------------------------------------------------------------- #
+# Q4 block-32
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("N,K", [(256, 512), (8, 32), (13, 96), (1000, 1056), (4096, 4096)])
+def test_q4_quantize_and_gemv(w4, variant, N, K):
+    prev = w4.testing_set_q4_variant(variant)
+    try:
+        w = workloads.weights(N, K, seed=N)
+        codes, sc = oracle.q4b32_quantize(w.numpy())
+        gc, gs = w4.q4b32_quantize(w.cuda())
+        torch.cuda.synchronize()
+        assert np.array_equal(gc.cpu().numpy(), codes)
+        assert np.array_equal(bits(gs), sc)
+        x = workloads.activations_fp16(K, seed=K)
+        y = w4.q4b32_gemv(x.cuda(), gc, gs).float().cpu().numpy()
+        y_ref, a_ref = oracle.q4b32_gemv(bits(x), codes, sc)
+        ok = oracle.within_tolerance(y, y_ref, a_ref)
+        assert ok.all(), int((~ok).sum())
+    finally:
+        w4.testing_set_q4_variant(prev)
+
+
+def test_q4_square_full_size(w4):
+    cfg = workloads.Q4_SQUARE
+    N, K = cfg["N"], cfg["K"]
+    w = workloads.weights(N, K, seed=0)
+    codes, sc = oracle.q4b32_quantize(w.numpy())
+    gc, gs = w4.q4b32_quantize(w.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(gc.cpu().numpy(), codes)
+    assert np.array_equal(bits(gs), sc)
+    del w
+    x = workloads.activations_fp16(K, seed=0)
+    y = w4.q4b32_gemv(x.cuda(), gc, gs).float().cpu().numpy()
+    rows = workloads.sample_indices(N, 2048, seed=1).numpy()
+    y_ref, a_ref = oracle.q4b32_gemv(bits(x), codes, sc, rows=rows)
+    assert oracle.within_tolerance(y[rows], y_ref, a_ref).all()
+
+
+# --------------------------------------------------------------------------- #
+# failure detection without a fault
+# --------------------------------------------------------------------------- #
+
+def test_bounded_wait_expires_and_is_reported(w4):
+    assert w4.w4a16_device_status() == 0
+    assert w4.w4a16_selftest_bounded_wait(2000) == 0
+    assert w4.w4a16_device_status() == 5  # W4A16_ERR_TIMEOUT, then cleared
+    assert w4.w4a16_device_status() == 0
+    # the context is still usable
+    z = torch.ones(4, device="cuda") * 2
+    assert z.sum().item() == 8.0
