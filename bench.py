@@ -1,0 +1,575 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 group-quantized matmul on GB300.
+
+Headline (one JSON line on stdout): the decode GEMV of the Llama-3-8B MLP up-projection
+(M = 1, N = 14336, K = 4096, group 128) -- a step is one ``w4a16_matmul`` launch on
+weights already resident in HBM. Throughput is the effective HBM bandwidth on weight +
+scale bytes (the pages' "effective GB/s": format bytes / time), timed with CUDA events
+around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than twice the
+129 MB L2), so no launch finds its weights in L2.
+
+The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
+the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
+quantize and GEMV (16384 x 16384), and the 196-matmul Qwen2.5-1.5B-shaped decode stack in
+one CUDA graph; each with its roofline fraction.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+
+With --impl reference the CPU oracle is timed instead (bounded samples of the same
+workload, same metric). Under torchrun each rank runs an independent replica on its own
+GPU (the GEMV does not shard); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "W4A16 µs & effective HBM GB/s at M=1; TFLOPS vs M=1..4096; % of roofline"
+PAGES_M1_GBPS = 169.0  # the pages' M=1 effective bandwidth for this shape (RTX 4060 Laptop)
+ROTATE = 12            # weight copies in rotation (12 x 31.2 MB > 2 x L2)
+GRAPH_LEN = 96         # launches per captured graph in the timed loop
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing (replicas only)
+# --------------------------------------------------------------------------- #
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- #
+# peaks, clocks
+# --------------------------------------------------------------------------- #
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- #
+# timing helpers
+# --------------------------------------------------------------------------- #
+
+def capture(fn, count: int, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(count):
+            fn(i)
+    return g
+
+
+def graph_time_us(fn, launches: int, reps: int, stream) -> float:
+    """Average device time per launch of fn(i), i = 0..launches-1 captured once and
+    replayed `reps` times (CUDA events on the capture stream)."""
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i)
+    torch.cuda.synchronize()
+    g = capture(fn, launches, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) * 1e3 / (launches * reps)
+
+
+def w4a16_bytes(M, N, K, group=128):
+    """Algorithmic bytes of one matmul: packed codes + BF16 scale/min + x + y."""
+    return N * K // 2 + 4 * N * (K // group) + 2 * M * K + 2 * M * N
+
+
+def weight_bytes(N, K, group=128):
+    return N * K // 2 + 4 * N * (K // group)
+
+
+def roofline_us(bytes_, flops, peaks):
+    return max(bytes_ / (peaks["hbm_gbs"] * 1e3), flops / (peaks["bf16_tflops"] * 1e6))
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+
+def workspace_for(M, N, K, device):
+    """The split-K workspace the library asks for at this shape (zero-filled), or None."""
+    import gemv_w4a16_group_gb300 as w4
+
+    need = w4.w4a16_matmul_workspace_bytes(M, N, K)
+    return torch.zeros(need, dtype=torch.uint8, device=device) if need else None
+
+
+def quantized_on_device(N, K, seed, device, outlier_frac=0.0):
+    import gemv_w4a16_group_gb300 as w4
+
+    w = workloads.weights(N, K, seed=seed, outlier_frac=outlier_frac).to(device)
+    codes, s, m = w4.w4a16_quantize(w)
+    qw = w4.w4a16_pack(codes)
+    return w, codes, qw, s, m
+
+
+def run_ours(args, world, rank, local):
+    import gemv_w4a16_group_gb300 as w4
+
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    peaks, peaks_src = load_peaks()
+    stream = torch.cuda.Stream(device)
+    cfg = workloads.LLAMA_UP
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+
+    w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
+    del w, codes
+    copies = [(qw.clone(), s.clone(), m.clone()) for _ in range(ROTATE)]
+    x = workloads.activations_bf16(M, K, seed=0).to(device)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    bytes_w = weight_bytes(N, K)
+
+    ws = workspace_for(M, N, K, device)
+
+    def step(i):
+        c = copies[i % ROTATE]
+        w4.w4a16_matmul(x, c[0], c[1], c[2], y=y, workspace=ws)
+
+    # warm-up: W untimed steps, then capture the timed loop
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    glen = min(GRAPH_LEN, args.steps)
+    g_main = capture(step, glen, stream)
+    tail = args.steps % glen
+    g_tail = capture(step, tail, stream) if tail else None
+    with torch.cuda.stream(stream):
+        g_main.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        ev0.record(stream)
+        for _ in range(args.steps // glen):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    local_s = ev0.elapsed_time(ev1) / 1e3
+    max_s = reduce_max(local_s, world, device)
+    clocks = sampler.summary()
+    us_per_step = local_s / args.steps * 1e6
+
+    result = None
+    if rank == 0:
+        value = world * bytes_w * args.steps / max_s / 1e9
+        achieved = bytes_w / (us_per_step * 1e3)
+        traffic = read_traffic("gemv_w4a16_kernel", w4a16_bytes(M, N, K))
+        result = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(max_s / args.steps * 1e3, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": round(value / world / PAGES_M1_GBPS, 2),
+            "vs_baseline_ref": "169 GB/s at M=1 on this shape, RTX 4060 Laptop (pages)",
+            "dtype": "bf16", "accumulate": "fp32", "weights": "int4 group-128 (4.25 bit)",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) BF16 x)",
+            "config": {"workload": cfg["name"], "M": M, "N": N, "K": K, "group": cfg["group"],
+                       "l2": f"rotating {ROTATE} weight copies ({ROTATE * bytes_w / 1e6:.0f} MB "
+                             "> 2x L2), CUDA-graph replay",
+                       "us_per_step": round(us_per_step, 3), "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": traffic, "peak_source": f"{peaks_src} copy bandwidth",
+                         "algorithmic_bytes_per_launch": bytes_w},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        result["e2e"] = e2e_ours(copies, x, y, M, N, K, device, stream)
+    del copies
+    if rank == 0 and world == 1 and not args.no_rows:
+        result["rows"] = rows_ours(peaks, device, stream)
+    if rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    barrier(world)
+    return result
+
+
+def kernel_source_digest(files) -> str:
+    """sha256 over the CUDA sources a kernel is built from (to tell stale counters)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gemv_w4a16_group_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def read_traffic(kernel: str, algorithmic: int):
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel's sources changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f).get(kernel)
+        if entry and entry["source_sha256"] == kernel_source_digest(entry["sources"]):
+            return entry["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def e2e_ours(copies, x_dev, y_dev, M, N, K, device, stream, steps=2000):
+    """Same metric through the public API with host buffers: each step copies x from
+    pinned host memory, runs w4a16_matmul and reads y back to pinned host memory."""
+    import gemv_w4a16_group_gb300 as w4
+
+    ws = workspace_for(M, N, K, device)
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    bytes_w = weight_bytes(N, K)
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            x_dev.copy_(x_host, non_blocking=True)
+            c = copies[i % ROTATE]
+            w4.w4a16_matmul(x_dev, c[0], c[1], c[2], y=y_dev, workspace=ws)
+            y_host.copy_(y_dev, non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            x_dev.copy_(x_host, non_blocking=True)
+            c = copies[i % ROTATE]
+            w4.w4a16_matmul(x_dev, c[0], c[1], c[2], y=y_dev, workspace=ws)
+            y_host.copy_(y_dev, non_blocking=True)
+            stream.synchronize()  # the step's result is on the host
+        t1 = time.perf_counter()
+    return {"value": round(bytes_w * steps / (t1 - t0) / 1e9, 1), "unit": "GB/s",
+            "us_per_step": round((t1 - t0) / steps * 1e6, 2),
+            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2}
+
+
+def rows_ours(peaks, device, stream):
+    """Every step of the hot path on its own workload, with its roofline fraction."""
+    import gemv_w4a16_group_gb300 as w4
+
+    rows = {}
+    hbm = peaks["hbm_gbs"]
+    # quantize + pack on the Llama up-projection weights
+    N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+    w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
+    us = graph_time_us(lambda i: w4.w4a16_quantize(w, codes=codes, scales=s, mins=m), 4, 5, stream)
+    b = N * K * 4 + N * K + 4 * N * (K // 128)
+    rows["w4a16_quantize"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                              "frac_hbm": round(b / us / 1e3 / hbm, 3)}
+    us = graph_time_us(lambda i: w4.w4a16_pack(codes, qw=qw), 4, 5, stream)
+    b = N * K + N * K // 2
+    rows["w4a16_pack"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                          "frac_hbm": round(b / us / 1e3 / hbm, 3)}
+    del w, codes, qw, s, m
+
+    # batch sweep with outliers, against BF16 cuBLAS at the same M
+    cfg = workloads.BATCH_SWEEP
+    N, K = cfg["N"], cfg["K"]
+    w, codes, qw, s, m = quantized_on_device(N, K, 0, device, outlier_frac=cfg["outlier_frac"])
+    w_bf16 = w.to(torch.bfloat16)
+    del w, codes
+    cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(ROTATE)]
+    bf_cps = [w_bf16.clone() for _ in range(3)]  # 3 x 117 MB > 2 x L2
+    sweep = []
+    for M in cfg["Ms"]:
+        x = workloads.activations_bf16(M, K, seed=M).to(device)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        ws = workspace_for(M, N, K, device)
+        big = M >= 1024
+        us = graph_time_us(lambda i: w4.w4a16_matmul(x, *cps[i % ROTATE], y=y, workspace=ws),
+                           ROTATE if big else 4 * ROTATE, 2 if big else 10, stream)
+        us_bf = graph_time_us(lambda i: torch.matmul(x, bf_cps[i % 3].T, out=y),
+                              6 if big else 12, 2 if big else 10, stream)
+        bts, fl = w4a16_bytes(M, N, K), 2 * M * N * K
+        roof = roofline_us(bts, fl, peaks)
+        sweep.append({"M": M, "us": round(us, 2), "TFLOPS": round(fl / us / 1e6, 1),
+                      "GBps": round(bts / us / 1e3, 1), "roofline_us": round(roof, 2),
+                      "frac": round(roof / us, 3),
+                      "bound": "hbm" if bts / (peaks["hbm_gbs"] * 1e3) >= fl / (peaks["bf16_tflops"] * 1e6) else "tensor",
+                      "bf16_cublas_us": round(us_bf, 2),
+                      "bf16_cublas_TFLOPS": round(fl / us_bf / 1e6, 1),
+                      "speedup_vs_bf16": round(us_bf / us, 2)})
+        del x, y
+    del cps, bf_cps, w_bf16
+    rows["batch_sweep"] = sweep
+    even = [r["M"] for r in sweep if r["speedup_vs_bf16"] <= 1.0]
+    bpw = 4.25 / 8
+    rows["crossover"] = {
+        "predicted_4bit_ridge_M": round(peaks["bf16_tflops"] * 1e12 * bpw / (2 * peaks["hbm_gbs"] * 1e9), 1),
+        "predicted_bf16_ridge_M": round(peaks["bf16_tflops"] * 1e12 * 2 / (2 * peaks["hbm_gbs"] * 1e9), 1),
+        "measured_breakeven_vs_bf16_M": even[0] if even else None,
+        "pages": "~28 (4-bit) and ~100 (BF16) at a ridge of 102 FLOP/B; break-even at 128 measured"}
+
+    # Q4 block-32, 16384 x 16384
+    qc_cfg = workloads.Q4_SQUARE
+    N, K = qc_cfg["N"], qc_cfg["K"]
+    w = workloads.weights(N, K, seed=0).to(device)
+    qc, qsc = w4.q4b32_quantize(w)
+    us = graph_time_us(lambda i: w4.q4b32_quantize(w, codes=qc, scales=qsc), 2, 3, stream)
+    b = N * K * 4 + N * K // 2 + N * K // 16
+    rows["q4b32_quantize"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                              "frac_hbm": round(b / us / 1e3 / hbm, 3)}
+    del w
+    xq = workloads.activations_fp16(K, seed=0).to(device)
+    yq = torch.empty(N, dtype=torch.float16, device=device)
+    qcps = [(qc.clone(), qsc.clone()) for _ in range(2)] + [(qc, qsc)]
+    us = graph_time_us(lambda i: w4.q4b32_gemv(xq, *qcps[i % 3], y=yq), 12, 10, stream)
+    b = N * K * 18 // 32
+    rows["q4b32_gemv"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                          "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2),
+                          "pages": "93.0 us (1,624 GB/s) on an RTX 5090"}
+    del qcps, qc, qsc
+
+    # Qwen2.5-1.5B-shaped decode stack: 196 matmuls in one CUDA graph
+    stack = []
+    tot_bytes = 0
+    for layer in range(workloads.QWEN_STACK["layers"]):
+        for name, Nl, Kl in workloads.QWEN_STACK["block"]:
+            g = torch.Generator(device=device)
+            g.manual_seed(layer * 16 + len(stack))
+            wl = torch.randn(Nl, Kl, generator=g, device=device) * workloads.WEIGHT_STD
+            cl, sl, ml = w4.w4a16_quantize(wl)
+            ql = w4.w4a16_pack(cl)
+            del wl, cl
+            xl = torch.randn(1, Kl, generator=g, device=device).to(torch.bfloat16)
+            yl = torch.empty(1, Nl, dtype=torch.bfloat16, device=device)
+            stack.append((xl, ql, sl, ml, yl, workspace_for(1, Nl, Kl, device)))
+            tot_bytes += w4a16_bytes(1, Nl, Kl)
+
+    def token(i):
+        for (xl, ql, sl, ml, yl, wsl) in stack:
+            w4.w4a16_matmul(xl, ql, sl, ml, y=yl, workspace=wsl)
+
+    us_tok = graph_time_us(token, 1, 50, stream)
+    rows["qwen_stack"] = {"matmuls": len(stack), "us_per_token": round(us_tok, 2),
+                          "bytes": tot_bytes, "roofline_us": round(tot_bytes / hbm / 1e3, 2),
+                          "frac": round(tot_bytes / hbm / 1e3 / us_tok, 3),
+                          "note": "weights (698 MB) > L2; one graph of 196 launches per token",
+                          "pages": "3.68 ms for 197 matmuls (tinygemm, RTX 4060 Laptop)"}
+    del stack
+    return rows
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (baseline and reference arm)
+# --------------------------------------------------------------------------- #
+
+def oracle_inputs():
+    import oracle
+
+    cfg = workloads.LLAMA_UP
+    w = workloads.weights(cfg["N"], cfg["K"], seed=0).numpy()
+    codes, s, m = oracle.w4a16_quantize(w)
+    qw = oracle.w4a16_pack(codes)
+    x = workloads.bits16(workloads.activations_bf16(1, cfg["K"], seed=0))
+    return x, qw, s, m
+
+
+def cpu_baseline(seconds: float):
+    """The oracle as it stands (single-threaded C, fp64 sums) on the full M=1 workload,
+    repeated until at least `seconds` of CPU time has been spent."""
+    import oracle
+
+    x, qw, s, m = oracle_inputs()
+    N, K = qw.shape[1], qw.shape[0] * 8
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.w4a16_matmul(x, qw, s, m)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(weight_bytes(N, K) * reps / el / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"full M=1 workload (all {N} columns, K={K}) x {reps} repetitions, "
+                      f"{el:.1f} s single-threaded"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm, on bounded samples of the same workload."""
+    if rank != 0:
+        return None
+    import oracle
+
+    x, qw, s, m = oracle_inputs()
+    N, K = qw.shape[1], qw.shape[0] * 8
+    t0 = time.perf_counter()
+    oracle.w4a16_matmul(x, qw, s, m, cols=list(range(0, N, 64)))
+    t_col = (time.perf_counter() - t0) / len(range(0, N, 64))
+    budget = 90.0  # seconds for warmup + timed steps together
+    per_step = budget / max(1, args.steps + args.warmup)
+    ncols = int(max(8, min(N, per_step / max(t_col, 1e-9))))
+    cols = list(range(0, N, max(1, N // ncols)))[:ncols]
+    for _ in range(args.warmup):
+        oracle.w4a16_matmul(x, qw, s, m, cols=cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.w4a16_matmul(x, qw, s, m, cols=cols)
+    el = time.perf_counter() - t0
+    bytes_step = weight_bytes(N, K) * len(cols) / N
+    value = bytes_step * args.steps / el / 1e9
+    sample = f"{len(cols)} of {N} output columns (all K={K}) per step, single-threaded"
+    cfg = workloads.LLAMA_UP
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["name"], "M": 1, "N": N, "K": K, "group": 128},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=96000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="headline line only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

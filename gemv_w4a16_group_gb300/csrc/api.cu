@@ -38,7 +38,7 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 // product), 2 = CUDA-core GEMV (mixed-precision inner product), 3 = tensor-core kernel.
 int g_force_kernel = 0;
 // M at or below which the CUDA-core GEMV runs when the choice is by M.
-int g_gemv_max_m = 4;
+int g_gemv_max_m = 2;
 
 uint64_t g_wait_limit_ns = w4k::kDefaultWaitLimitNs;
 
@@ -78,12 +78,37 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw, w4a16_s
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Split-K plan of the tensor-core kernel for this shape on the current device.
+static w4k::TcSplit tc_split_plan(int M, int N, int K, size_t* bytes_needed) {
+  w4k::TcSplit plan;
+  *bytes_needed = 0;
+  static int sms_cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return plan;
+  if (sms_cache[dev] == 0)
+    cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sms_cache[dev];
+  const int bm = w4k::tc_block_m(M);
+  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bm - 1) / bm);
+  const long long slots = static_cast<long long>(sms) * w4k::tc_ctas_per_sm(bm);
+  const int kb = K / 64;
+  int splits = static_cast<int>(slots / (tiles > 0 ? tiles : 1));
+  if (splits > kb / 2) splits = kb / 2;  // at least two k-blocks per CTA
+  if (splits > 16) splits = 16;
+  if (splits < 2) return plan;
+  plan.splits = splits;
+  const size_t counters = ((static_cast<size_t>(tiles) * 4 + 255) / 256) * 256;
+  const size_t mp = static_cast<size_t>((M + bm - 1) / bm) * bm;
+  *bytes_needed = counters + static_cast<size_t>(splits) * mp * N * 4;
+  return plan;
+}
+
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
-  (void)M;
-  (void)N;
-  (void)K;
-  (void)group;
-  return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || group != 128 || K % group != 0) return 0;
+  if (M <= g_gemv_max_m) return 0;
+  size_t bytes = 0;
+  tc_split_plan(M, N, K, &bytes);
+  return bytes;
 }
 
 w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
@@ -98,17 +123,39 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
   if (workspace != nullptr && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t* q = reinterpret_cast<const uint32_t*>(qw);
-  int kernel = g_force_kernel;
-  if (kernel == 0) kernel = (M <= g_gemv_max_m) ? 1 : 3;
-  if (kernel == 1 || kernel == 2)
-    return from_cuda(w4k::launch_w4a16_gemv(x, q, scales, mins, y, M, N, K, kernel - 1, s));
   uint32_t* status = status_word_ptr();
   if (status == nullptr) return W4A16_ERR_CUDA;
+  int kernel = g_force_kernel;
+  if (kernel == 0) kernel = (M <= g_gemv_max_m && w4k::gemv_supports(M, K)) ? 2 : 3;
+  if (kernel == 1 || kernel == 2) {
+    // The GEMV takes up to gemv_max_rows() rows per launch; larger M (forced) loops.
+    const int step = w4k::gemv_max_rows();
+    if (!w4k::gemv_supports(M < step ? M : step, K)) return W4A16_ERR_UNSUPPORTED;
+    for (int m0 = 0; m0 < M; m0 += step) {
+      const int mb = (M - m0) < step ? (M - m0) : step;
+      cudaError_t e = w4k::launch_w4a16_gemv(x + static_cast<size_t>(m0) * K, q, scales, mins,
+                                             y + static_cast<size_t>(m0) * N, mb, N, K, kernel - 1,
+                                             status, g_wait_limit_ns, s);
+      if (e != cudaSuccess) return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+  }
   const int bm = w4k::tc_block_m(M);
   w4k::TcMaps maps;
   cudaError_t e = w4k::make_tc_maps(x, q, scales, mins, M, N, K, bm, &maps);
   if (e != cudaSuccess) return W4A16_ERR_CUDA;
-  return from_cuda(w4k::launch_w4a16_tc(maps, y, M, N, K, bm, status, g_wait_limit_ns, s));
+  // Split K across CTAs when the caller's workspace holds the plan's partial tiles.
+  size_t need = 0;
+  w4k::TcSplit split = tc_split_plan(M, N, K, &need);
+  if (split.splits > 1 && workspace != nullptr && workspace_bytes >= need) {
+    const size_t tiles = static_cast<size_t>((N + 127) / 128) * ((M + bm - 1) / bm);
+    const size_t counters = ((tiles * 4 + 255) / 256) * 256;
+    split.counter = static_cast<uint32_t*>(workspace);
+    split.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters);
+  } else {
+    split = w4k::TcSplit();
+  }
+  return from_cuda(w4k::launch_w4a16_tc(maps, y, M, N, K, bm, status, g_wait_limit_ns, split, s));
 }
 
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
@@ -120,7 +167,7 @@ w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
-static int g_q4_variant = 0;
+static int g_q4_variant = 1;
 
 w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                         uint16_t* y, int N, int K, w4a16_stream_t stream) {

@@ -28,7 +28,6 @@ namespace {
 
 constexpr int kBN = 128;  // weight columns per CTA (MMA M)
 constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row of BF16)
-constexpr int kStages = 4;
 constexpr int kDequantWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -38,6 +37,9 @@ constexpr uint32_t kRowBytes = kBN * 2;           // one scale (or min) row = 25
 
 template <int BM>
 struct Smem {
+  // Narrow tiles keep 3 stages so that a CTA needs only 128 TMEM columns and four CTAs
+  // (16 dequantising warps) share an SM.
+  static constexpr int kStages = BM <= 32 ? 3 : 4;
   static constexpr uint32_t x_bytes = BM * 128;
   static constexpr uint32_t x_off = 0;
   static constexpr uint32_t pk_off = x_off + kStages * x_bytes;
@@ -46,13 +48,14 @@ struct Smem {
   static constexpr uint32_t bar_off = mn_off + kStages * kRowBytes;
   static constexpr uint32_t nbars = 3 * kStages + 2;  // full, empty, afull, accfull, drain
   static constexpr uint32_t misc_off = bar_off + nbars * 8;
-  static constexpr uint32_t total = misc_off + 16;
+  static constexpr uint32_t total = misc_off + 16;  // tmem address, abort flag, split count
   static constexpr uint32_t alloc = total + 1024;  // slack to align the base to 1024 B
   static constexpr uint32_t tx_bytes = x_bytes + kPkBytes + 2 * kRowBytes;
   // TMEM: accumulator columns [0, BM), weight stages from a 32-column boundary after it;
   // the allocation is a power of two.
   static constexpr uint32_t a_col0 = BM < 32 ? 32u : static_cast<uint32_t>(BM);
-  static constexpr uint32_t tmem_cols = (a_col0 + kStages * 32 <= 256) ? 256u : 512u;
+  static constexpr uint32_t tmem_cols =
+      (a_col0 + kStages * 32 <= 128) ? 128u : (a_col0 + kStages * 32 <= 256) ? 256u : 512u;
   static_assert(a_col0 + kStages * 32 <= 512, "TMEM overflow");
   static_assert(x_bytes % 1024 == 0, "x stage must keep 1024-byte alignment");
 };
@@ -60,8 +63,10 @@ struct Smem {
 template <int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ TcMaps maps, uint16_t* __restrict__ y, int M, int N,
-                    int K, uint32_t* __restrict__ status, uint64_t limit_ns) {
+                    int K, uint32_t* __restrict__ status, uint64_t limit_ns,
+                    float* __restrict__ ws_partial, uint32_t* __restrict__ ws_counter) {
   using L = Smem<BM>;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -80,7 +85,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * BM;
-  const int KB = K / kBK;
+  // Split K over gridDim.z CTAs: this CTA takes k-blocks [kb0, kb0 + KB).
+  const int splits = gridDim.z;
+  const int KB_all = K / kBK;
+  const int per_split = (KB_all + splits - 1) / splits;
+  const int kb0 = blockIdx.z * per_split;
+  const int KB = min(KB_all, kb0 + per_split) - kb0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -117,10 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb >= kStages && !mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, status, limit_ns))
           break;
         mbar_arrive_expect_tx(&full[s], L::tx_bytes);
-        tma_load_2d(sx + s * L::x_bytes, &maps.x, &full[s], kb * kBK, m0);
-        tma_load_2d(spk + s * (kPkBytes / 4), &maps.qw, &full[s], n0, kb * (kBK / 8));
-        tma_load_2d(ssc + s * kBN, &maps.scales, &full[s], n0, kb / 2);
-        tma_load_2d(smn + s * kBN, &maps.mins, &full[s], n0, kb / 2);
+        const int gkb = kb0 + kb;
+        tma_load_2d(sx + s * L::x_bytes, &maps.x, &full[s], gkb * kBK, m0);
+        tma_load_2d(spk + s * (kPkBytes / 4), &maps.qw, &full[s], n0, gkb * (kBK / 8));
+        tma_load_2d(ssc + s * kBN, &maps.scales, &full[s], n0, gkb / 2);
+        tma_load_2d(smn + s * kBN, &maps.mins, &full[s], n0, gkb / 2);
         ++issued;
       }
       if (*abort_flag) {
@@ -194,28 +205,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&afull[s]);
     }
     // Epilogue: accumulator lane `row` holds y[m0 + j, n0 + row] in column j.
-    if (ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns)) {
-      tc_fence_after_sync();
-      const int n = n0 + row;
+    const bool have_acc = ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns);
+    const int n = n0 + row;
+    constexpr int kChunks = BM >= 32 ? BM / 32 : 1;
+    if (have_acc) tc_fence_after_sync();
+    if (splits == 1) {
+      if (have_acc) {
 #pragma unroll 1
-      for (int c = 0; c < BM / 32 || (BM < 32 && c == 0); ++c) {
-        uint32_t v[32];
-        if (BM >= 32) {
-          tmem_ld_32cols(lane_base + c * 32, v);
-        } else {
-          tmem_ld_32cols(lane_base, v);  // columns >= BM hold no rows; never stored
-        }
-        tmem_ld_wait();
-        if (n < N) {
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t v[32];
+          tmem_ld_32cols(lane_base + c * 32, v);  // BM < 32: columns >= BM are never stored
+          tmem_ld_wait();
+          if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + c * 32 + j;
-            if (j < BM && m < M)
-              y[static_cast<size_t>(m) * N + n] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+            for (int j = 0; j < 32; ++j) {
+              const int m = m0 + c * 32 + j;
+              if (j < BM && m < M)
+                y[static_cast<size_t>(m) * N + n] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+            }
           }
         }
       }
+    } else {
+      // Split K: write this CTA's fp32 partial tile, count arrivals per output tile; the
+      // last CTA of the tile sums the partials in split order (deterministic) and stores.
+      const size_t Mp = static_cast<size_t>(gridDim.y) * BM;
+      if (have_acc) {
+        float* part = ws_partial + static_cast<size_t>(blockIdx.z) * Mp * N;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t v[32];
+          tmem_ld_32cols(lane_base + c * 32, v);
+          tmem_ld_wait();
+          if (n < N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int m = m0 + c * 32 + j;
+              if (j < BM) __stcg(part + static_cast<size_t>(m) * N + n, __uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"n"(kDequantWarps * 32) : "memory");
+      uint32_t* tile_count = ws_counter + blockIdx.y * gridDim.x + blockIdx.x;
+      // Low 16 bits count arrivals; a CTA without a valid partial also sets bit 16.
+      if (threadIdx.x == 0) {
+        const uint32_t inc = have_acc ? 1u : 0x10001u;
+        *reinterpret_cast<volatile uint32_t*>(tmem_holder + 2) = atomicAdd(tile_count, inc) + inc;
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(kDequantWarps * 32) : "memory");
+      const uint32_t after = *reinterpret_cast<volatile uint32_t*>(tmem_holder + 2);
+      const bool last = (after & 0xFFFFu) == static_cast<uint32_t>(splits);
+      if (last && after < 0x10000u) {
+        __threadfence();
+        if (n < N) {
+#pragma unroll 1
+          for (int j = 0; j < BM; ++j) {
+            const int m = m0 + j;
+            if (m >= M) break;
+            float acc = 0.f;
+            for (int z = 0; z < splits; ++z)
+              acc += __ldcg(ws_partial + (static_cast<size_t>(z) * Mp + m) * N + n);
+            y[static_cast<size_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+          }
+        }
+      }
+      if (threadIdx.x == 0 && last) *tile_count = 0u;  // ready for the next call
+
     }
   }
 
@@ -279,16 +337,22 @@ cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base
 
 template <int BM>
 cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint32_t* status,
-                      uint64_t limit_ns, cudaStream_t stream) {
+                      uint64_t limit_ns, const TcSplit& split, cudaStream_t stream) {
   using L = Smem<BM>;
   auto kern = w4a16_tc_kernel<BM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L::alloc));
   if (e != cudaSuccess) return e;
-  dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM);
-  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  kern<<<grid, kThreads, L::alloc, stream>>>(maps, y, M, N, K, status, limit_ns);
+  dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM, split.splits);
+  if (grid.y > 65535 || split.splits < 1) return cudaErrorInvalidConfiguration;
+  kern<<<grid, kThreads, L::alloc, stream>>>(maps, y, M, N, K, status, limit_ns, split.partial,
+                                             split.counter);
   return cudaGetLastError();
+}
+
+template <int BM>
+int ctas_per_sm_by_tmem() {
+  return static_cast<int>(512u / Smem<BM>::tmem_cols);
 }
 
 }  // namespace
@@ -322,14 +386,25 @@ cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* 
 }
 
 cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
-                            uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+                            uint32_t* status, uint64_t limit_ns, const TcSplit& split,
+                            cudaStream_t stream) {
   switch (bm) {
-    case 16: return launch_bm<16>(maps, y, M, N, K, status, limit_ns, stream);
-    case 32: return launch_bm<32>(maps, y, M, N, K, status, limit_ns, stream);
-    case 64: return launch_bm<64>(maps, y, M, N, K, status, limit_ns, stream);
-    case 128: return launch_bm<128>(maps, y, M, N, K, status, limit_ns, stream);
-    case 256: return launch_bm<256>(maps, y, M, N, K, status, limit_ns, stream);
+    case 16: return launch_bm<16>(maps, y, M, N, K, status, limit_ns, split, stream);
+    case 32: return launch_bm<32>(maps, y, M, N, K, status, limit_ns, split, stream);
+    case 64: return launch_bm<64>(maps, y, M, N, K, status, limit_ns, split, stream);
+    case 128: return launch_bm<128>(maps, y, M, N, K, status, limit_ns, split, stream);
+    case 256: return launch_bm<256>(maps, y, M, N, K, status, limit_ns, split, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int tc_ctas_per_sm(int bm) {
+  switch (bm) {
+    case 16: return ctas_per_sm_by_tmem<16>();
+    case 32: return ctas_per_sm_by_tmem<32>();
+    case 64: return ctas_per_sm_by_tmem<64>();
+    case 128: return ctas_per_sm_by_tmem<128>();
+    default: return ctas_per_sm_by_tmem<256>();
   }
 }
 

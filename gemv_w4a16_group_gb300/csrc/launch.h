@@ -24,12 +24,14 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   cudaStream_t stream);
 
-// CUDA-core GEMV for small M (dequantization in registers). `variant` selects the
-// inner product: 0 = packed fp32 FMA on offset codes, 1 = mixed BF16 x BF16 -> fp32 FMA.
+// CUDA-core GEMV for small M (dequantization in registers, weights staged by TMA).
+// `variant` selects the inner product: 0 = packed fp32 FMA on offset codes, 1 = mixed
+// BF16 x BF16 -> fp32 FMA. gemv_supports() tells whether M and K fit its limits.
 int gemv_max_rows();
+bool gemv_supports(int M, int K);
 cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                               const uint16_t* mins, uint16_t* y, int M, int N, int K, int variant,
-                              cudaStream_t stream);
+                              uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
 
 // TMA + tcgen05 kernel: y^T tile = W_hat tile (tensor memory) x x^T tile (shared memory).
 struct TcMaps {
@@ -38,11 +40,20 @@ struct TcMaps {
   CUtensorMap scales;  // bf16 [K/128, N], box {128, 1}
   CUtensorMap mins;    // bf16 [K/128, N], box {128, 1}
 };
+// Split-K over gridDim.z CTAs: fp32 partial tiles [splits][ceil(M/bm)*bm][N] and one
+// arrival counter per output tile (zero before the launch; the kernel leaves it zero).
+struct TcSplit {
+  int splits = 1;
+  float* partial = nullptr;
+  uint32_t* counter = nullptr;
+};
 int tc_block_m(int M);
+int tc_ctas_per_sm(int bm);  // resident CTAs per SM that tensor memory allows
 cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                          const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps);
 cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
-                            uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
+                            uint32_t* status, uint64_t wait_limit_ns, const TcSplit& split,
+                            cudaStream_t stream);
 
 // Q4 block-32 GEMV.
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,

@@ -24,7 +24,7 @@ int w4a16_testing_force_kernel(int kernel);
  * value only queries. Returns the previous value. */
 int w4a16_testing_set_gemv_max_m(int m);
 
-/* Inner product of q4b32_gemv: 0 = packed fp32 (default), 1 = mixed FP16. Other values
+/* Inner product of q4b32_gemv: 0 = packed fp32, 1 = mixed FP16 (default). Other values
  * only query. Returns the previous value. */
 int w4a16_testing_set_q4_variant(int v);
 

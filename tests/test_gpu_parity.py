@@ -172,7 +172,7 @@ def test_llama_up_proj_m1_every_output(w4, force_kernel, kernel):
 
 @pytest.mark.parametrize("name,N,K", [(n, N, K) for n, N, K in workloads.QWEN_BLOCK])
 def test_qwen_stack_shapes_m1(w4, name, N, K):
-    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=hash(name) % 1000)
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=sum(map(ord, name)))
     qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
     x = workloads.activations_bf16(1, K, seed=K)
     check_matmul(w4, x, qw_np, s_np, m_np, qw, s, m)
@@ -283,3 +283,38 @@ def test_bounded_wait_expires_and_is_reported(w4):
     # the context is still usable
     z = torch.ones(4, device="cuda") * 2
     assert z.sum().item() == 8.0
+
+
+# --------------------------------------------------------------------------- #
+# split K through a caller-owned workspace
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("M,N,K", [(1, 14336, 4096), (3, 1536, 1536), (8, 1536, 8960),
+                                   (16, 14336, 4096), (32, 256, 1536), (64, 8960, 1536),
+                                   (128, 1536, 1536), (200, 1024, 4096)])
+def test_matmul_split_k_workspace(w4, M, N, K):
+    """Small-M tensor-core launches split K over CTAs through the workspace: same
+    tolerance, same bits twice, and the workspace's counters are left at zero."""
+    prev = w4.testing_set_gemv_max_m(0)  # every M takes the tensor-core kernel
+    try:
+        need = w4.w4a16_matmul_workspace_bytes(M, N, K)
+        w, codes, s_np, m_np, qw_np = quantized(N, K, seed=M + N)
+        qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+        x = workloads.activations_bf16(M, K, seed=M)
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
+        y1 = w4.w4a16_matmul(x.cuda(), qw, s, m, workspace=ws if need else None)
+        y2 = w4.w4a16_matmul(x.cuda(), qw, s, m, workspace=ws if need else None)
+        torch.cuda.synchronize()
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+        cols = None if M * N * K <= 2**31 else workloads.sample_indices(N, 64, seed=M).numpy()
+        y_ref, a_ref = oracle.w4a16_matmul(bits(x), qw_np, s_np, m_np, cols=cols)
+        yv = y1.float().cpu().numpy()
+        if cols is not None:
+            yv = yv[:, cols]
+        assert oracle.within_tolerance(yv, y_ref, a_ref).all()
+        if need:
+            tiles = (N + 127) // 128  # one m-tile at every M used here
+            assert torch.count_nonzero(ws[:256 * ((tiles * 4 + 255) // 256)]).item() == 0
+        assert w4.w4a16_device_status() == 0
+    finally:
+        w4.testing_set_gemv_max_m(prev)
