@@ -26,7 +26,7 @@ from .build import LIB_PATH
 
 __all__ = [
     "W4A16Error", "library_path", "w4a16_quantize", "w4a16_pack", "w4a16_matmul",
-    "w4a16_matmul_workspace_bytes", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
+    "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
     "testing_set_q4_variant",
 ]
@@ -57,6 +57,7 @@ def _load():
         "w4a16_quantize": [P, I, I, I, P, P, P, P],
         "w4a16_pack": [P, I, I, P, P],
         "w4a16_matmul": [P, P, P, P, P, I, I, I, I, P, S, P],
+        "w4a16_matmul_noalloc": [P, P, P, P, P, I, I, I, I, P],
         "q4b32_quantize": [P, I, I, P, P, P],
         "q4b32_gemv": [P, P, P, P, I, I, P],
         "w4a16_device_status": [P],
@@ -156,6 +157,24 @@ def w4a16_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, mins: 
         _dev(scales, "scales", torch.bfloat16, (K // group, N)),
         _dev(mins, "mins", torch.bfloat16, (K // group, N)),
         _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
+    return y
+
+
+def w4a16_matmul_noalloc(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor,
+                         mins: torch.Tensor, y: torch.Tensor, group: int = 128,
+                         stream=None) -> torch.Tensor:
+    """y = x . w_hat^T without any allocation by the library or this function: the
+    caller passes y. For callers that cannot allocate device memory; the scratch is a
+    fixed 16 MiB array inside the library, shared by every call on the device, so calls
+    that may overlap on the GPU must be ordered. Make the first call on a device before
+    any stream capture."""
+    M, K = x.shape
+    N = qw.shape[1]
+    _check("w4a16_matmul_noalloc", _lib.w4a16_matmul_noalloc(
+        _dev(x, "x", torch.bfloat16), _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)),
+        _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, _stream(stream)))
     return y
 
 

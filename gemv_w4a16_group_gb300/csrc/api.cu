@@ -16,7 +16,7 @@ __device__ uint32_t g_status_word;
 constexpr int kMaxDevices = 64;
 
 // Device address of g_status_word for the current device (looked up once per device).
-uint32_t* status_word_ptr() {
+uint32_t* status_word_ptr_impl() {
   static uint32_t* ptrs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
@@ -29,6 +29,8 @@ uint32_t* status_word_ptr() {
   }
   return ptrs[dev];
 }
+
+uint32_t* status_word_ptr() { return status_word_ptr_impl(); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -43,6 +45,36 @@ int g_gemv_max_m = 2;
 uint64_t g_wait_limit_ns = w4k::kDefaultWaitLimitNs;
 
 }  // namespace
+
+namespace w4k {
+uint32_t* status_word() { return status_word_ptr_impl(); }
+}  // namespace w4k
+
+// Split-K plan of the tensor-core kernel for this shape on the current device.
+w4k::TcSplit w4k::tc_split_plan(int M, int N, int K, size_t* bytes_needed) {
+  w4k::TcSplit plan;
+  *bytes_needed = 0;
+  static int sms_cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return plan;
+  if (sms_cache[dev] == 0)
+    cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sms_cache[dev];
+  const int bm = w4k::tc_block_m(M);
+  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bm - 1) / bm);
+  const long long slots = static_cast<long long>(sms) * w4k::tc_ctas_per_sm(bm);
+  const int kb = K / 64;
+  int splits = static_cast<int>(slots / (tiles > 0 ? tiles : 1));
+  if (splits > kb / 2) splits = kb / 2;  // at least two k-blocks per CTA
+  if (splits > 16) splits = 16;
+  if (splits < 2) return plan;
+  plan.splits = splits;
+  const size_t counters = ((static_cast<size_t>(tiles) * 4 + 255) / 256) * 256;
+  const size_t mp = static_cast<size_t>((M + bm - 1) / bm) * bm;
+  *bytes_needed = counters + static_cast<size_t>(splits) * mp * N * 4;
+  return plan;
+}
+
 
 extern "C" {
 
@@ -78,36 +110,11 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw, w4a16_s
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// Split-K plan of the tensor-core kernel for this shape on the current device.
-static w4k::TcSplit tc_split_plan(int M, int N, int K, size_t* bytes_needed) {
-  w4k::TcSplit plan;
-  *bytes_needed = 0;
-  static int sms_cache[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return plan;
-  if (sms_cache[dev] == 0)
-    cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
-  const int sms = sms_cache[dev];
-  const int bm = w4k::tc_block_m(M);
-  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + bm - 1) / bm);
-  const long long slots = static_cast<long long>(sms) * w4k::tc_ctas_per_sm(bm);
-  const int kb = K / 64;
-  int splits = static_cast<int>(slots / (tiles > 0 ? tiles : 1));
-  if (splits > kb / 2) splits = kb / 2;  // at least two k-blocks per CTA
-  if (splits > 16) splits = 16;
-  if (splits < 2) return plan;
-  plan.splits = splits;
-  const size_t counters = ((static_cast<size_t>(tiles) * 4 + 255) / 256) * 256;
-  const size_t mp = static_cast<size_t>((M + bm - 1) / bm) * bm;
-  *bytes_needed = counters + static_cast<size_t>(splits) * mp * N * 4;
-  return plan;
-}
-
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
   if (M <= 0 || N <= 0 || K <= 0 || group != 128 || K % group != 0) return 0;
   if (M <= g_gemv_max_m) return 0;
   size_t bytes = 0;
-  tc_split_plan(M, N, K, &bytes);
+  w4k::tc_split_plan(M, N, K, &bytes);
   return bytes;
 }
 
@@ -146,7 +153,7 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
   if (e != cudaSuccess) return W4A16_ERR_CUDA;
   // Split K across CTAs when the caller's workspace holds the plan's partial tiles.
   size_t need = 0;
-  w4k::TcSplit split = tc_split_plan(M, N, K, &need);
+  w4k::TcSplit split = w4k::tc_split_plan(M, N, K, &need);
   if (split.splits > 1 && workspace != nullptr && workspace_bytes >= need) {
     const size_t tiles = static_cast<size_t>((N + 127) / 128) * ((M + bm - 1) / bm);
     const size_t counters = ((tiles * 4 + 255) / 256) * 256;

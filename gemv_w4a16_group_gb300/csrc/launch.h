@@ -49,6 +49,11 @@ struct TcSplit {
 };
 int tc_block_m(int M);
 int tc_ctas_per_sm(int bm);  // resident CTAs per SM that tensor memory allows
+// Split plan for this shape on the current device; *bytes_needed = workspace bytes
+// (counters rounded to 256 B, then the partial tiles), 0 when the plan does not split.
+TcSplit tc_split_plan(int M, int N, int K, size_t* bytes_needed);
+// Device address of the library's status word on the current device (nullptr on error).
+uint32_t* status_word();
 cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                          const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps);
 cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,

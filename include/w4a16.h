@@ -103,6 +103,25 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);
 
 /*
+ * w4a16_matmul_noalloc -- the same product as w4a16_matmul for callers that cannot
+ * allocate device memory or lend the library a buffer (for example a plugin inside a
+ * runtime that owns all device memory, or a loop that must not pay for an allocation).
+ * The pages have no counterpart: it exists only for such callers.
+ *   Arguments as for w4a16_matmul, without a workspace. It always runs the tensor-core
+ *   kernel; when that kernel splits K, its scratch is a 16 MiB array compiled into the
+ *   library (held on every device that loads the library until the process exits).
+ *   Returns W4A16_ERR_WORKSPACE, launching nothing, for a shape whose split needs more
+ *   than 16 MiB of scratch.
+ *   All calls on a device share that array: calls whose kernels may overlap on the GPU
+ *   race, so order them (one stream, or events). Each call clears the counters it uses
+ *   first. The first call on a device looks up the array's device address; make it
+ *   before any stream capture.
+ */
+w4a16_status w4a16_matmul_noalloc(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                                  const uint16_t* mins, uint16_t* y, int M, int N, int K,
+                                  int group, w4a16_stream_t stream);
+
+/*
  * q4b32_quantize -- fp32 weights to Q4 blocks of 32 ("Why My 4-Bit CUDA Kernel Wasn't
  * Faster": 16 bytes of codes plus a 2-byte scale the 32 weights share).
  *   w      fp32 [N, K]
