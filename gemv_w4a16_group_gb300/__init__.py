@@ -215,7 +215,7 @@ def w4a16_selftest_bounded_wait(limit_us: int, stream=None) -> int:
 
 
 def testing_force_kernel(kernel: int) -> int:
-    """0 = by M, 1/2 = CUDA-core GEMV (fp32x2 / mixed BF16 inner product), 3 = tcgen05."""
+    """0 = by M, 1 = the small-M GEMV kernel, 2 = the tcgen05 tensor-core kernel."""
     return int(_lib.w4a16_testing_force_kernel(kernel))
 
 

@@ -36,11 +36,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
 
-// Kernel choice for w4a16_matmul: 0 = by M (default), 1 = CUDA-core GEMV (fp32x2 inner
-// product), 2 = CUDA-core GEMV (mixed-precision inner product), 3 = tensor-core kernel.
+// Kernel choice for w4a16_matmul: 0 = by M (default), 1 = small-M GEMV kernel,
+// 2 = TMA + tcgen05 tensor-core kernel.
 int g_force_kernel = 0;
 // M at or below which the CUDA-core GEMV runs when the choice is by M.
-int g_gemv_max_m = 2;
+int g_gemv_max_m = 8;
 
 uint64_t g_wait_limit_ns = w4k::kDefaultWaitLimitNs;
 
@@ -112,9 +112,11 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw, w4a16_s
 
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
   if (M <= 0 || N <= 0 || K <= 0 || group != 128 || K % group != 0) return 0;
-  if (M <= g_gemv_max_m) return 0;
   size_t bytes = 0;
-  w4k::tc_split_plan(M, N, K, &bytes);
+  if (M <= g_gemv_max_m && w4k::gemv_supports(M, K))
+    w4k::gemv_split_plan(M, N, K, &bytes);
+  else
+    w4k::tc_split_plan(M, N, K, &bytes);
   return bytes;
 }
 
@@ -133,15 +135,25 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
   uint32_t* status = status_word_ptr();
   if (status == nullptr) return W4A16_ERR_CUDA;
   int kernel = g_force_kernel;
-  if (kernel == 0) kernel = (M <= g_gemv_max_m && w4k::gemv_supports(M, K)) ? 2 : 3;
-  if (kernel == 1 || kernel == 2) {
+  if (kernel == 0) kernel = (M <= g_gemv_max_m && w4k::gemv_supports(M, K)) ? 1 : 2;
+  if (kernel == 1) {
     // The GEMV takes up to gemv_max_rows() rows per launch; larger M (forced) loops.
     const int step = w4k::gemv_max_rows();
     if (!w4k::gemv_supports(M < step ? M : step, K)) return W4A16_ERR_UNSUPPORTED;
     for (int m0 = 0; m0 < M; m0 += step) {
       const int mb = (M - m0) < step ? (M - m0) : step;
+      // Split K over thread blocks when the caller's workspace holds the plan.
+      size_t need = 0;
+      w4k::GemvSplit split = w4k::gemv_split_plan(mb, N, K, &need);
+      if (split.splits > 1 && workspace != nullptr && workspace_bytes >= need) {
+        const size_t counters = ((static_cast<size_t>((N + 127) / 128) * 4 + 255) / 256) * 256;
+        split.counter = static_cast<uint32_t*>(workspace);
+        split.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters);
+      } else {
+        split = w4k::GemvSplit();
+      }
       cudaError_t e = w4k::launch_w4a16_gemv(x + static_cast<size_t>(m0) * K, q, scales, mins,
-                                             y + static_cast<size_t>(m0) * N, mb, N, K, kernel - 1,
+                                             y + static_cast<size_t>(m0) * N, mb, N, K, split,
                                              status, g_wait_limit_ns, s);
       if (e != cudaSuccess) return W4A16_ERR_CUDA;
     }
@@ -212,7 +224,7 @@ w4a16_status w4a16_selftest_bounded_wait(uint32_t limit_us, w4a16_stream_t strea
 
 // Test and benchmark hooks (declared in w4a16_testing.h, not part of the public header).
 int w4a16_testing_force_kernel(int kernel) {
-  if (kernel < 0 || kernel > 3) return -1;
+  if (kernel < 0 || kernel > 2) return -1;
   const int prev = g_force_kernel;
   g_force_kernel = kernel;
   return prev;

@@ -37,16 +37,19 @@ constexpr uint32_t kRowBytes = kBN * 2;           // one scale (or min) row = 25
 
 template <int BM>
 struct Smem {
-  // Narrow tiles keep 3 stages so that a CTA needs only 128 TMEM columns and four CTAs
-  // (16 dequantising warps) share an SM.
-  static constexpr int kStages = BM <= 32 ? 3 : 4;
+  // Shared-memory ring (x tile + packed words + scale/min rows per stage): deep for narrow
+  // tiles so that ~80-100 KB per SM are in flight against DRAM latency. The rebuilt
+  // weight tiles live in a separate, shorter ring of TMEM stages.
+  static constexpr int kStages = BM <= 16 ? 12 : BM <= 32 ? 10 : BM <= 64 ? 8 : BM <= 128 ? 6 : 4;
+  static constexpr int kAStages = BM <= 32 ? 3 : 4;
   static constexpr uint32_t x_bytes = BM * 128;
   static constexpr uint32_t x_off = 0;
   static constexpr uint32_t pk_off = x_off + kStages * x_bytes;
   static constexpr uint32_t sc_off = pk_off + kStages * kPkBytes;
   static constexpr uint32_t mn_off = sc_off + kStages * kRowBytes;
   static constexpr uint32_t bar_off = mn_off + kStages * kRowBytes;
-  static constexpr uint32_t nbars = 3 * kStages + 2;  // full, empty, afull, accfull, drain
+  // full[S], empty[S], afull[SA], aempty[SA], accfull, drain
+  static constexpr uint32_t nbars = 2 * kStages + 2 * kAStages + 2;
   static constexpr uint32_t misc_off = bar_off + nbars * 8;
   static constexpr uint32_t total = misc_off + 16;  // tmem address, abort flag, split count
   static constexpr uint32_t alloc = total + 1024;  // slack to align the base to 1024 B
@@ -55,18 +58,20 @@ struct Smem {
   // the allocation is a power of two.
   static constexpr uint32_t a_col0 = BM < 32 ? 32u : static_cast<uint32_t>(BM);
   static constexpr uint32_t tmem_cols =
-      (a_col0 + kStages * 32 <= 128) ? 128u : (a_col0 + kStages * 32 <= 256) ? 256u : 512u;
-  static_assert(a_col0 + kStages * 32 <= 512, "TMEM overflow");
+      (a_col0 + kAStages * 32 <= 128) ? 128u : (a_col0 + kAStages * 32 <= 256) ? 256u : 512u;
+  static_assert(a_col0 + kAStages * 32 <= 512, "TMEM overflow");
+  static_assert(alloc <= 227u * 1024u, "shared memory overflow");
   static_assert(x_bytes % 1024 == 0, "x stage must keep 1024-byte alignment");
 };
 
 template <int BM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     w4a16_tc_kernel(const __grid_constant__ TcMaps maps, uint16_t* __restrict__ y, int M, int N,
                     int K, uint32_t* __restrict__ status, uint64_t limit_ns,
                     float* __restrict__ ws_partial, uint32_t* __restrict__ ws_counter) {
   using L = Smem<BM>;
   constexpr int kStages = L::kStages;
+  constexpr int kAStages = L::kAStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -75,11 +80,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint16_t* ssc = reinterpret_cast<uint16_t*>(smem + L::sc_off);
   uint16_t* smn = reinterpret_cast<uint16_t*>(smem + L::mn_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
-  uint64_t* full = bars;                 // TMA bytes landed (count 1 + tx)
-  uint64_t* empty = bars + kStages;      // MMAs reading the stage are done (commit)
-  uint64_t* afull = bars + 2 * kStages;  // weight stage written to TMEM (4 warps)
-  uint64_t* accfull = bars + 3 * kStages;
-  uint64_t* drain = bars + 3 * kStages + 1;
+  uint64_t* full = bars;                        // TMA bytes landed (count 1 + tx)
+  uint64_t* empty = bars + kStages;             // MMAs reading the stage are done (commit)
+  uint64_t* afull = bars + 2 * kStages;         // weight stage written to TMEM (4 warps)
+  uint64_t* aempty = afull + kAStages;          // MMAs reading that TMEM stage are done
+  uint64_t* accfull = aempty + kAStages;
+  uint64_t* drain = accfull + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile uint32_t* abort_flag = tmem_holder + 1;
 
@@ -96,12 +102,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
       mbar_init(&afull[s], kDequantWarps);
+      mbar_init(&aempty[s], 1);
     }
     mbar_init(accfull, 1);
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_barrier_init();
+    pdl_launch_dependents();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, L::tmem_cols);
@@ -120,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
+      pdl_wait();  // x (in every stage) may be written by the previous kernel
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kStages;
@@ -148,19 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kBN, BM);
       bool ok = true;
       for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1u;
-        ok = mbar_wait_bounded(&afull[s], ph, abort_flag, status, limit_ns) &&
-             mbar_wait_bounded(&full[s], ph, abort_flag, status, limit_ns);
+        const int s = kb % kStages, sa = kb % kAStages;
+        ok = mbar_wait_bounded(&afull[sa], (kb / kAStages) & 1u, abort_flag, status, limit_ns) &&
+             mbar_wait_bounded(&full[s], (kb / kStages) & 1u, abort_flag, status, limit_ns);
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t xs = smem_addr(sx + s * L::x_bytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          tc_mma_a_tmem(tmem, tmem + L::a_col0 + s * 32 + kk * 8,
+          tc_mma_a_tmem(tmem, tmem + L::a_col0 + sa * 32 + kk * 8,
                         smem_desc_kmajor_sw128(xs + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
+        tc_commit(&aempty[sa]);
       }
       if (ok) tc_commit(accfull);
       // Whatever happened, wait until every MMA issued here has completed.
@@ -169,14 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(drain, 0u, &no_abort, status, limit_ns);
     }
   } else if (warp < kDequantWarps) {
+    pdl_wait();  // y and the workspace may still be in use by the previous kernel
     const int row = warp * 32 + lane;  // TMEM lane = weight column n0 + row
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const uint32_t b128 = 0x43004300u;  // BF16 (128, 128)
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1u;
-      if (!mbar_wait_bounded(&full[s], ph, abort_flag, status, limit_ns)) {
+      const int s = kb % kStages, sa = kb % kAStages;
+      if (!mbar_wait_bounded(&full[s], (kb / kStages) & 1u, abort_flag, status, limit_ns) ||
+          (kb >= kAStages && !mbar_wait_bounded(&aempty[sa], ((kb / kAStages) - 1) & 1u,
+                                                abort_flag, status, limit_ns))) {
         ok = false;
         break;
       }
@@ -198,11 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           out[4 * c + i] = *reinterpret_cast<const uint32_t*>(&wv);
         }
       }
-      tmem_st_32cols(lane_base + L::a_col0 + s * 32, out);
+      tmem_st_32cols(lane_base + L::a_col0 + sa * 32, out);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[s]);
+      if (lane == 0) mbar_arrive(&afull[sa]);
     }
     // Epilogue: accumulator lane `row` holds y[m0 + j, n0 + row] in column j.
     const bool have_acc = ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns);
@@ -261,14 +274,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last && after < 0x10000u) {
         __threadfence();
         if (n < N) {
+          // 4 rows at a time, up to 4 splits per round: 16 independent loads in flight.
 #pragma unroll 1
-          for (int j = 0; j < BM; ++j) {
-            const int m = m0 + j;
-            if (m >= M) break;
-            float acc = 0.f;
-            for (int z = 0; z < splits; ++z)
-              acc += __ldcg(ws_partial + (static_cast<size_t>(z) * Mp + m) * N + n);
-            y[static_cast<size_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+          for (int j0 = 0; j0 < BM && m0 + j0 < M; j0 += 4) {
+            float acc[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[jj] = 0.f;
+#pragma unroll 1
+            for (int z0 = 0; z0 < splits; z0 += 4) {
+              float v[4][4];
+#pragma unroll
+              for (int dz = 0; dz < 4; ++dz)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                  const int z = z0 + dz, m = m0 + j0 + jj;
+                  v[dz][jj] = (z < splits && m < M)
+                                  ? __ldcg(ws_partial + (static_cast<size_t>(z) * Mp + m) * N + n)
+                                  : 0.f;
+                }
+#pragma unroll
+              for (int dz = 0; dz < 4; ++dz)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[jj] += v[dz][jj];
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int m = m0 + j0 + jj;
+              if (m < M)
+                y[static_cast<size_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[jj]));
+            }
           }
         }
       }
@@ -345,14 +379,15 @@ cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint
   if (e != cudaSuccess) return e;
   dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM, split.splits);
   if (grid.y > 65535 || split.splits < 1) return cudaErrorInvalidConfiguration;
-  kern<<<grid, kThreads, L::alloc, stream>>>(maps, y, M, N, K, status, limit_ns, split.partial,
-                                             split.counter);
-  return cudaGetLastError();
+  return launch_with_pdl(kern, grid, dim3(kThreads), L::alloc, stream, maps, y, M, N, K, status,
+                         limit_ns, split.partial, split.counter);
 }
 
 template <int BM>
 int ctas_per_sm_by_tmem() {
-  return static_cast<int>(512u / Smem<BM>::tmem_cols);
+  const int by_tmem = static_cast<int>(512u / Smem<BM>::tmem_cols);
+  const int by_smem = static_cast<int>((228u * 1024u) / (Smem<BM>::alloc + 1024u));
+  return by_tmem < by_smem ? by_tmem : by_smem;
 }
 
 }  // namespace

@@ -24,14 +24,23 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   cudaStream_t stream);
 
-// CUDA-core GEMV for small M (dequantization in registers, weights staged by TMA).
-// `variant` selects the inner product: 0 = packed fp32 FMA on offset codes, 1 = mixed
-// BF16 x BF16 -> fp32 FMA. gemv_supports() tells whether M and K fit its limits.
+// GEMV / skinny kernel for M <= 8 (weights staged by TMA, dequantised in registers into
+// mma.sync fragments). With a split plan (splits > 1) the K range of each 128-column slab
+// is divided over thread blocks: fp32 partials [splits][mr][N] and one arrival counter per
+// slab (zero before the launch; the kernel leaves it zero). gemv_supports() tells whether
+// M and K fit its limits.
+struct GemvSplit {
+  int splits = 1;
+  float* partial = nullptr;
+  uint32_t* counter = nullptr;
+};
 int gemv_max_rows();
 bool gemv_supports(int M, int K);
+GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed);
 cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
-                              const uint16_t* mins, uint16_t* y, int M, int N, int K, int variant,
-                              uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
+                              const uint16_t* mins, uint16_t* y, int M, int N, int K,
+                              const GemvSplit& split, uint32_t* status, uint64_t wait_limit_ns,
+                              cudaStream_t stream);
 
 // TMA + tcgen05 kernel: y^T tile = W_hat tile (tensor memory) x x^T tile (shared memory).
 struct TcMaps {

@@ -81,6 +81,9 @@ __global__ void __launch_bounds__(kThreads)
   const int b_end = min(nb, b_begin + bpw);
   const size_t row_bytes = static_cast<size_t>(K) >> 1;
 
+  if (tid == 0) pdl_launch_dependents();
+  pdl_wait();  // x may be written by the previous kernel on the stream
+
   float yacc[kRows];
 #pragma unroll
   for (int r = 0; r < kRows; ++r) yacc[r] = 0.f;
@@ -176,11 +179,8 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                               uint16_t* y, int N, int K, int variant, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((N + kRows - 1) / kRows);
-  if (variant == 1)
-    q4b32_gemv_kernel<1><<<blocks, kThreads, 0, stream>>>(x, codes, scales, y, N, K);
-  else
-    q4b32_gemv_kernel<0><<<blocks, kThreads, 0, stream>>>(x, codes, scales, y, N, K);
-  return cudaGetLastError();
+  auto kern = variant == 1 ? q4b32_gemv_kernel<1> : q4b32_gemv_kernel<0>;
+  return launch_with_pdl(kern, dim3(blocks), dim3(kThreads), 0, stream, x, codes, scales, y, N, K);
 }
 
 }  // namespace w4k

@@ -14,14 +14,14 @@
 extern "C" {
 #endif
 
-/* Kernel w4a16_matmul uses: 0 = chosen by M (default), 1 = CUDA-core GEMV with the
- * packed fp32 inner product, 2 = CUDA-core GEMV with the mixed BF16 inner product,
- * 3 = TMA + tcgen05 tensor-core kernel. Returns the previous choice, or -1 if `kernel`
- * is out of range (nothing changes then). */
+/* Kernel w4a16_matmul uses: 0 = chosen by M (default), 1 = the small-M GEMV kernel
+ * (forced for M > 8 it runs once per block of 8 rows), 2 = the TMA + tcgen05
+ * tensor-core kernel. Returns the previous choice, or -1 if `kernel` is out of range
+ * (nothing changes then). */
 int w4a16_testing_force_kernel(int kernel);
 
-/* Largest M that the by-M choice sends to the CUDA-core GEMV (default 4). A negative
- * value only queries. Returns the previous value. */
+/* Largest M that the by-M choice sends to the GEMV kernel (default 8, its maximum). A
+ * negative value only queries. Returns the previous value. */
 int w4a16_testing_set_gemv_max_m(int m);
 
 /* Inner product of q4b32_gemv: 0 = packed fp32, 1 = mixed FP16 (default). Other values
