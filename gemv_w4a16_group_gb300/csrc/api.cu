@@ -146,9 +146,9 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
       size_t need = 0;
       w4k::GemvSplit split = w4k::gemv_split_plan(mb, N, K, &need);
       if (split.splits > 1 && workspace != nullptr && workspace_bytes >= need) {
-        const size_t counters = ((static_cast<size_t>((N + 127) / 128) * 4 + 255) / 256) * 256;
         split.counter = static_cast<uint32_t*>(workspace);
-        split.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters);
+        split.partial =
+            reinterpret_cast<float*>(static_cast<char*>(workspace) + split.partial_offset);
       } else {
         split = w4k::GemvSplit();
       }

@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_barrier_init();
-    pdl_launch_dependents();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_holder, L::tmem_cols);
@@ -127,6 +126,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_holder;
+  // Dependent launches only after this CTA holds its tensor memory: a dependent CTA on the
+  // same SM may then wait for this one's columns, but this one never waits for it.
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == kTmaWarp) {
     if (lane == 0) {

@@ -1,43 +1,51 @@
-// W4A16 GEMV / skinny kernel for small M (M <= 8): weights staged by TMA, dequantised in
-// registers, the multiply-adds done by BF16 mma.sync fragments built straight from the
-// packed words.
+// W4A16 GEMV / skinny kernel for small M (M <= 8): packed words staged by TMA, codes widened
+// to FP16 in registers with one mask per pair of codes, inner products on the tensor
+// pipe (mma.sync m16n8k16, FP16 x FP16 -> FP32), scale and minimum folded per group.
 //
 //   y[m, n] = sum_g ( s[g,n] * sum_{k in g} x[m,k] q[n,k] + min[g,n] * sum_{k in g} x[m,k] )
 //
 // The factorised per-group form is the one the pages give for their M = 1 kernel ("Low-
 // Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", "How the measurements were
-// taken": it "sums s x sum x.q + min x sum x per group in FP32"). The work split follows
-// "Quantization and GEMV", "Writing a GEMV kernel": 128-bit reads, K split across warps
-// (and, for balance, across thread blocks), a shuffle/shared-memory reduction, adapted to
-// the K/8 x N packed layout (N contiguous).
+// taken": FP32 sums of s x sum x.q plus min x sum x, group by group). The work split
+// follows "Quantization and GEMV", "Writing a GEMV kernel" (wide reads, K split over
+// warps, fixed-order reductions), adapted to the K/8 x N packed layout (N contiguous).
 //
-// Why the tensor core in a GEMV: at 4 bits the unpacking is a real share of the issue
-// slots ("Where the time goes at M = 1"). A CUDA-core inner product costs one FMA per code
-// plus the unpacking; here one m16n8k16 instruction takes 256 codes, so a packed word
-// costs 3 shifts + 4 LOP3 (code pairs ORed into BF16 mantissas: 0x4300 | q = 128 + q)
-// plus a quarter of an MMA, and M up to 8 costs the same as M = 1. The kernel stays bound
-// by HBM.
+// What bounds it on GB300. At 4 bits an SM must turn ~6 packed words per clock into
+// products to keep up with its share of HBM ("Where the time goes at M = 1": the unpacking
+// decides). Masks and shifts run on the integer pipe at half the FMA rate, so the kernel
+// spends as few of them as it can: in an FP16 the mantissa holds bits 0..9, so a 16-bit
+// half of a word yields two codes in place (0x6400 | q = 1024 + q from bits 0..3, and
+// 0x6400 | 16 q = 1024 + 16 q from bits 4..7). A word costs 4 masks + 1 shift for its 8
+// codes (BF16, with 7 mantissa bits, would need 3 shifts). The products go to the tensor
+// pipe (one m16n8k16 per 256 codes, batch rows in the n8 dimension), which runs beside the
+// integer pipe.
 //
-// Launch shape (measured on GB300: the TMA engine is limited by box rows, so boxes must be
-// wide; and a launch must overlap the previous one to stream at full bandwidth):
-//   * work units = (slab of 128 columns, k-range); with a workspace the K range of a slab
-//     is split so that the units balance over the SMs; persistent grid (<= one CTA per
-//     SM), CTA c takes units c, c + G, ...;
-//   * a producer warp streams each unit in chunks of 128 columns x 512 k (64 rows of 512 B:
-//     32 KB of packed words + 2 KB of scales and minimums) into a shared-memory ring with
-//     TMA (~200 KB in flight per SM at M = 1). It issues its weight loads before it waits
-//     for the previous kernel on the stream (programmatic dependent launch);
-//   * 16 consumer warps: warp w takes column quarter w % 4 (32 columns) of group w / 4 of
-//     each chunk. Lane (gq, c) = (lane / 4, lane % 4) reads packed row 4b + c of block b
-//     (b = 0..3) and columns 4gq..4gq+3 with one 16-byte shared load; its four words fill
-//     the A fragments of two 16-row MMA tiles (tile t: rows gq <- column 4gq + 2t,
-//     gq + 8 <- column 4gq + 2t + 1);
-//   * the k order inside an MMA is permuted so that code pairs (q_j, q_{j+4}) -- one LOP3
-//     each -- are fragment pairs; x is stored once per CTA in shared memory in the matching
-//     order (B fragments);
-//   * per group the fp32 accumulator D = sum (128 + q) x is folded into y with
-//     y += s * D + (min - 128 s) * sum_g x, the group sums of x computed once per CTA;
-//   * per unit the 4 warps of a column quarter are summed in a fixed order; a split slab
+// x is converted to FP16 exactly, scaled per group of 128 by a power of two 2^e so that its
+// largest magnitude lands in [2^14, 2^15) (a BF16 value has 8 significant bits, a normal
+// FP16 11), and the k slots holding 16 q get x 2^(e-4). Per group the tensor core then
+// returns D = 2^e (sum q x + 1024 sum_even x + 64 sum_odd x) (even / odd: position of k in
+// its packed word), so
+//   y += (s 2^-e) D + (min X - s T),  X = sum_g x,  T = 1024 sum_even x + 64 sum_odd x,
+// with X, T and 2^-e computed once per CTA in fp32.
+//
+// Launch shape:
+//   * work units = (slab of W = 64, 96 or 128 columns, k-range); W is chosen so that the
+//     slabs spread evenly over the SMs (N = 14336 -> 150 slabs of 96); with a workspace a
+//     slab's K range may be split across CTAs. Grid <= SM count, CTA c takes units c, c+G..;
+//   * a producer warp streams each unit in chunks of W columns x 24 / (W / 32) groups (48 KB
+//     of packed words + scales + minimums) into a shared-memory ring with TMA, starting
+//     before it waits for the previous kernel on the stream (programmatic dependent launch;
+//     weights are not written by the kernels it overlaps). One CTA per SM: a ring sized for
+//     two co-resident CTAs let the block scheduler place two CTAs of the same launch on one
+//     SM, which then set the launch's tail;
+//   * 24 consumer warps (6 per SM sub-partition, to hide the latency of the unpack ->
+//     multiply chains): warp w takes column quarter w % (W / 32) (32 columns) of group
+//     w / (W / 32) of each chunk. Lane (gq, c) = (lane / 4, lane % 4) reads packed row
+//     4b + c of block b (b = 0..3) and columns 4gq..4gq+3 with one 16-byte shared load; its
+//     four words fill the A fragments of two 16-row MMA tiles (tile t: rows gq <- column
+//     4gq + 2t, gq + 8 <- column 4gq + 2t + 1); x waits in shared memory in B-fragment
+//     order (the lanes' offsets are fixed per warp; blocks and stages add constants);
+//   * per unit the group partials of each column are summed in a fixed order; a split slab
 //     writes fp32 partials and the last CTA to arrive (arrival counter) sums them in split
 //     order (deterministic, no float atomics) and resets the counter.
 #include "common.cuh"
@@ -46,88 +54,112 @@
 namespace w4k {
 namespace {
 
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 24;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kSlabCols = 128;
-constexpr int kChunkRows = 64;                                     // packed rows (512 k)
-constexpr int kChunkGroups = kChunkRows / 16;                      // 4 groups of 128
-constexpr uint32_t kChunkWordBytes = kChunkRows * kSlabCols * 4;   // 32 KB
-constexpr uint32_t kChunkRowBytes = kChunkGroups * kSlabCols * 2;  // 1 KB (scales or mins)
-constexpr uint32_t kChunkBytes = kChunkWordBytes + 2 * kChunkRowBytes;
 constexpr int kMaxRows = 8;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kSmemOneCta = 227u * 1024u;
 
-static_assert(kChunkGroups * (kSlabCols / 32) == kConsumerWarps, "one (group, quarter) per warp");
-
-template <int MR>
-struct GemvSmem {
-  // Weights in flight per SM: 6 x 34 KB at M = 1, fewer stages as x grows with M.
-  static constexpr int kStages = MR <= 1 ? 6 : MR <= 2 ? 5 : MR <= 4 ? 4 : 3;
-  static constexpr uint32_t ring = kStages * kChunkBytes;
-  static constexpr uint32_t red_off = ring;  // [kConsumerWarps][MR][32] floats
-  static constexpr uint32_t xsum_off = red_off + kConsumerWarps * MR * 32 * 4;
-  // x in B-fragment order: per packed row R and batch row m, 16 bytes
-  // {(x0, x4), (x1, x5), (x2, x6), (x3, x7)} of x[m, 8R .. 8R + 8).
-  __host__ __device__ static uint32_t xperm_off(int K) {
-    return (xsum_off + MR * (K >> 7) * 4u + 15u) & ~15u;
-  }
-  // mbarriers need 8-byte alignment.
-  __host__ __device__ static uint32_t bar_off(int K) { return xperm_off(K) + 2u * MR * K; }
-  __host__ __device__ static uint32_t total(int K) { return bar_off(K) + (2 * kStages) * 8 + 16; }
+// Slab of W = 32 QW columns; a chunk holds GPC groups of 128 k (16 packed rows each) so that
+// every consumer warp owns one (group, column quarter).
+template <int QW>
+struct Shape {
+  static constexpr int W = 32 * QW;
+  static constexpr int GPC = kConsumerWarps / QW;
+  static constexpr int ROWS = 16 * GPC;
+  static constexpr uint32_t word_bytes = static_cast<uint32_t>(W) * ROWS * 4u;  // 48 KB
+  static constexpr uint32_t row_bytes = static_cast<uint32_t>(GPC) * W * 2u;    // scales
+  static constexpr uint32_t stage_bytes = word_bytes + 2u * row_bytes;
+  static_assert(GPC * QW == kConsumerWarps, "one (group, quarter) per consumer warp");
+  static_assert(stage_bytes % 128u == 0u, "TMA destinations stay 128-byte aligned");
 };
 
-// D += A (16x16, BF16) * B (16x8, BF16), fp32 accumulators; fragment layout of mma.sync
+// Shared-memory layout: ring, per-warp partials, per-(row, group) constants of x, x in
+// B-fragment order, barriers.
+struct GemvLayout {
+  uint32_t red_off, cst_off, xperm_off, bar_off, total;
+  __host__ __device__ GemvLayout(uint32_t stage_bytes, int rows_pad, int MR, int G, int stages) {
+    red_off = static_cast<uint32_t>(stages) * stage_bytes;               // [24][MR][32] fp32
+    cst_off = red_off + kConsumerWarps * MR * 32u * 4u;                  // X, T, U: [3][MR][G]
+    xperm_off = (cst_off + 3u * MR * G * 4u + 15u) & ~15u;               // [rows_pad][MR] 16 B
+    bar_off = (xperm_off + static_cast<uint32_t>(rows_pad) * MR * 16u + 7u) & ~7u;
+    total = bar_off + 2u * kMaxStages * 8u + 16u;
+  }
+};
+
+// (1024 + q) / (1024 + 16 q) FP16 pairs for the 8 codes of `w` (q_j in bits 4j..4j+3):
+// p0 = (q0, q4), p1 = (16 q1, 16 q5), p2 = (q2, q6), p3 = (16 q3, 16 q7).
+__device__ __forceinline__ void code_pairs_f16(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t w8 = w >> 8;
+  p[0] = (w & 0x000F000Fu) | 0x64006400u;
+  p[1] = (w & 0x00F000F0u) | 0x64006400u;
+  p[2] = (w8 & 0x000F000Fu) | 0x64006400u;
+  p[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+}
+
+// D += A (16x16, FP16) * B (16x8, FP16), fp32 accumulators; fragment layout of mma.sync
 // m16n8k16 (row-major A, column-major B).
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// (128 + q_i, 128 + q_{i+4}) as a BF16 pair, for the 8 codes of `w`.
-__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {
-  p[0] = (w & 0x000F000Fu) | 0x43004300u;
-  p[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-  p[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-  p[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
 struct GemvMaps {
-  CUtensorMap qw;      // int32 [K/8, N], box {128, 64}
-  CUtensorMap scales;  // bf16 [K/128, N], box {128, 4}
-  CUtensorMap mins;    // bf16 [K/128, N], box {128, 4}
+  CUtensorMap qw;      // int32 [K/8, N], box {W, ROWS}
+  CUtensorMap scales;  // bf16 [K/128, N], box {W, GPC}
+  CUtensorMap mins;    // bf16 [K/128, N], box {W, GPC}
 };
 
-template <int MR>
+template <int MR, int QW>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_w4a16_kernel(const __grid_constant__ GemvMaps maps, const uint16_t* __restrict__ x,
-                      uint16_t* __restrict__ y, int M, int N, int K, int splits,
+                      uint16_t* __restrict__ y, int M, int N, int K, int stages, int splits,
                       float* __restrict__ ws_partial, uint32_t* __restrict__ ws_counter,
                       uint32_t* __restrict__ status, uint64_t limit_ns) {
   static_assert(MR <= 8, "one n8 tile of batch rows");
-  using L = GemvSmem<MR>;
-  constexpr int kStages = L::kStages;
+  using S = Shape<QW>;
+  constexpr int W = S::W, GPC = S::GPC, ROWS = S::ROWS;
+  const int G = K >> 7;
+  const int kchunks = (G + GPC - 1) / GPC;
+  const int rows_pad = kchunks * ROWS;
+  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages);
   extern __shared__ __align__(128) uint8_t smem[];
-  float* sRed = reinterpret_cast<float*>(smem + L::red_off);
-  float* sXsum = reinterpret_cast<float*>(smem + L::xsum_off);       // [MR][G]
-  uint4* sXperm = reinterpret_cast<uint4*>(smem + L::xperm_off(K));  // [K/8][MR]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bar_off(K));
-  uint64_t* empty = full + kStages;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kStages);
+  float* sRed = reinterpret_cast<float*>(smem + L.red_off);
+  float* sX = reinterpret_cast<float*>(smem + L.cst_off);  // [MR][G] sum x
+  float* sT = sX + MR * G;                                  // [MR][G] 1024 sum_even + 64 sum_odd
+  float* sU = sT + MR * G;                                  // [MR][G] 2^-e
+  uint4* sXperm = reinterpret_cast<uint4*>(smem + L.xperm_off);  // [rows_pad][MR]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + kMaxStages;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kMaxStages);
   volatile uint32_t* last_flag = abort_flag + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = K >> 7;
-  const int kchunks = (K / 8 + kChunkRows - 1) / kChunkRows;
   const int per_unit = (kchunks + splits - 1) / splits;  // chunks per k-range
-  const int nslab = (N + kSlabCols - 1) / kSlabCols;
+  const int nslab = (N + W - 1) / W;
   const int nunits = nslab * splits;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -141,34 +173,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer warp: weights only, no wait on the previous kernel -------
     if (lane == 0) {
       tma_prefetch_desc(&maps.qw);
+      tma_prefetch_desc(&maps.scales);
+      tma_prefetch_desc(&maps.mins);
       int j = 0;
-      bool stop = false;
-      for (int u = blockIdx.x; u < nunits && !stop; u += gridDim.x) {
-        const int slab = u / splits, kr = u - (u / splits) * splits;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int slab = u / splits, kr = u - slab * splits;
         const int kc_end = min(kchunks, (kr + 1) * per_unit);
         for (int kc = kr * per_unit; kc < kc_end; ++kc, ++j) {
-          const int s = j % kStages;
-          if (j >= kStages && !mbar_wait_bounded(&empty[s], ((j / kStages) - 1) & 1u, abort_flag,
-                                                 status, limit_ns)) {
-            stop = true;
+          const int s = j % stages;
+          const uint32_t use = static_cast<uint32_t>(j / stages);
+          if (use > 0 &&
+              !mbar_wait_bounded(&empty[s], (use - 1) & 1u, abort_flag, status, limit_ns)) {
+            ok = false;
             break;
           }
-          uint8_t* buf = smem + s * kChunkBytes;
-          mbar_arrive_expect_tx(&full[s], kChunkBytes);
-          tma_load_2d(buf, &maps.qw, &full[s], slab * kSlabCols, kc * kChunkRows);
-          tma_load_2d(buf + kChunkWordBytes, &maps.scales, &full[s], slab * kSlabCols,
-                      kc * kChunkGroups);
-          tma_load_2d(buf + kChunkWordBytes + kChunkRowBytes, &maps.mins, &full[s],
-                      slab * kSlabCols, kc * kChunkGroups);
+          uint8_t* buf = smem + s * S::stage_bytes;
+          mbar_arrive_expect_tx(&full[s], S::stage_bytes);
+          tma_load_2d(buf, &maps.qw, &full[s], slab * W, kc * ROWS);
+          tma_load_2d(buf + S::word_bytes, &maps.scales, &full[s], slab * W, kc * GPC);
+          tma_load_2d(buf + S::word_bytes + S::row_bytes, &maps.mins, &full[s], slab * W,
+                      kc * GPC);
         }
       }
       // Stay until this CTA's last copies have landed (bounded), so none is in flight
       // when the CTA exits, whatever the consumers did.
       const int issued = j;
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int last = issued - 1 - ((issued - 1 - s) % kStages);
+      for (int s = 0; s < stages && s < issued; ++s) {
+        const int last = (issued - 1 - s) / stages;  // last use of stage s
         volatile uint32_t no_abort = 0u;
-        mbar_wait_bounded(&full[s], (last / kStages) & 1u, &no_abort, status, limit_ns);
+        mbar_wait_bounded(&full[s], static_cast<uint32_t>(last) & 1u, &no_abort, status,
+                          limit_ns);
       }
     }
     return;
@@ -176,58 +211,102 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------- consumer warps ----------------
   pdl_wait();  // x, y and the workspace may belong to the previous kernel on the stream
-  // Group sums of x, one warp per (row, group), fixed reduction order.
-  for (int it = warp; it < MR * G; it += kConsumerWarps) {
-    const int mm = it / G, g = it - mm * G;
-    float v = 0.f;
-    if (mm < M) {
-      const uint2 u2 = __ldg(reinterpret_cast<const uint2*>(
-          x + static_cast<size_t>(mm) * K + g * 128 + lane * 4));
-      v = (bf16_bits_to_f32(u2.x & 0xFFFFu) + __uint_as_float(u2.x & 0xFFFF0000u)) +
-          (bf16_bits_to_f32(u2.y & 0xFFFFu) + __uint_as_float(u2.y & 0xFFFF0000u));
-    }
+  {
+    // x -> FP16 in B-fragment order, per (row m, group g) scale 2^e and the sums X, T.
+    // Item i = m * rows_pad + R (R fastest): the 16 lanes of a group are adjacent.
+    const int rows = K >> 3;
+    const int items = MR * rows_pad;
+    const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
+    // Loads of up to 4 items per thread are issued before any of them is used.
+    for (int base = 0; base < items_pad; base += 4 * kConsumers) {
+      uint4 xin[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) sXsum[it] = v;
-  }
-  // x in B-fragment order.
-  for (int i = tid; i < (K >> 3) * MR; i += kConsumers) {
-    const int R = i / MR, mm = i - R * MR;
-    uint4 e = make_uint4(0u, 0u, 0u, 0u);
-    if (mm < M) {
-      const uint4 xv =
-          __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(mm) * K + 8 * R));
-      e.x = __byte_perm(xv.x, xv.z, 0x5410);  // (x0, x4)
-      e.y = __byte_perm(xv.x, xv.z, 0x7632);  // (x1, x5)
-      e.z = __byte_perm(xv.y, xv.w, 0x5410);  // (x2, x6)
-      e.w = __byte_perm(xv.y, xv.w, 0x7632);  // (x3, x7)
+      for (int t = 0; t < 4; ++t) {
+        const int i = base + t * kConsumers + tid;
+        const int m = i / rows_pad, R = i - m * rows_pad;
+        xin[t] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < items && m < M && R < rows)
+          xin[t] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(m) * K + 8 * R));
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = base + t * kConsumers + tid;
+        if (i >= items_pad) break;  // warp-uniform: items_pad and the strides are multiples of 32
+        const int m = i / rows_pad, R = i - m * rows_pad;
+        float v[8];
+        const uint32_t xw[4] = {xin[t].x, xin[t].y, xin[t].z, xin[t].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[2 * h] = bf16_bits_to_f32(xw[h] & 0xFFFFu);
+          v[2 * h + 1] = __uint_as_float(xw[h] & 0xFFFF0000u);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+        float sum_even = (v[0] + v[2]) + (v[4] + v[6]);
+        float sum_odd = (v[1] + v[3]) + (v[5] + v[7]);
+        float sum = sum_even + sum_odd;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          sum_even += __shfl_xor_sync(0xffffffffu, sum_even, o);
+          sum_odd += __shfl_xor_sync(0xffffffffu, sum_odd, o);
+        }
+        // amax 2^e in [2^14, 2^15): e = 141 - biased exponent, kept where 2^e is a normal
+        // float; an all-zero group keeps e = 0.
+        int e = 0;
+        if (amax > 0.f)
+          e = max(-100, min(100, 141 - static_cast<int>(__float_as_uint(amax) >> 23)));
+        const float lo = pow2f(e), hi = pow2f(e - 4);
+        if (i < items) {
+          uint4 out;
+          out.x = f16x2_bits(v[0] * lo, v[4] * lo);  // (x0, x4) 2^e
+          out.y = f16x2_bits(v[1] * hi, v[5] * hi);  // (x1, x5) 2^(e-4)
+          out.z = f16x2_bits(v[2] * lo, v[6] * lo);  // (x2, x6) 2^e
+          out.w = f16x2_bits(v[3] * hi, v[7] * hi);  // (x3, x7) 2^(e-4)
+          sXperm[R * MR + m] = out;
+          if ((R & 15) == 0 && R < rows) {
+            const int g = R >> 4;
+            sX[m * G + g] = sum;
+            sT[m * G + g] = fmaf(1024.0f, sum_even, 64.0f * sum_odd);
+            sU[m * G + g] = pow2f(-e);
+          }
+        }
+      }
     }
-    sXperm[i] = e;
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  consumer_bar();
 
   const int gq = lane >> 2, c = lane & 3;
-  const int q4 = warp & 3, gl = warp >> 2;  // column quarter, group within a chunk
-  int j = 0;
+  const int qq = warp % QW, gl = warp / QW;  // column quarter, group within a chunk
+  // Per-lane constant offsets: block b of a chunk adds b * 4 rows (compile-time strides).
+  const int row0 = gl * 16 + c;  // packed row of block 0 in the chunk
+  const uint32_t w_off = static_cast<uint32_t>(row0 * (W * 4) + qq * 128 + gq * 16);
+  const uint32_t s_off = S::word_bytes + static_cast<uint32_t>(gl * (W * 2) + (qq * 32 + gq * 4) * 2);
+  // B fragment: batch row gq; product columns gq >= MR are never read, so those lanes may
+  // load any existing row.
+  const uint4* x_lane = sXperm + row0 * MR + (gq & (MR - 1));
+  int s = 0;
+  uint32_t phase = 0u;  // ring position of the next chunk
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-    const int slab = u / splits, kr = u - (u / splits) * splits;
+    const int slab = u / splits, kr = u - slab * splits;
     const int kc_end = min(kchunks, (kr + 1) * per_unit);
-    // yacc[col jj][bb]: column slab*128 + 32*q4 + 4*gq + jj, batch row 2c + bb
+    // yacc[col jj][bb]: column slab*W + 32*qq + 4*gq + jj, batch row 2c + bb
     float yacc[4][2];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) yacc[jj][0] = yacc[jj][1] = 0.f;
 
-    for (int kc = kr * per_unit; kc < kc_end; ++kc, ++j) {
-      const int s = j % kStages;
-      const int g = kc * kChunkGroups + gl;  // this warp's group
+    for (int kc = kr * per_unit; kc < kc_end; ++kc) {
+      const int g = kc * GPC + gl;  // this warp's group
       // On an expired wait every warp keeps walking the chunk list without computing, so
       // all consumer warps still meet at the per-unit barriers below.
-      const bool landed =
-          mbar_wait_bounded(&full[s], (j / kStages) & 1u, abort_flag, status, limit_ns);
-      const uint8_t* buf = smem + s * kChunkBytes;
+      const bool landed = mbar_wait_bounded(&full[s], phase, abort_flag, status, limit_ns);
+      const uint8_t* buf = smem + s * S::stage_bytes;
       if (landed && g < G) {
-        // Two independent accumulator chains (even / odd blocks).
-        float d[2][2][4];  // [chain][tile t][fragment]
+        const uint8_t* wp = buf + w_off;
+        const uint4* xp = x_lane + kc * (ROWS * MR);
+        float d[2][2][4];  // [chain][tile t][fragment]: even / odd blocks
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
@@ -236,37 +315,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int f = 0; f < 4; ++f) d[ch][t][f] = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const int rl = gl * 16 + b * 4 + c;  // packed row in the chunk
-          const int R = kc * kChunkRows + rl;  // global packed row
-          const uint4 wv = *reinterpret_cast<const uint4*>(buf + rl * 512 + q4 * 128 + gq * 16);
-          // B fragment: batch row gq (zero where that row does not exist)
-          const uint4 e =
-              gq < MR ? sXperm[R * MR + (gq < MR ? gq : 0)] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 wv = *reinterpret_cast<const uint4*>(wp + b * (4 * W * 4));
+          const uint4 e = xp[b * 4 * MR];
           uint32_t p[4][4];
-          code_pairs(wv.x, p[0]);
-          code_pairs(wv.y, p[1]);
-          code_pairs(wv.z, p[2]);
-          code_pairs(wv.w, p[3]);
+          code_pairs_f16(wv.x, p[0]);
+          code_pairs_f16(wv.y, p[1]);
+          code_pairs_f16(wv.z, p[2]);
+          code_pairs_f16(wv.w, p[3]);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             // rows gq <- column 4gq + 2t, rows gq + 8 <- column 4gq + 2t + 1
-            mma_bf16_16816(d[b & 1][t], p[2 * t][0], p[2 * t + 1][0], p[2 * t][1],
-                           p[2 * t + 1][1], e.x, e.y);
-            mma_bf16_16816(d[b & 1][t], p[2 * t][2], p[2 * t + 1][2], p[2 * t][3],
-                           p[2 * t + 1][3], e.z, e.w);
+            mma_f16_16816(d[b & 1][t], p[2 * t][0], p[2 * t + 1][0], p[2 * t][1],
+                          p[2 * t + 1][1], e.x, e.y);
+            mma_f16_16816(d[b & 1][t], p[2 * t][2], p[2 * t + 1][2], p[2 * t][3],
+                          p[2 * t + 1][3], e.z, e.w);
           }
         }
-        // Fold this group into y: y += s * D + (min - 128 s) * sum_g x, for batch rows that
-        // exist (row 2c + bb; lanes whose rows do not exist add zeros).
-        const uint32_t soff = kChunkWordBytes + gl * 256 + (q4 * 32 + gq * 4) * 2;
-        const uint2 s2 = *reinterpret_cast<const uint2*>(buf + soff);
-        const uint2 m2 = *reinterpret_cast<const uint2*>(buf + soff + kChunkRowBytes);
+        // Fold this group: y += (s 2^-e) D + (min X - s T) for the batch rows that exist
+        // (row 2c + bb; lanes whose rows do not exist add zeros).
+        const uint2 s2 = *reinterpret_cast<const uint2*>(buf + s_off);
+        const uint2 m2 = *reinterpret_cast<const uint2*>(buf + s_off + S::row_bytes);
         const uint32_t sw[2] = {s2.x, s2.y}, mw[2] = {m2.x, m2.y};
-        float xs[2];
+        float gx[2], gt[2], gu[2];
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int mrow = 2 * c + bb;
-          xs[bb] = (bb < MR && mrow < MR) ? sXsum[(mrow < MR ? mrow : 0) * G + g] : 0.f;
+          const bool ex = bb < MR && mrow < MR;
+          const int ci = (ex ? mrow : 0) * G + g;
+          gx[bb] = ex ? sX[ci] : 0.f;
+          gt[bb] = ex ? sT[ci] : 0.f;
+          gu[bb] = ex ? sU[ci] : 0.f;
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -274,21 +352,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               bf16_bits_to_f32((jj & 1) ? (sw[jj >> 1] >> 16) : (sw[jj >> 1] & 0xFFFFu));
           const float mn =
               bf16_bits_to_f32((jj & 1) ? (mw[jj >> 1] >> 16) : (mw[jj >> 1] & 0xFFFFu));
-          const float off = fmaf(-128.0f, sc, mn);
           const int t = jj >> 1, h = jj & 1;  // column 4gq + jj is tile t, fragment half h
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb) {
             if (bb >= MR) continue;  // no lane holds an existing row here
             const float dv = d[0][t][2 * h + bb] + d[1][t][2 * h + bb];
-            yacc[jj][bb] = fmaf(sc, dv, fmaf(off, xs[bb], yacc[jj][bb]));
+            yacc[jj][bb] =
+                fmaf(sc * gu[bb], dv, fmaf(mn, gx[bb], fmaf(-sc, gt[bb], yacc[jj][bb])));
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == stages) {
+        s = 0;
+        phase ^= 1u;
+      }
     }
 
-    // Unit done: warp partials to shared memory, fixed-order sum over the 4 groups of
+    // Unit done: warp partials to shared memory, fixed-order sum over the GPC groups of
     // each column quarter.
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj)
@@ -297,13 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mrow = 2 * c + bb;
         if (mrow < MR) sRed[(warp * MR + mrow) * 32 + gq * 4 + jj] = yacc[jj][bb];
       }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-    for (int i = tid; i < MR * kSlabCols; i += kConsumers) {
-      const int mm = i / kSlabCols, col = i - mm * kSlabCols, qq = col >> 5, c32 = col & 31;
+    consumer_bar();
+    for (int i = tid; i < MR * W; i += kConsumers) {
+      const int mm = i / W, col = i - mm * W, q = col >> 5, c32 = col & 31;
       float v = 0.f;
 #pragma unroll
-      for (int gg = 0; gg < kChunkGroups; ++gg) v += sRed[((gg * 4 + qq) * MR + mm) * 32 + c32];
-      const int nn = slab * kSlabCols + col;
+      for (int gg = 0; gg < GPC; ++gg) v += sRed[((gg * QW + q) * MR + mm) * 32 + c32];
+      const int nn = slab * W + col;
       if (mm < M && nn < N) {
         if (splits == 1)
           y[static_cast<size_t>(mm) * N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -313,15 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (splits > 1) {
       __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+      consumer_bar();
       if (tid == 0)
         *last_flag = (atomicAdd(ws_counter + slab, 1u) + 1u == static_cast<uint32_t>(splits));
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+      consumer_bar();
       if (*last_flag) {
         __threadfence();
-        for (int i = tid; i < MR * kSlabCols; i += kConsumers) {
-          const int mm = i / kSlabCols, col = i - mm * kSlabCols;
-          const int nn = slab * kSlabCols + col;
+        for (int i = tid; i < MR * W; i += kConsumers) {
+          const int mm = i / W, col = i - mm * W;
+          const int nn = slab * W + col;
           if (mm < M && nn < N) {
             float v = 0.f;
             for (int z = 0; z < splits; ++z)
@@ -332,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) ws_counter[slab] = 0u;  // ready for the next call
       }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    consumer_bar();
   }
 }
 
@@ -379,55 +461,100 @@ int sm_count() {
 
 int mr_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
+// Slab width 32 qw: the fewest columns per SM in the busiest round; ties go to wider slabs.
+int choose_qw(int N, int sms) {
+  int best = 4, best_cost = 0;
+  for (int qw = 4; qw >= 2; --qw) {
+    const int w = 32 * qw, nslab = (N + w - 1) / w;
+    const int cost = ((nslab + sms - 1) / sms) * w;
+    if (qw == 4 || cost < best_cost) {
+      best = qw;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+uint32_t stage_bytes_of(int qw) {
+  return qw == 4 ? Shape<4>::stage_bytes : qw == 3 ? Shape<3>::stage_bytes : Shape<2>::stage_bytes;
+}
+int gpc_of(int qw) { return kConsumerWarps / qw; }
+
+// Ring depth: as deep as fits beside x and the partials.
+int stages_for(int MR, int K, int qw) {
+  const int G = K >> 7, gpc = gpc_of(qw);
+  const int rows_pad = ((G + gpc - 1) / gpc) * 16 * gpc;
+  const uint32_t sb = stage_bytes_of(qw);
+  const uint32_t fixed = GemvLayout(sb, rows_pad, MR, G, 0).total;
+  if (fixed >= kSmemOneCta) return 0;
+  const int s = static_cast<int>((kSmemOneCta - fixed) / sb);
+  return s > kMaxStages ? kMaxStages : s;
+}
+
+template <int MR, int QW>
+cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N,
+                         int K, const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
+                         int sms, cudaStream_t stream) {
+  using S = Shape<QW>;
+  const int stages = stages_for(MR, K, QW);
+  if (stages < 2) return cudaErrorInvalidValue;
+  const int G = K >> 7;
+  const int rows_pad = ((G + S::GPC - 1) / S::GPC) * S::ROWS;
+  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages);
+  auto kern = gemv_w4a16_kernel<MR, QW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L.total));
+  if (e != cudaSuccess) return e;
+  const int nunits = ((N + S::W - 1) / S::W) * split.splits;
+  dim3 grid(static_cast<unsigned>(nunits < sms ? nunits : sms));
+  return launch_with_pdl(kern, grid, dim3(kThreads), L.total, stream, maps, x, y, M, N, K,
+                         stages, split.splits, split.partial, split.counter, status, limit_ns);
+}
+
 template <int MR>
 cudaError_t launch_mr(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N, int K,
-                      const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
-                      cudaStream_t stream) {
-  using L = GemvSmem<MR>;
-  const uint32_t smem = L::total(K);
-  auto kern = gemv_w4a16_kernel<MR>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const int nunits = ((N + kSlabCols - 1) / kSlabCols) * split.splits;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  dim3 grid(static_cast<unsigned>(nunits < sms ? nunits : sms));
-  return launch_with_pdl(kern, grid, dim3(kThreads), smem, stream, maps, x, y, M, N, K,
-                         split.splits, split.partial, split.counter, status, limit_ns);
+                      int qw, const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
+                      int sms, cudaStream_t stream) {
+  switch (qw) {
+    case 4: return launch_shape<MR, 4>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
+    case 3: return launch_shape<MR, 3>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
+    default: return launch_shape<MR, 2>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
+  }
 }
 
 }  // namespace
 
 int gemv_max_rows() { return kMaxRows; }
 
-// x in fragment order and its group sums must fit in shared memory next to the ring.
+// x in B-fragment order and its per-group constants must leave room for a 2-stage ring.
 bool gemv_supports(int M, int K) {
-  if (M < 1 || M > kMaxRows) return false;
-  const uint32_t total = M <= 1 ? GemvSmem<1>::total(K)
-                         : M <= 2 ? GemvSmem<2>::total(K)
-                         : M <= 4 ? GemvSmem<4>::total(K)
-                                  : GemvSmem<8>::total(K);
-  return total <= 227u * 1024u;
+  if (M < 1 || M > kMaxRows || K < 128) return false;
+  const int sms = sm_count();
+  // The slab width depends on N; the narrowest slab has the largest x buffer per chunk.
+  return stages_for(mr_of(M), K, 2) >= 2 && stages_for(mr_of(M), K, 3) >= 2 &&
+         stages_for(mr_of(M), K, 4) >= 2 && sms >= 0;
 }
 
 GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed) {
   GemvSplit plan;
   *bytes_needed = 0;
   const int sms = sm_count();
-  const int nslab = (N + kSlabCols - 1) / kSlabCols;
-  const int kchunks = (K / 8 + kChunkRows - 1) / kChunkRows;
-  if (sms <= 0 || nslab >= sms) return plan;
-  // About three units per SM; each k-range at least one chunk.
-  int splits = (3 * sms + nslab - 1) / nslab;
+  if (sms <= 0) return plan;
+  const int qw = choose_qw(N, sms);
+  const int w = 32 * qw, gpc = gpc_of(qw);
+  const int nslab = (N + w - 1) / w;
+  const int kchunks = ((K >> 7) + gpc - 1) / gpc;
+  // One unit per CTA: split each slab's K range over the SMs the slabs leave idle.
+  int splits = sms / nslab;
   if (splits > kchunks) splits = kchunks;
   if (splits > 64) splits = 64;
+  if (splits < 2) return plan;
   const int per_unit = (kchunks + splits - 1) / splits;
   splits = (kchunks + per_unit - 1) / per_unit;  // no empty k-range
   if (splits < 2) return plan;
   plan.splits = splits;
-  const size_t counters = ((static_cast<size_t>(nslab) * 4 + 255) / 256) * 256;
-  *bytes_needed = counters + static_cast<size_t>(splits) * mr_of(M) * N * 4;
+  plan.partial_offset = ((static_cast<size_t>(nslab) * 4 + 255) / 256) * 256;
+  *bytes_needed = plan.partial_offset + static_cast<size_t>(splits) * mr_of(M) * N * 4;
   return plan;
 }
 
@@ -435,22 +562,26 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint1
                               const uint16_t* mins, uint16_t* y, int M, int N, int K,
                               const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
                               cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int q = choose_qw(N, sms);
+  const uint32_t w = 32u * q, gpc = static_cast<uint32_t>(gpc_of(q));
   GemvMaps maps;
   cudaError_t e;
   e = encode(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, kSlabCols, kChunkRows);
+             static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, w, 16u * gpc);
   if (e != cudaSuccess) return e;
   e = encode(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kSlabCols, kChunkGroups);
+             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc);
   if (e != cudaSuccess) return e;
   e = encode(&maps.mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kSlabCols, kChunkGroups);
+             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc);
   if (e != cudaSuccess) return e;
   switch (mr_of(M)) {
-    case 1: return launch_mr<1>(maps, x, y, M, N, K, split, status, limit_ns, stream);
-    case 2: return launch_mr<2>(maps, x, y, M, N, K, split, status, limit_ns, stream);
-    case 4: return launch_mr<4>(maps, x, y, M, N, K, split, status, limit_ns, stream);
-    default: return launch_mr<8>(maps, x, y, M, N, K, split, status, limit_ns, stream);
+    case 1: return launch_mr<1>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
+    case 2: return launch_mr<2>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
+    case 4: return launch_mr<4>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
+    default: return launch_mr<8>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
   }
 }
 

@@ -24,8 +24,8 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   cudaStream_t stream);
 
-// GEMV / skinny kernel for M <= 8 (weights staged by TMA, dequantised in registers into
-// mma.sync fragments). With a split plan (splits > 1) the K range of each 128-column slab
+// GEMV / skinny kernel for M <= 8 (weights staged by TMA, codes widened into tensor memory,
+// inner products on tcgen05.mma, per-group fold in fp32). With a split plan (splits > 1) the K range of each 128-column slab
 // is divided over thread blocks: fp32 partials [splits][mr][N] and one arrival counter per
 // slab (zero before the launch; the kernel leaves it zero). gemv_supports() tells whether
 // M and K fit its limits.
@@ -33,6 +33,7 @@ struct GemvSplit {
   int splits = 1;
   float* partial = nullptr;
   uint32_t* counter = nullptr;
+  size_t partial_offset = 0;  // bytes of the workspace before the partials (the counters)
 };
 int gemv_max_rows();
 bool gemv_supports(int M, int K);
