@@ -29,22 +29,27 @@
 // with X, T and 2^-e computed once per CTA in fp32.
 //
 // Launch shape:
-//   * work units = (slab of W = 64, 96 or 128 columns, k-range); W is chosen so that the
-//     slabs spread evenly over the SMs (N = 14336 -> 150 slabs of 96); with a workspace a
-//     slab's K range may be split across CTAs. Grid <= SM count, CTA c takes units c, c+G..;
-//   * a producer warp streams each unit in chunks of W columns x 24 / (W / 32) groups (48 KB
-//     of packed words + scales + minimums) into a shared-memory ring with TMA, starting
-//     before it waits for the previous kernel on the stream (programmatic dependent launch;
-//     weights are not written by the kernels it overlaps). One CTA per SM: a ring sized for
-//     two co-resident CTAs let the block scheduler place two CTAs of the same launch on one
-//     SM, which then set the launch's tail;
-//   * 24 consumer warps (6 per SM sub-partition, to hide the latency of the unpack ->
-//     multiply chains): warp w takes column quarter w % (W / 32) (32 columns) of group
-//     w / (W / 32) of each chunk. Lane (gq, c) = (lane / 4, lane % 4) reads packed row
-//     4b + c of block b (b = 0..3) and columns 4gq..4gq+3 with one 16-byte shared load; its
-//     four words fill the A fragments of two 16-row MMA tiles (tile t: rows gq <- column
-//     4gq + 2t, gq + 8 <- column 4gq + 2t + 1); x waits in shared memory in B-fragment
-//     order (the lanes' offsets are fixed per warp; blocks and stages add constants);
+//   * even mode (N >= 48 columns per SM): exactly one CTA per SM, CTA c owns 8 q or
+//     8 (q + 1) consecutive columns (N = 14336: 120 CTAs of 96, 32 of 88) and all of K. Its
+//     shared-memory ring leaves room for a second CTA on the SM, which is the next launch's:
+//     with one CTA per SM in every launch the block scheduler has exactly one free slot per
+//     SM for the next launch, so no SM runs two CTAs of one launch (with more CTAs than SMs
+//     and room for two per SM, a launch's CTAs doubled up on a few SMs and set its tail);
+//   * slab mode (narrow N, or N too wide for 128 columns per SM): slabs of W = 64, 96 or 128
+//     columns, persistent grid (<= one CTA per SM, CTA c takes units c, c + G, ...), one
+//     CTA per SM; with a workspace a slab's K range may be split across CTAs;
+//   * a producer warp streams each unit in chunks of W columns x (consumer warps) / (W / 32)
+//     groups (1 KB of packed words per consumer warp, plus scales and minimums) into the
+//     ring with TMA, starting before it waits for the previous kernel on the stream
+//     (programmatic dependent launch; weights are not written by the kernels it overlaps),
+//     so in even mode the next launch's weights stream while this launch computes;
+//   * 12 (even mode) or 24 (slab mode) consumer warps: warp w takes column quarter
+//     w % (W / 32) (32 columns) of group w / (W / 32) of each chunk. Lane (gq, c) =
+//     (lane / 4, lane % 4) reads packed row 4b + c of block b (b = 0..3) and columns
+//     4gq..4gq+3 with one 16-byte shared load; its four words fill the A fragments of two
+//     16-row MMA tiles (tile t: rows gq <- column 4gq + 2t, gq + 8 <- column 4gq + 2t + 1);
+//     x waits in shared memory in B-fragment order (the lanes' offsets are fixed per warp;
+//     blocks and stages add constants);
 //   * per unit the group partials of each column are summed in a fixed order; a split slab
 //     writes fp32 partials and the last CTA to arrive (arrival counter) sums them in split
 //     order (deterministic, no float atomics) and resets the counter.
@@ -54,24 +59,27 @@
 namespace w4k {
 namespace {
 
-constexpr int kConsumerWarps = 24;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxRows = 8;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kSmemOneCta = 227u * 1024u;
+constexpr uint32_t kSmemTwoCtas = 113u * 1024u;  // two CTAs (and their reserves) per SM
 
 // Slab of W = 32 QW columns; a chunk holds GPC groups of 128 k (16 packed rows each) so that
 // every consumer warp owns one (group, column quarter).
-template <int QW>
+// CW consumer warps + one producer warp. 12 consumer warps leave room (registers, shared
+// memory) for a second CTA on the SM, 24 do not.
+template <int QW, int CW>
 struct Shape {
+  static constexpr int kConsumers = CW * 32;
+  static constexpr int kThreads = kConsumers + 32;
+  static constexpr int kMinBlocks = CW <= 12 ? 2 : 1;
   static constexpr int W = 32 * QW;
-  static constexpr int GPC = kConsumerWarps / QW;
+  static constexpr int GPC = CW / QW;
   static constexpr int ROWS = 16 * GPC;
-  static constexpr uint32_t word_bytes = static_cast<uint32_t>(W) * ROWS * 4u;  // 48 KB
+  static constexpr uint32_t word_bytes = static_cast<uint32_t>(W) * ROWS * 4u;  // 1 KB x CW
   static constexpr uint32_t row_bytes = static_cast<uint32_t>(GPC) * W * 2u;    // scales
   static constexpr uint32_t stage_bytes = word_bytes + 2u * row_bytes;
-  static_assert(GPC * QW == kConsumerWarps, "one (group, quarter) per consumer warp");
+  static_assert(GPC * QW == CW, "one (group, quarter) per consumer warp");
   static_assert(stage_bytes % 128u == 0u, "TMA destinations stay 128-byte aligned");
 };
 
@@ -79,9 +87,10 @@ struct Shape {
 // B-fragment order, barriers.
 struct GemvLayout {
   uint32_t red_off, cst_off, xperm_off, bar_off, total;
-  __host__ __device__ GemvLayout(uint32_t stage_bytes, int rows_pad, int MR, int G, int stages) {
-    red_off = static_cast<uint32_t>(stages) * stage_bytes;               // [24][MR][32] fp32
-    cst_off = red_off + kConsumerWarps * MR * 32u * 4u;                  // X, T, U: [3][MR][G]
+  __host__ __device__ GemvLayout(uint32_t stage_bytes, int rows_pad, int MR, int G, int stages,
+                                 int CW) {
+    red_off = static_cast<uint32_t>(stages) * stage_bytes;               // [CW][MR][32] fp32
+    cst_off = red_off + static_cast<uint32_t>(CW) * MR * 32u * 4u;       // X, T, U: [3][MR][G]
     xperm_off = (cst_off + 3u * MR * G * 4u + 15u) & ~15u;               // [rows_pad][MR] 16 B
     bar_off = (xperm_off + static_cast<uint32_t>(rows_pad) * MR * 16u + 7u) & ~7u;
     total = bar_off + 2u * kMaxStages * 8u + 16u;
@@ -119,8 +128,9 @@ __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
   return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
 }
 
+template <int NC>
 __device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
 }
 
 struct GemvMaps {
@@ -129,19 +139,20 @@ struct GemvMaps {
   CUtensorMap mins;    // bf16 [K/128, N], box {W, GPC}
 };
 
-template <int MR, int QW>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MR, int QW, int CW>
+__global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBlocks)
     gemv_w4a16_kernel(const __grid_constant__ GemvMaps maps, const uint16_t* __restrict__ x,
                       uint16_t* __restrict__ y, int M, int N, int K, int stages, int splits,
-                      float* __restrict__ ws_partial, uint32_t* __restrict__ ws_counter,
-                      uint32_t* __restrict__ status, uint64_t limit_ns) {
+                      int col_q, int col_r, float* __restrict__ ws_partial,
+                      uint32_t* __restrict__ ws_counter, uint32_t* __restrict__ status,
+                      uint64_t limit_ns) {
   static_assert(MR <= 8, "one n8 tile of batch rows");
-  using S = Shape<QW>;
-  constexpr int W = S::W, GPC = S::GPC, ROWS = S::ROWS;
+  using S = Shape<QW, CW>;
+  constexpr int W = S::W, GPC = S::GPC, ROWS = S::ROWS, NC = S::kConsumers;
   const int G = K >> 7;
   const int kchunks = (G + GPC - 1) / GPC;
   const int rows_pad = kchunks * ROWS;
-  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages);
+  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages, CW);
   extern __shared__ __align__(128) uint8_t smem[];
   float* sRed = reinterpret_cast<float*>(smem + L.red_off);
   float* sX = reinterpret_cast<float*>(smem + L.cst_off);  // [MR][G] sum x
@@ -155,13 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int per_unit = (kchunks + splits - 1) / splits;  // chunks per k-range
-  const int nslab = (N + W - 1) / W;
+  // Slabs: W columns each, or (col_q > 0) one per CTA with 8 col_q or 8 (col_q + 1)
+  // columns, the first col_r slabs wider, so that every SM gets the same share of N.
+  const int nslab = col_q > 0 ? static_cast<int>(gridDim.x) : (N + W - 1) / W;
   const int nunits = nslab * splits;
+  auto slab_col0 = [&](int slab) {
+    return col_q > 0 ? 8 * (slab * col_q + min(slab, col_r)) : slab * W;
+  };
+  auto slab_cols = [&](int slab) {
+    return col_q > 0 ? 8 * (col_q + (slab < col_r ? 1 : 0)) : W;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], CW);
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ---------------- producer warp: weights only, no wait on the previous kernel -------
     if (lane == 0) {
       tma_prefetch_desc(&maps.qw);
@@ -190,9 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* buf = smem + s * S::stage_bytes;
           mbar_arrive_expect_tx(&full[s], S::stage_bytes);
-          tma_load_2d(buf, &maps.qw, &full[s], slab * W, kc * ROWS);
-          tma_load_2d(buf + S::word_bytes, &maps.scales, &full[s], slab * W, kc * GPC);
-          tma_load_2d(buf + S::word_bytes + S::row_bytes, &maps.mins, &full[s], slab * W,
+          const int col0 = slab_col0(slab);
+          tma_load_2d(buf, &maps.qw, &full[s], col0, kc * ROWS);
+          tma_load_2d(buf + S::word_bytes, &maps.scales, &full[s], col0, kc * GPC);
+          tma_load_2d(buf + S::word_bytes + S::row_bytes, &maps.mins, &full[s], col0,
                       kc * GPC);
         }
       }
@@ -218,11 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int items = MR * rows_pad;
     const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
     // Loads of up to 4 items per thread are issued before any of them is used.
-    for (int base = 0; base < items_pad; base += 4 * kConsumers) {
+    for (int base = 0; base < items_pad; base += 4 * NC) {
       uint4 xin[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = base + t * kConsumers + tid;
+        const int i = base + t * NC + tid;
         const int m = i / rows_pad, R = i - m * rows_pad;
         xin[t] = make_uint4(0u, 0u, 0u, 0u);
         if (i < items && m < M && R < rows)
@@ -230,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = base + t * kConsumers + tid;
+        const int i = base + t * NC + tid;
         if (i >= items_pad) break;  // warp-uniform: items_pad and the strides are multiples of 32
         const int m = i / rows_pad, R = i - m * rows_pad;
         float v[8];
@@ -276,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  consumer_bar();
+  consumer_bar<NC>();
 
   const int gq = lane >> 2, c = lane & 3;
   const int qq = warp % QW, gl = warp / QW;  // column quarter, group within a chunk
@@ -292,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
     const int slab = u / splits, kr = u - slab * splits;
     const int kc_end = min(kchunks, (kr + 1) * per_unit);
-    // yacc[col jj][bb]: column slab*W + 32*qq + 4*gq + jj, batch row 2c + bb
+    const int col0 = slab_col0(slab), col_end = min(N, col0 + slab_cols(slab));
+    // yacc[col jj][bb]: column col0 + 32*qq + 4*gq + jj, batch row 2c + bb
     float yacc[4][2];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) yacc[jj][0] = yacc[jj][1] = 0.f;
@@ -379,14 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mrow = 2 * c + bb;
         if (mrow < MR) sRed[(warp * MR + mrow) * 32 + gq * 4 + jj] = yacc[jj][bb];
       }
-    consumer_bar();
-    for (int i = tid; i < MR * W; i += kConsumers) {
+    consumer_bar<NC>();
+    for (int i = tid; i < MR * W; i += NC) {
       const int mm = i / W, col = i - mm * W, q = col >> 5, c32 = col & 31;
       float v = 0.f;
 #pragma unroll
       for (int gg = 0; gg < GPC; ++gg) v += sRed[((gg * QW + q) * MR + mm) * 32 + c32];
-      const int nn = slab * W + col;
-      if (mm < M && nn < N) {
+      const int nn = col0 + col;
+      if (mm < M && nn < col_end) {
         if (splits == 1)
           y[static_cast<size_t>(mm) * N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         else
@@ -395,16 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (splits > 1) {
       __threadfence();
-      consumer_bar();
+      consumer_bar<NC>();
       if (tid == 0)
         *last_flag = (atomicAdd(ws_counter + slab, 1u) + 1u == static_cast<uint32_t>(splits));
-      consumer_bar();
+      consumer_bar<NC>();
       if (*last_flag) {
         __threadfence();
-        for (int i = tid; i < MR * W; i += kConsumers) {
+        for (int i = tid; i < MR * W; i += NC) {
           const int mm = i / W, col = i - mm * W;
-          const int nn = slab * W + col;
-          if (mm < M && nn < N) {
+          const int nn = col0 + col;
+          if (mm < M && nn < col_end) {
             float v = 0.f;
             for (int z = 0; z < splits; ++z)
               v += __ldcg(ws_partial + (static_cast<size_t>(z) * MR + mm) * N + nn);
@@ -414,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) ws_counter[slab] = 0u;  // ready for the next call
       }
     }
-    consumer_bar();
+    consumer_bar<NC>();
   }
 }
 
@@ -475,87 +496,130 @@ int choose_qw(int N, int sms) {
   return best;
 }
 
-uint32_t stage_bytes_of(int qw) {
-  return qw == 4 ? Shape<4>::stage_bytes : qw == 3 ? Shape<3>::stage_bytes : Shape<2>::stage_bytes;
-}
-int gpc_of(int qw) { return kConsumerWarps / qw; }
+// How a launch covers N. Even mode (col_q > 0): one CTA per SM, CTA c owns 8 col_q or
+// 8 (col_q + 1) columns, and the ring leaves room for the next launch's CTA on the same SM
+// (12 consumer warps); with exactly one CTA per SM in every launch, the block scheduler
+// has one free slot per SM for the next launch, so no SM ever runs two CTAs of one launch.
+// Slab mode: slabs of 32 qw columns, persistent grid, 24 consumer warps, one CTA per SM.
+struct GemvPlan {
+  int qw = 4, cw = 24, col_q = 0, col_r = 0, nslab = 0;
+};
 
-// Ring depth: as deep as fits beside x and the partials.
-int stages_for(int MR, int K, int qw) {
-  const int G = K >> 7, gpc = gpc_of(qw);
-  const int rows_pad = ((G + gpc - 1) / gpc) * 16 * gpc;
-  const uint32_t sb = stage_bytes_of(qw);
-  const uint32_t fixed = GemvLayout(sb, rows_pad, MR, G, 0).total;
-  if (fixed >= kSmemOneCta) return 0;
-  const int s = static_cast<int>((kSmemOneCta - fixed) / sb);
+GemvPlan make_plan(int N, int sms) {
+  GemvPlan p;
+  const int n8 = N / 8, q = n8 / sms, r = n8 % sms;
+  const int maxw = 8 * (q + (r > 0 ? 1 : 0));
+  if (q >= 6 && maxw <= 128) {
+    p.qw = maxw <= 64 ? 2 : maxw <= 96 ? 3 : 4;
+    p.cw = 12;
+    p.col_q = q;
+    p.col_r = r;
+    p.nslab = sms;
+  } else {
+    p.qw = choose_qw(N, sms);
+    p.nslab = (N + 32 * p.qw - 1) / (32 * p.qw);
+  }
+  return p;
+}
+
+template <int QW, int CW>
+uint32_t fixed_smem(int MR, int K) {
+  using S = Shape<QW, CW>;
+  const int G = K >> 7;
+  const int rows_pad = ((G + S::GPC - 1) / S::GPC) * S::ROWS;
+  return GemvLayout(S::stage_bytes, rows_pad, MR, G, 0, CW).total;
+}
+
+// Ring depth: as deep as the budget allows beside x and the partials (at most kMaxStages).
+template <int QW, int CW>
+int stages_for(int MR, int K, uint32_t budget) {
+  const uint32_t fixed = fixed_smem<QW, CW>(MR, K);
+  if (fixed >= budget) return 0;
+  const int s = static_cast<int>((budget - fixed) / Shape<QW, CW>::stage_bytes);
   return s > kMaxStages ? kMaxStages : s;
 }
 
-template <int MR, int QW>
+template <int QW, int CW>
+int stages_of(int MR, int K) {
+  // Two CTAs per SM when the ring can still hold two stages, else the whole SM.
+  const int two = CW <= 12 ? stages_for<QW, CW>(MR, K, kSmemTwoCtas) : 0;
+  return two >= 2 ? two : stages_for<QW, CW>(MR, K, kSmemOneCta);
+}
+
+template <int MR, int QW, int CW>
 cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N,
-                         int K, const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
-                         int sms, cudaStream_t stream) {
-  using S = Shape<QW>;
-  const int stages = stages_for(MR, K, QW);
+                         int K, const GemvSplit& split, const GemvPlan& plan, uint32_t* status,
+                         uint64_t limit_ns, int sms, cudaStream_t stream) {
+  using S = Shape<QW, CW>;
+  const int stages = stages_of<QW, CW>(MR, K);
   if (stages < 2) return cudaErrorInvalidValue;
   const int G = K >> 7;
   const int rows_pad = ((G + S::GPC - 1) / S::GPC) * S::ROWS;
-  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages);
-  auto kern = gemv_w4a16_kernel<MR, QW>;
+  const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages, CW);
+  auto kern = gemv_w4a16_kernel<MR, QW, CW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
-  const int nunits = ((N + S::W - 1) / S::W) * split.splits;
-  dim3 grid(static_cast<unsigned>(nunits < sms ? nunits : sms));
-  return launch_with_pdl(kern, grid, dim3(kThreads), L.total, stream, maps, x, y, M, N, K,
-                         stages, split.splits, split.partial, split.counter, status, limit_ns);
+  const int nunits = plan.nslab * split.splits;
+  dim3 grid(static_cast<unsigned>(plan.col_q > 0 ? plan.nslab : (nunits < sms ? nunits : sms)));
+  return launch_with_pdl(kern, grid, dim3(S::kThreads), L.total, stream, maps, x, y, M, N, K,
+                         stages, split.splits, plan.col_q, plan.col_r, split.partial,
+                         split.counter, status, limit_ns);
 }
 
 template <int MR>
 cudaError_t launch_mr(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N, int K,
-                      int qw, const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
-                      int sms, cudaStream_t stream) {
-  switch (qw) {
-    case 4: return launch_shape<MR, 4>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
-    case 3: return launch_shape<MR, 3>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
-    default: return launch_shape<MR, 2>(maps, x, y, M, N, K, split, status, limit_ns, sms, stream);
-  }
+                      const GemvSplit& split, const GemvPlan& plan, uint32_t* status,
+                      uint64_t limit_ns, int sms, cudaStream_t stream) {
+#define W4K_GEMV_CASE(QW, CW)                                                                  \
+  if (plan.qw == QW && plan.cw == CW)                                                         \
+    return launch_shape<MR, QW, CW>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, \
+                                    stream);
+  W4K_GEMV_CASE(4, 24)
+  W4K_GEMV_CASE(3, 24)
+  W4K_GEMV_CASE(2, 24)
+  W4K_GEMV_CASE(4, 12)
+  W4K_GEMV_CASE(3, 12)
+  W4K_GEMV_CASE(2, 12)
+#undef W4K_GEMV_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 int gemv_max_rows() { return kMaxRows; }
 
-// x in B-fragment order and its per-group constants must leave room for a 2-stage ring.
+// x in B-fragment order and its per-group constants must leave room for a 2-stage ring in
+// every shape a launch may take.
 bool gemv_supports(int M, int K) {
   if (M < 1 || M > kMaxRows || K < 128) return false;
-  const int sms = sm_count();
-  // The slab width depends on N; the narrowest slab has the largest x buffer per chunk.
-  return stages_for(mr_of(M), K, 2) >= 2 && stages_for(mr_of(M), K, 3) >= 2 &&
-         stages_for(mr_of(M), K, 4) >= 2 && sms >= 0;
+  const int mr = mr_of(M);
+  return stages_of<4, 24>(mr, K) >= 2 && stages_of<3, 24>(mr, K) >= 2 &&
+         stages_of<2, 24>(mr, K) >= 2 && stages_of<4, 12>(mr, K) >= 2 &&
+         stages_of<3, 12>(mr, K) >= 2 && stages_of<2, 12>(mr, K) >= 2;
 }
 
 GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed) {
-  GemvSplit plan;
+  GemvSplit split;
   *bytes_needed = 0;
   const int sms = sm_count();
-  if (sms <= 0) return plan;
-  const int qw = choose_qw(N, sms);
-  const int w = 32 * qw, gpc = gpc_of(qw);
-  const int nslab = (N + w - 1) / w;
+  if (sms <= 0) return split;
+  const GemvPlan plan = make_plan(N, sms);
+  if (plan.col_q > 0) return split;  // every SM already has its share of N
+  const int gpc = plan.cw / plan.qw;
   const int kchunks = ((K >> 7) + gpc - 1) / gpc;
   // One unit per CTA: split each slab's K range over the SMs the slabs leave idle.
-  int splits = sms / nslab;
+  int splits = sms / plan.nslab;
   if (splits > kchunks) splits = kchunks;
   if (splits > 64) splits = 64;
-  if (splits < 2) return plan;
+  if (splits < 2) return split;
   const int per_unit = (kchunks + splits - 1) / splits;
   splits = (kchunks + per_unit - 1) / per_unit;  // no empty k-range
-  if (splits < 2) return plan;
-  plan.splits = splits;
-  plan.partial_offset = ((static_cast<size_t>(nslab) * 4 + 255) / 256) * 256;
-  *bytes_needed = plan.partial_offset + static_cast<size_t>(splits) * mr_of(M) * N * 4;
-  return plan;
+  if (splits < 2) return split;
+  split.splits = splits;
+  split.partial_offset = ((static_cast<size_t>(plan.nslab) * 4 + 255) / 256) * 256;
+  *bytes_needed = split.partial_offset + static_cast<size_t>(splits) * mr_of(M) * N * 4;
+  return split;
 }
 
 cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
@@ -564,8 +628,9 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint1
                               cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int q = choose_qw(N, sms);
-  const uint32_t w = 32u * q, gpc = static_cast<uint32_t>(gpc_of(q));
+  const GemvPlan plan = make_plan(N, sms);
+  if (plan.col_q > 0 && split.splits != 1) return cudaErrorInvalidValue;
+  const uint32_t w = 32u * plan.qw, gpc = static_cast<uint32_t>(plan.cw / plan.qw);
   GemvMaps maps;
   cudaError_t e;
   e = encode(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
@@ -578,10 +643,10 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint1
              static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc);
   if (e != cudaSuccess) return e;
   switch (mr_of(M)) {
-    case 1: return launch_mr<1>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
-    case 2: return launch_mr<2>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
-    case 4: return launch_mr<4>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
-    default: return launch_mr<8>(maps, x, y, M, N, K, q, split, status, limit_ns, sms, stream);
+    case 1: return launch_mr<1>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
+    case 2: return launch_mr<2>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
+    case 4: return launch_mr<4>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
+    default: return launch_mr<8>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
   }
 }
 
