@@ -14,6 +14,7 @@ quantize and GEMV (16384 x 16384), and the 196-matmul Qwen2.5-1.5B-shaped decode
 one CUDA graph; each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+  python bench.py --case gemv_m1 --launches 6     # a few untimed launches, for ncu
 
 With --impl reference the CPU oracle is timed instead (bounded samples of the same
 workload, same metric). Under torchrun each rank runs an independent replica on its own
@@ -547,6 +548,50 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+PROFILE_CASES = ("gemv_m1", "gemv_m8", "tc_m16", "tc_m4096", "q4b32_gemv", "quantize", "pack")
+
+
+def profile_case(args):
+    """A few launches of one workload, untimed, for a profiler (ncu -k ... -c ...): the
+    Llama-3-8B up-projection (14336 x 4096) at M = 1, 8, 16 or 4096 with 6 rotating weight
+    copies (174 MB > L2), the Q4 block-32 GEMV (16384 x 16384), or quantize / pack."""
+    import gemv_w4a16_group_gb300 as w4
+
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    case, n = args.case, args.launches
+    if case in ("gemv_m1", "gemv_m8", "tc_m16", "tc_m4096", "quantize", "pack"):
+        N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+        w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
+        if case == "quantize":
+            for _ in range(n):
+                w4.w4a16_quantize(w, codes=codes, scales=s, mins=m)
+        elif case == "pack":
+            for _ in range(n):
+                w4.w4a16_pack(codes, qw=qw)
+        else:
+            del w, codes
+            M = {"gemv_m1": 1, "gemv_m8": 8, "tc_m16": 16, "tc_m4096": 4096}[case]
+            cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
+            x = workloads.activations_bf16(M, K, seed=M).to(device)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            ws = workspace_for(M, N, K, device)
+            for i in range(n):
+                w4.w4a16_matmul(x, *cps[i % 6], y=y, workspace=ws)
+    else:
+        N = K = workloads.Q4_SQUARE["N"]
+        w = workloads.weights(N, K, seed=0).to(device)
+        qc, qsc = w4.q4b32_quantize(w)
+        del w
+        x = workloads.activations_fp16(K, seed=0).to(device)
+        cps = [(qc.clone(), qsc.clone()) for _ in range(2)] + [(qc, qsc)]
+        for i in range(n):
+            w4.q4b32_gemv(x, *cps[i % 3])
+    torch.cuda.synchronize()
+    status = w4.w4a16_device_status()
+    return {"case": case, "launches": n, "device_status": status}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,7 +600,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-rows", action="store_true", help="headline line only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", choices=PROFILE_CASES, default=None,
+                    help="run a few untimed launches of one workload (for ncu) and exit")
+    ap.add_argument("--launches", type=int, default=6, help="launches for --case")
     args = ap.parse_args(argv)
+    if args.case is not None:
+        print(json.dumps(profile_case(args)), flush=True)
+        return
     if args.steps < 1:
         ap.error("--steps must be >= 1")
     world, rank, local = dist_env()
