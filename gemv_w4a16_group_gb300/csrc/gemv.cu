@@ -78,9 +78,14 @@ struct Shape {
   static constexpr int ROWS = 16 * GPC;
   static constexpr uint32_t word_bytes = static_cast<uint32_t>(W) * ROWS * 4u;  // 1 KB x CW
   static constexpr uint32_t row_bytes = static_cast<uint32_t>(GPC) * W * 2u;    // scales
-  static constexpr uint32_t stage_bytes = word_bytes + 2u * row_bytes;
+  // TMA destinations must be 128-byte aligned: the scale and minimum boxes each start on
+  // their own 128-byte boundary (a box of 5 groups x 96 columns is 960 bytes).
+  static constexpr uint32_t row_stride = (row_bytes + 127u) & ~127u;
+  static constexpr uint32_t tx_bytes = word_bytes + 2u * row_bytes;  // bytes one stage receives
+  static constexpr uint32_t stage_bytes = word_bytes + 2u * row_stride;
   static_assert(GPC * QW == CW, "one (group, quarter) per consumer warp");
-  static_assert(stage_bytes % 128u == 0u, "TMA destinations stay 128-byte aligned");
+  static_assert(word_bytes % 128u == 0u && row_stride % 128u == 0u && stage_bytes % 128u == 0u,
+                "TMA destinations stay 128-byte aligned");
 };
 
 // Shared-memory layout: ring, per-warp partials, per-(row, group) constants of x, x in
@@ -116,6 +121,20 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
@@ -208,11 +227,11 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
             break;
           }
           uint8_t* buf = smem + s * S::stage_bytes;
-          mbar_arrive_expect_tx(&full[s], S::stage_bytes);
+          mbar_arrive_expect_tx(&full[s], S::tx_bytes);
           const int col0 = slab_col0(slab);
           tma_load_2d(buf, &maps.qw, &full[s], col0, kc * ROWS);
           tma_load_2d(buf + S::word_bytes, &maps.scales, &full[s], col0, kc * GPC);
-          tma_load_2d(buf + S::word_bytes + S::row_bytes, &maps.mins, &full[s], col0,
+          tma_load_2d(buf + S::word_bytes + S::row_stride, &maps.mins, &full[s], col0,
                       kc * GPC);
         }
       }
@@ -300,33 +319,43 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
 
   const int gq = lane >> 2, c = lane & 3;
   const int qq = warp % QW, gl = warp / QW;  // column quarter, group within a chunk
-  // Per-lane constant offsets: block b of a chunk adds b * 4 rows (compile-time strides).
+  // Per-lane constant shared-memory addresses: block b of a chunk adds b * 4 rows, a stage
+  // adds stage_bytes (compile-time strides).
   const int row0 = gl * 16 + c;  // packed row of block 0 in the chunk
+  const uint32_t ring_base = smem_addr(smem);
   const uint32_t w_off = static_cast<uint32_t>(row0 * (W * 4) + qq * 128 + gq * 16);
   const uint32_t s_off = S::word_bytes + static_cast<uint32_t>(gl * (W * 2) + (qq * 32 + gq * 4) * 2);
-  // B fragment: batch row gq; product columns gq >= MR are never read, so those lanes may
-  // load any existing row.
-  const uint4* x_lane = sXperm + row0 * MR + (gq & (MR - 1));
+  // B fragment: lane (gq, c) supplies batch row gq & (MR - 1), so product column n holds
+  // row n & (MR - 1), and lane c's fragment columns 2c, 2c + 1 hold rows (2c + bb) & (MR - 1).
+  const uint32_t x_lane = smem_addr(sXperm) + static_cast<uint32_t>((row0 * MR + (gq & (MR - 1))) * 16);
+  // Lanes whose fragments hold the same rows share the fold: with MR <= 2 all four c-lanes
+  // hold every row and fold one column each, with MR = 4 lanes c and c ^ 2 split four
+  // columns, with MR = 8 each lane folds its own two rows of all four columns.
+  constexpr int CPL = MR <= 2 ? 1 : MR == 4 ? 2 : 4;  // columns folded per lane
+  constexpr int NBB = MR == 1 ? 1 : 2;                // fragment columns (rows) per lane
+  const int jj0 = MR <= 2 ? c : MR == 4 ? 2 * (c >> 1) : 0;
   int s = 0;
   uint32_t phase = 0u;  // ring position of the next chunk
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
     const int slab = u / splits, kr = u - slab * splits;
     const int kc_end = min(kchunks, (kr + 1) * per_unit);
     const int col0 = slab_col0(slab), col_end = min(N, col0 + slab_cols(slab));
-    // yacc[col jj][bb]: column col0 + 32*qq + 4*gq + jj, batch row 2c + bb
-    float yacc[4][2];
+    // yacc[i][bb]: column col0 + 32*qq + 4*gq + jj0 + i, batch row (2c + bb) & (MR - 1)
+    float yacc[CPL][NBB];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) yacc[jj][0] = yacc[jj][1] = 0.f;
+    for (int i = 0; i < CPL; ++i)
+#pragma unroll
+      for (int bb = 0; bb < NBB; ++bb) yacc[i][bb] = 0.f;
 
     for (int kc = kr * per_unit; kc < kc_end; ++kc) {
       const int g = kc * GPC + gl;  // this warp's group
       // On an expired wait every warp keeps walking the chunk list without computing, so
       // all consumer warps still meet at the per-unit barriers below.
       const bool landed = mbar_wait_bounded(&full[s], phase, abort_flag, status, limit_ns);
-      const uint8_t* buf = smem + s * S::stage_bytes;
+      const uint32_t buf = ring_base + static_cast<uint32_t>(s) * S::stage_bytes;
       if (landed && g < G) {
-        const uint8_t* wp = buf + w_off;
-        const uint4* xp = x_lane + kc * (ROWS * MR);
+        const uint32_t wa = buf + w_off;
+        const uint32_t xa = x_lane + static_cast<uint32_t>(kc * (ROWS * MR * 16));
         float d[2][2][4];  // [chain][tile t][fragment]: even / odd blocks
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch)
@@ -336,8 +365,8 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
             for (int f = 0; f < 4; ++f) d[ch][t][f] = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const uint4 wv = *reinterpret_cast<const uint4*>(wp + b * (4 * W * 4));
-          const uint4 e = xp[b * 4 * MR];
+          const uint4 wv = lds128(wa + b * (4 * W * 4));
+          const uint4 e = lds128(xa + b * (4 * MR * 16));
           uint32_t p[4][4];
           code_pairs_f16(wv.x, p[0]);
           code_pairs_f16(wv.y, p[1]);
@@ -352,34 +381,40 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
                           p[2 * t + 1][3], e.z, e.w);
           }
         }
-        // Fold this group: y += (s 2^-e) D + (min X - s T) for the batch rows that exist
-        // (row 2c + bb; lanes whose rows do not exist add zeros).
-        const uint2 s2 = *reinterpret_cast<const uint2*>(buf + s_off);
-        const uint2 m2 = *reinterpret_cast<const uint2*>(buf + s_off + S::row_bytes);
-        const uint32_t sw[2] = {s2.x, s2.y}, mw[2] = {m2.x, m2.y};
-        float gx[2], gt[2], gu[2];
+        // Fold this group: y += (s 2^-e) D + (min X - s T). Column 4gq + jj is tile jj / 2,
+        // fragment half jj % 2.
+        float dsum[4][NBB];
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int mrow = 2 * c + bb;
-          const bool ex = bb < MR && mrow < MR;
-          const int ci = (ex ? mrow : 0) * G + g;
-          gx[bb] = ex ? sX[ci] : 0.f;
-          gt[bb] = ex ? sT[ci] : 0.f;
-          gu[bb] = ex ? sU[ci] : 0.f;
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int bb = 0; bb < NBB; ++bb)
+            dsum[jj][bb] = d[0][jj >> 1][2 * (jj & 1) + bb] + d[1][jj >> 1][2 * (jj & 1) + bb];
+        float gx[NBB], gt[NBB], gu[NBB];
+#pragma unroll
+        for (int bb = 0; bb < NBB; ++bb) {
+          const int ci = ((2 * c + bb) & (MR - 1)) * G + g;
+          gx[bb] = sX[ci];
+          gt[bb] = sT[ci];
+          gu[bb] = sU[ci];
         }
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float sc =
-              bf16_bits_to_f32((jj & 1) ? (sw[jj >> 1] >> 16) : (sw[jj >> 1] & 0xFFFFu));
-          const float mn =
-              bf16_bits_to_f32((jj & 1) ? (mw[jj >> 1] >> 16) : (mw[jj >> 1] & 0xFFFFu));
-          const int t = jj >> 1, h = jj & 1;  // column 4gq + jj is tile t, fragment half h
+        for (int i = 0; i < CPL; ++i) {
+          const int jj = jj0 + i;
+          const float sc = bf16_bits_to_f32(lds_u16(buf + s_off + 2 * jj));
+          const float mn = bf16_bits_to_f32(lds_u16(buf + s_off + S::row_stride + 2 * jj));
 #pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            if (bb >= MR) continue;  // no lane holds an existing row here
-            const float dv = d[0][t][2 * h + bb] + d[1][t][2 * h + bb];
-            yacc[jj][bb] =
-                fmaf(sc * gu[bb], dv, fmaf(mn, gx[bb], fmaf(-sc, gt[bb], yacc[jj][bb])));
+          for (int bb = 0; bb < NBB; ++bb) {
+            float dv;
+            if constexpr (CPL == 4) {
+              dv = dsum[i][bb];
+            } else if constexpr (CPL == 2) {
+              dv = (c >> 1) ? dsum[2 + i][bb] : dsum[i][bb];
+            } else {
+              dv = (c & 2) ? ((c & 1) ? dsum[3][bb] : dsum[2][bb])
+                           : ((c & 1) ? dsum[1][bb] : dsum[0][bb]);
+            }
+            yacc[i][bb] =
+                fmaf(sc * gu[bb], dv, fmaf(mn, gx[bb], fmaf(-sc, gt[bb], yacc[i][bb])));
           }
         }
       }
@@ -394,12 +429,10 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
     // Unit done: warp partials to shared memory, fixed-order sum over the GPC groups of
     // each column quarter.
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
+    for (int i = 0; i < CPL; ++i)
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int mrow = 2 * c + bb;
-        if (mrow < MR) sRed[(warp * MR + mrow) * 32 + gq * 4 + jj] = yacc[jj][bb];
-      }
+      for (int bb = 0; bb < NBB; ++bb)
+        sRed[(warp * MR + ((2 * c + bb) & (MR - 1))) * 32 + gq * 4 + jj0 + i] = yacc[i][bb];
     consumer_bar<NC>();
     for (int i = tid; i < MR * W; i += NC) {
       const int mm = i / W, col = i - mm * W, q = col >> 5, c32 = col & 31;
