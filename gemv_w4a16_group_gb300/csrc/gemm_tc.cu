@@ -28,10 +28,19 @@ namespace {
 
 constexpr int kBN = 128;  // weight columns per CTA (MMA M)
 constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row of BF16)
-constexpr int kDequantWarps = 4;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+// Warp roles: dequantising warps 0..DQ-1 (TMEM lane quarter w % 4, k-part w / 4 of each
+// 64-k block), then the TMA warp and the MMA warp. The widest tile (BM = 256) keeps the
+// tensor pipe busiest and gets two dequantising warps per lane quarter; narrower tiles keep
+// four so that two CTAs fit on an SM.
+template <int BM>
+struct Roles {
+  static constexpr int kDequantWarps = BM >= 256 ? 8 : 4;
+  static constexpr int kParts = kDequantWarps / 4;  // k-parts of a 64-k block
+  static constexpr int kTmaWarp = kDequantWarps;
+  static constexpr int kMmaWarp = kDequantWarps + 1;
+  static constexpr int kThreads = (kDequantWarps + 2) * 32;
+  static constexpr int kMinBlocks = BM >= 256 ? 1 : 2;
+};
 constexpr uint32_t kPkBytes = kBK / 8 * kBN * 4;  // 8 rows x 128 words = 4 KB
 constexpr uint32_t kRowBytes = kBN * 2;           // one scale (or min) row = 256 B
 
@@ -65,13 +74,16 @@ struct Smem {
 };
 
 template <int BM>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
     w4a16_tc_kernel(const __grid_constant__ TcMaps maps, uint16_t* __restrict__ y, int M, int N,
                     int K, uint32_t* __restrict__ status, uint64_t limit_ns,
                     float* __restrict__ ws_partial, uint32_t* __restrict__ ws_counter) {
   using L = Smem<BM>;
+  using R = Roles<BM>;
   constexpr int kStages = L::kStages;
   constexpr int kAStages = L::kAStages;
+  constexpr int kDequantWarps = R::kDequantWarps, kParts = R::kParts;
+  constexpr int kTmaWarp = R::kTmaWarp, kMmaWarp = R::kMmaWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -183,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp < kDequantWarps) {
     pdl_wait();  // y and the workspace may still be in use by the previous kernel
-    const int row = warp * 32 + lane;  // TMEM lane = weight column n0 + row
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = weight column n0 + row
+    const int part = warp >> 2;              // this warp's k-part of each 64-k block
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t b128 = 0x43004300u;  // BF16 (128, 128)
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
@@ -200,9 +213,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
       const __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&m2u);
       const __nv_bfloat162 off = *reinterpret_cast<const __nv_bfloat162*>(&b128);
-      uint32_t out[32];
+      constexpr int kWords = kBK / 8 / kParts;  // packed words of this warp's k-part
+      uint32_t out[4 * kWords];
 #pragma unroll
-      for (int c = 0; c < kBK / 8; ++c) {
+      for (int cc = 0; cc < kWords; ++cc) {
+        const int c = part * kWords + cc;
         const uint32_t w = spk[s * (kPkBytes / 4) + c * kBN + row];
         uint32_t p[4];
         codes_to_bf16x2_consecutive(w, p);
@@ -210,10 +225,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < 4; ++i) {
           const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p[i]), off);
           const __nv_bfloat162 wv = __hfma2(q2, s2, m2);  // q*s + min, one rounding
-          out[4 * c + i] = *reinterpret_cast<const uint32_t*>(&wv);
+          out[4 * cc + i] = *reinterpret_cast<const uint32_t*>(&wv);
         }
       }
-      tmem_st_32cols(lane_base + L::a_col0 + sa * 32, out);
+      if constexpr (kParts == 1)
+        tmem_st_32cols(lane_base + L::a_col0 + sa * 32, out);
+      else
+        tmem_st_16cols(lane_base + L::a_col0 + sa * 32 + part * 16, out);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -227,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (splits == 1) {
       if (have_acc) {
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = part; c < kChunks; c += kParts) {
           uint32_t v[32];
           tmem_ld_32cols(lane_base + c * 32, v);  // BM < 32: columns >= BM are never stored
           tmem_ld_wait();
@@ -247,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       // last CTA of the tile sums the partials in split order (deterministic) and stores.
       const size_t Mp = static_cast<size_t>(gridDim.y) * BM;
       if (have_acc) {
-        float* part = ws_partial + static_cast<size_t>(blockIdx.z) * Mp * N;
+        float* mine = ws_partial + static_cast<size_t>(blockIdx.z) * Mp * N;
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = part; c < kChunks; c += kParts) {
           uint32_t v[32];
           tmem_ld_32cols(lane_base + c * 32, v);
           tmem_ld_wait();
@@ -257,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int m = m0 + c * 32 + j;
-              if (j < BM) __stcg(part + static_cast<size_t>(m) * N + n, __uint_as_float(v[j]));
+              if (j < BM) __stcg(mine + static_cast<size_t>(m) * N + n, __uint_as_float(v[j]));
             }
           }
         }
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (n < N) {
           // 4 rows at a time, up to 4 splits per round: 16 independent loads in flight.
 #pragma unroll 1
-          for (int j0 = 0; j0 < BM && m0 + j0 < M; j0 += 4) {
+          for (int j0 = 4 * part; j0 < BM && m0 + j0 < M; j0 += 4 * kParts) {
             float acc[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) acc[jj] = 0.f;
@@ -381,7 +399,7 @@ cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint
   if (e != cudaSuccess) return e;
   dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM, split.splits);
   if (grid.y > 65535 || split.splits < 1) return cudaErrorInvalidConfiguration;
-  return launch_with_pdl(kern, grid, dim3(kThreads), L::alloc, stream, maps, y, M, N, K, status,
+  return launch_with_pdl(kern, grid, dim3(Roles<BM>::kThreads), L::alloc, stream, maps, y, M, N, K, status,
                          limit_ns, split.partial, split.counter);
 }
 
