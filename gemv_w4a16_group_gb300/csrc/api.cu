@@ -186,7 +186,7 @@ w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
-static int g_q4_variant = 1;
+static int g_q4_variant = 2;
 
 w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                         uint16_t* y, int N, int K, w4a16_stream_t stream) {
@@ -194,8 +194,17 @@ w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t*
   if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(w4k::launch_q4b32_gemv(x, codes, scales, y, N, K, g_q4_variant,
-                                          reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g_q4_variant == 2 && w4k::q4b32_tc_supports(N, K)) {
+    uint32_t* status = status_word_ptr();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(
+        w4k::launch_q4b32_gemv_tc(x, codes, scales, y, N, K, status, g_wait_limit_ns, s));
+  }
+  // Shapes the tensor-pipe kernel does not take (K % 256 != 0, very long K) use the
+  // CUDA-core kernel.
+  return from_cuda(w4k::launch_q4b32_gemv(x, codes, scales, y, N, K,
+                                          g_q4_variant == 0 ? 0 : 1, s));
 }
 
 w4a16_status w4a16_device_status(w4a16_stream_t stream) {
@@ -238,7 +247,7 @@ int w4a16_testing_set_gemv_max_m(int m) {
 
 int w4a16_testing_set_q4_variant(int v) {
   const int prev = g_q4_variant;
-  if (v == 0 || v == 1) g_q4_variant = v;
+  if (v >= 0 && v <= 2) g_q4_variant = v;
   return prev;
 }
 

@@ -73,6 +73,13 @@ cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K
 // Q4 block-32 GEMV.
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                               uint16_t* y, int N, int K, int variant, cudaStream_t stream);
+// Q4 block-32 GEMV on the tensor pipe (TMA-staged, mma.sync FP16 -> fp32). Needs K % 256 == 0
+// (TMA row strides of the scales) and x, its per-block constants and a two-stage ring in
+// shared memory; q4b32_tc_supports() tells. Bounded waits report through `status`.
+bool q4b32_tc_supports(int N, int K);
+cudaError_t launch_q4b32_gemv_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                                 uint16_t* y, int N, int K, uint32_t* status,
+                                 uint64_t wait_limit_ns, cudaStream_t stream);
 
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);

@@ -24,8 +24,9 @@ int w4a16_testing_force_kernel(int kernel);
  * negative value only queries. Returns the previous value. */
 int w4a16_testing_set_gemv_max_m(int m);
 
-/* Inner product of q4b32_gemv: 0 = packed fp32, 1 = mixed FP16 (default). Other values
- * only query. Returns the previous value. */
+/* Kernel of q4b32_gemv: 2 = TMA-staged tensor-pipe kernel (default; shapes it does not
+ * take fall back to 1), 1 = CUDA-core kernel with mixed FP16 FMAs, 0 = CUDA-core kernel
+ * with packed fp32 FMAs. Other values only query. Returns the previous value. */
 int w4a16_testing_set_q4_variant(int v);
 
 #ifdef __cplusplus

@@ -237,9 +237,12 @@ def test_matmul_rejects_misaligned_views(w4):
 # Q4 block-32
 # --------------------------------------------------------------------------- #
 
-@pytest.mark.parametrize("variant", [0, 1])
-@pytest.mark.parametrize("N,K", [(256, 512), (8, 32), (13, 96), (1000, 1056), (4096, 4096)])
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("N,K", [(256, 512), (8, 32), (13, 96), (1000, 1056), (4096, 4096),
+                                 (13, 1024), (2056, 2560), (300, 5120)])
 def test_q4_quantize_and_gemv(w4, variant, N, K):
+    """Variant 2 is the TMA / tensor-pipe kernel where it takes the shape (K % 512 == 0),
+    else the CUDA-core kernel; 0 and 1 force the CUDA-core inner products."""
     prev = w4.testing_set_q4_variant(variant)
     try:
         w = workloads.weights(N, K, seed=N)
