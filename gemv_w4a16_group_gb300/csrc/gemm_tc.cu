@@ -355,38 +355,10 @@ __global__ void bounded_wait_selftest_kernel(uint32_t* status, uint64_t limit_ns
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                       uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                       CUtensorMapSwizzle swz) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return encode_tensor_map(map, dt, base, inner, outer, row_bytes, box_inner, box_outer, swz);
 }
 
 template <int BM>
@@ -394,7 +366,7 @@ cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint
                       uint64_t limit_ns, const TcSplit& split, cudaStream_t stream) {
   using L = Smem<BM>;
   auto kern = w4a16_tc_kernel<BM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                        static_cast<int>(L::alloc));
   if (e != cudaSuccess) return e;
   dim3 grid((N + kBN - 1) / kBN, (M + BM - 1) / BM, split.splits);

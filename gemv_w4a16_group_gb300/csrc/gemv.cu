@@ -472,39 +472,6 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-cudaError_t encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 int sm_count() {
   static int count[64] = {};
   int dev = 0;
@@ -590,7 +557,7 @@ cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, i
   const int rows_pad = ((G + S::GPC - 1) / S::GPC) * S::ROWS;
   const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages, CW);
   auto kern = gemv_w4a16_kernel<MR, QW, CW>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
   const int nunits = plan.nslab * split.splits;
@@ -666,14 +633,17 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint1
   const uint32_t w = 32u * plan.qw, gpc = static_cast<uint32_t>(plan.cw / plan.qw);
   GemvMaps maps;
   cudaError_t e;
-  e = encode(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, w, 16u * gpc);
+  e = encode_tensor_map(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, w, 16u * gpc,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  e = encode(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc);
+  e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales,
+                        static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
+                        static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  e = encode(&maps.mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins, static_cast<uint64_t>(N),
-             static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc);
+  e = encode_tensor_map(&maps.mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins,
+                        static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
+                        static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   switch (mr_of(M)) {
     case 1: return launch_mr<1>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);

@@ -11,6 +11,14 @@
 
 namespace w4k {
 
+// TMA descriptor of a 2-D tensor (inner dimension contiguous, rows `row_bytes` apart),
+// box {box_inner, box_outer}, out-of-bounds elements read as zero. Cached by arguments.
+cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device, size).
+cudaError_t set_max_dynamic_smem(const void* func, int bytes);
+
 // Bits of the per-device status word (read and cleared by w4a16_device_status).
 constexpr uint32_t kStatusTimeout = 1u;
 

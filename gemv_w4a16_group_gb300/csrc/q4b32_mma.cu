@@ -310,34 +310,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 namespace {
 
-typedef CUresult (*Q4EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-cudaError_t q4_encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
-                      uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                      uint32_t box_outer, CUtensorMapSwizzle swizzle) {
-  static Q4EncodeFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return cudaErrorNotSupported;
-    fn = reinterpret_cast<Q4EncodeFn>(p);
-  }
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 int q4_sm_count() {
   static int count[64] = {};
   int dev = 0;
@@ -380,18 +352,18 @@ cudaError_t launch_q4b32_gemv_tc(const uint16_t* x, const uint8_t* codes, const 
   const Q4Plan plan = q4_plan(N, K, sms);
   if (plan.T == 0) return cudaErrorNotSupported;
   Q4Maps maps;
-  cudaError_t e = q4_encode(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
+  cudaError_t e = encode_tensor_map(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
                             static_cast<uint64_t>(K) / 2, static_cast<uint64_t>(N),
                             static_cast<uint64_t>(K) / 2, kQBoxK / 2,
                             static_cast<uint32_t>(16 * plan.T), CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = q4_encode(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales,
+  e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales,
                 static_cast<uint64_t>(K) / 32, static_cast<uint64_t>(N),
                 static_cast<uint64_t>(K) / 16, kQChunkK / 32, static_cast<uint32_t>(16 * plan.T),
                 CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   const uint32_t smem = Q4Layout(plan.T, K, plan.stages).total + 1024u;
-  e = cudaFuncSetAttribute(q4b32_gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = set_max_dynamic_smem(reinterpret_cast<const void*>(q4b32_gemv_tc_kernel),
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = plan.nunits < sms ? plan.nunits : sms;
