@@ -33,7 +33,7 @@ __all__ = [
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
                 3: "W4A16_ERR_MISALIGNED", 4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT",
-                6: "W4A16_ERR_WORKSPACE"}
+                6: "W4A16_ERR_WORKSPACE", 7: "W4A16_ERR_LAYOUT"}
 
 
 class W4A16Error(RuntimeError):

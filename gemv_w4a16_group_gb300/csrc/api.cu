@@ -87,6 +87,7 @@ const char* w4a16_status_string(w4a16_status status) {
     case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
     case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
     case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+    case W4A16_ERR_LAYOUT: return "W4A16_ERR_LAYOUT";
   }
   return "W4A16_ERR_UNKNOWN";
 }
@@ -220,7 +221,8 @@ w4a16_status w4a16_device_status(w4a16_stream_t stream) {
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return W4A16_ERR_CUDA;
   }
-  return (word & w4k::kStatusTimeout) ? W4A16_ERR_TIMEOUT : W4A16_OK;
+  if (word & w4k::kStatusTimeout) return W4A16_ERR_TIMEOUT;
+  return (word & w4k::kStatusLayout) ? W4A16_ERR_LAYOUT : W4A16_OK;
 }
 
 w4a16_status w4a16_selftest_bounded_wait(uint32_t limit_us, w4a16_stream_t stream) {

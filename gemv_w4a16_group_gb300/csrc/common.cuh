@@ -260,6 +260,17 @@ __device__ __forceinline__ void codes_to_f32_offset(uint32_t w, float (&f)[8]) {
   f[6] = __uint_as_float((u3 & 0x0000F000u) | 0x45000000u);
   f[7] = __uint_as_float((u3 & 0x000F0000u) | 0x43000000u);
 }
+// (a & MASK) | c as one LOP3. Written out in PTX because the same expression in C++, four
+// times per packed word in an unrolled loop, compiled to code that held more registers
+// (spilling at 72 per thread) and ran the GEMV's inner loop at half the speed (measured
+// with a shared-memory-only copy of the loop: 695 vs 323 clocks per 24 KB chunk).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
+  return r;
+}
+
 // Offsets used by codes_to_f32_offset for code j of a word.
 __host__ __device__ constexpr float code_offset_f32(int j) { return (j & 1) ? 128.0f : 2048.0f; }
 
@@ -271,7 +282,7 @@ __device__ __forceinline__ void codes_to_bf16x2_consecutive(uint32_t w, uint32_t
   for (int i = 0; i < 4; ++i) {
     // byte 0 <- byte i of w (q_{2i} low), byte 2 <- byte i of v (q_{2i+1} low)
     const uint32_t t = __byte_perm(w, v, (i) | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12));
-    p[i] = (t & 0x000F000Fu) | 0x43004300u;
+    p[i] = and_or<0x000F000Fu>(t, 0x43004300u);
   }
 }
 

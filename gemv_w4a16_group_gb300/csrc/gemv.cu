@@ -63,6 +63,9 @@ constexpr int kMaxRows = 8;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kSmemOneCta = 227u * 1024u;
 constexpr uint32_t kSmemTwoCtas = 113u * 1024u;  // two CTAs (and their reserves) per SM
+// The packed words land 128-byte swizzled, which wants 1024-byte aligned destinations; the
+// dynamic shared-memory base is 128-byte aligned, so the kernel rounds it up (at most 896 B).
+constexpr uint32_t kAlignPad = 1024u - 128u;
 
 // Slab of W = 32 QW columns; a chunk holds GPC groups of 128 k (16 packed rows each) so that
 // every consumer warp owns one (group, column quarter).
@@ -82,14 +85,18 @@ struct Shape {
   // their own 128-byte boundary (a box of 5 groups x 96 columns is 960 bytes).
   static constexpr uint32_t row_stride = (row_bytes + 127u) & ~127u;
   static constexpr uint32_t tx_bytes = word_bytes + 2u * row_bytes;  // bytes one stage receives
-  static constexpr uint32_t stage_bytes = word_bytes + 2u * row_stride;
+  static constexpr uint32_t sc_bytes = 2u * row_stride;  // scales + minimums of one stage
+  static constexpr uint32_t stage_bytes = word_bytes + sc_bytes;
+  static constexpr uint32_t box_bytes = static_cast<uint32_t>(ROWS) * 128u;  // one quarter
   static_assert(GPC * QW == CW, "one (group, quarter) per consumer warp");
-  static_assert(word_bytes % 128u == 0u && row_stride % 128u == 0u && stage_bytes % 128u == 0u,
-                "TMA destinations stay 128-byte aligned");
+  static_assert(box_bytes % 1024u == 0u && word_bytes == box_bytes * QW,
+                "swizzled word boxes start on 1024-byte boundaries");
+  static_assert(row_stride % 128u == 0u, "TMA destinations stay 128-byte aligned");
 };
 
-// Shared-memory layout: ring, per-warp partials, per-(row, group) constants of x, x in
-// B-fragment order, barriers.
+// Shared-memory layout (from the 1024-byte aligned base): the word ring (stages x
+// word_bytes), the scale/minimum ring (stages x sc_bytes), per-warp partials, per-(row,
+// group) constants of x, x in B-fragment order, barriers; `total` includes the alignment pad.
 struct GemvLayout {
   uint32_t red_off, cst_off, xperm_off, bar_off, total;
   __host__ __device__ GemvLayout(uint32_t stage_bytes, int rows_pad, int MR, int G, int stages,
@@ -98,7 +105,7 @@ struct GemvLayout {
     cst_off = red_off + static_cast<uint32_t>(CW) * MR * 32u * 4u;       // X, T, U: [3][MR][G]
     xperm_off = (cst_off + 3u * MR * G * 4u + 15u) & ~15u;               // [rows_pad][MR] 16 B
     bar_off = (xperm_off + static_cast<uint32_t>(rows_pad) * MR * 16u + 7u) & ~7u;
-    total = bar_off + 2u * kMaxStages * 8u + 16u;
+    total = bar_off + 2u * kMaxStages * 8u + 16u + kAlignPad;
   }
 };
 
@@ -106,10 +113,11 @@ struct GemvLayout {
 // p0 = (q0, q4), p1 = (16 q1, 16 q5), p2 = (q2, q6), p3 = (16 q3, 16 q7).
 __device__ __forceinline__ void code_pairs_f16(uint32_t w, uint32_t (&p)[4]) {
   const uint32_t w8 = w >> 8;
-  p[0] = (w & 0x000F000Fu) | 0x64006400u;
-  p[1] = (w & 0x00F000F0u) | 0x64006400u;
-  p[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  p[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+  const uint32_t magic = 0x64006400u;
+  p[0] = and_or<0x000F000Fu>(w, magic);
+  p[1] = and_or<0x00F000F0u>(w, magic);
+  p[2] = and_or<0x000F000Fu>(w8, magic);
+  p[3] = and_or<0x00F000F0u>(w8, magic);
 }
 
 // D += A (16x16, FP16) * B (16x8, FP16), fp32 accumulators; fragment layout of mma.sync
@@ -153,7 +161,7 @@ __device__ __forceinline__ void consumer_bar() {
 }
 
 struct GemvMaps {
-  CUtensorMap qw;      // int32 [K/8, N], box {W, ROWS}
+  CUtensorMap qw;      // int32 [K/8, N], box {32, ROWS}, 128-byte swizzle
   CUtensorMap scales;  // bf16 [K/128, N], box {W, GPC}
   CUtensorMap mins;    // bf16 [K/128, N], box {W, GPC}
 };
@@ -172,7 +180,14 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
   const int kchunks = (G + GPC - 1) / GPC;
   const int rows_pad = kchunks * ROWS;
   const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages, CW);
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+  if (pad > kAlignPad) {  // base less than 128-byte aligned: report, touch nothing
+    if (threadIdx.x == 0) atomicOr(status, kStatusLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   float* sRed = reinterpret_cast<float*>(smem + L.red_off);
   float* sX = reinterpret_cast<float*>(smem + L.cst_off);  // [MR][G] sum x
   float* sT = sX + MR * G;                                  // [MR][G] 1024 sum_even + 64 sum_odd
@@ -226,13 +241,15 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
             ok = false;
             break;
           }
-          uint8_t* buf = smem + s * S::stage_bytes;
+          uint8_t* wbuf = smem + s * S::word_bytes;
+          uint8_t* sbuf = smem + stages * S::word_bytes + s * S::sc_bytes;
           mbar_arrive_expect_tx(&full[s], S::tx_bytes);
           const int col0 = slab_col0(slab);
-          tma_load_2d(buf, &maps.qw, &full[s], col0, kc * ROWS);
-          tma_load_2d(buf + S::word_bytes, &maps.scales, &full[s], col0, kc * GPC);
-          tma_load_2d(buf + S::word_bytes + S::row_stride, &maps.mins, &full[s], col0,
-                      kc * GPC);
+#pragma unroll
+          for (int q = 0; q < QW; ++q)
+            tma_load_2d(wbuf + q * S::box_bytes, &maps.qw, &full[s], col0 + 32 * q, kc * ROWS);
+          tma_load_2d(sbuf, &maps.scales, &full[s], col0, kc * GPC);
+          tma_load_2d(sbuf + S::row_stride, &maps.mins, &full[s], col0, kc * GPC);
         }
       }
       // Stay until this CTA's last copies have landed (bounded), so none is in flight
@@ -319,15 +336,24 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
 
   const int gq = lane >> 2, c = lane & 3;
   const int qq = warp % QW, gl = warp / QW;  // column quarter, group within a chunk
-  // Per-lane constant shared-memory addresses: block b of a chunk adds b * 4 rows, a stage
-  // adds stage_bytes (compile-time strides).
-  const int row0 = gl * 16 + c;  // packed row of block 0 in the chunk
+  // Lane (gq, c) reads packed row 16 gl + 2c + (b & 1) + 8 (b >> 1) of its column quarter in
+  // block b: the 16 rows of the group once each, in an order where the 8 lanes of a shared-
+  // memory phase (gq in {2p, 2p + 1}, c = 0..3) hit 16-byte chunks gq ^ (2c + (b & 1)) of the
+  // swizzled rows (chunk j of row r sits at j ^ (r mod 8)): 8 distinct chunks, all 32 banks,
+  // no conflict. x follows the same row order, so each MMA still pairs matching k.
+  // Per-lane constant addresses: odd blocks use the odd row, blocks 2 and 3 add 8 rows, a
+  // stage adds word_bytes / sc_bytes.
   const uint32_t ring_base = smem_addr(smem);
-  const uint32_t w_off = static_cast<uint32_t>(row0 * (W * 4) + qq * 128 + gq * 16);
-  const uint32_t s_off = S::word_bytes + static_cast<uint32_t>(gl * (W * 2) + (qq * 32 + gq * 4) * 2);
+  const int r_even = gl * 16 + 2 * c, r_odd = r_even + 1;
+  const uint32_t w_even =
+      static_cast<uint32_t>(qq) * S::box_bytes + static_cast<uint32_t>(r_even * 128 + ((gq ^ (2 * c)) << 4));
+  const uint32_t w_odd =
+      static_cast<uint32_t>(qq) * S::box_bytes + static_cast<uint32_t>(r_odd * 128 + ((gq ^ (2 * c + 1)) << 4));
+  const uint32_t sc_ring = ring_base + static_cast<uint32_t>(stages) * S::word_bytes;
+  const uint32_t s_off = static_cast<uint32_t>(gl * (W * 2) + (qq * 32 + gq * 4) * 2);
   // B fragment: lane (gq, c) supplies batch row gq & (MR - 1), so product column n holds
   // row n & (MR - 1), and lane c's fragment columns 2c, 2c + 1 hold rows (2c + bb) & (MR - 1).
-  const uint32_t x_lane = smem_addr(sXperm) + static_cast<uint32_t>((row0 * MR + (gq & (MR - 1))) * 16);
+  const uint32_t x_lane = smem_addr(sXperm) + static_cast<uint32_t>((r_even * MR + (gq & (MR - 1))) * 16);
   // Lanes whose fragments hold the same rows share the fold: with MR <= 2 all four c-lanes
   // hold every row and fold one column each, with MR = 4 lanes c and c ^ 2 split four
   // columns, with MR = 8 each lane folds its own two rows of all four columns.
@@ -352,9 +378,9 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
       // On an expired wait every warp keeps walking the chunk list without computing, so
       // all consumer warps still meet at the per-unit barriers below.
       const bool landed = mbar_wait_bounded(&full[s], phase, abort_flag, status, limit_ns);
-      const uint32_t buf = ring_base + static_cast<uint32_t>(s) * S::stage_bytes;
+      const uint32_t wbuf = ring_base + static_cast<uint32_t>(s) * S::word_bytes;
+      const uint32_t sbuf = sc_ring + static_cast<uint32_t>(s) * S::sc_bytes;
       if (landed && g < G) {
-        const uint32_t wa = buf + w_off;
         const uint32_t xa = x_lane + static_cast<uint32_t>(kc * (ROWS * MR * 16));
         float d[2][2][4];  // [chain][tile t][fragment]: even / odd blocks
 #pragma unroll
@@ -365,8 +391,8 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
             for (int f = 0; f < 4; ++f) d[ch][t][f] = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const uint4 wv = lds128(wa + b * (4 * W * 4));
-          const uint4 e = lds128(xa + b * (4 * MR * 16));
+          const uint4 wv = lds128(wbuf + ((b & 1) ? w_odd : w_even) + (b >> 1) * 1024);
+          const uint4 e = lds128(xa + ((b & 1) + 8 * (b >> 1)) * (MR * 16));
           uint32_t p[4][4];
           code_pairs_f16(wv.x, p[0]);
           code_pairs_f16(wv.y, p[1]);
@@ -400,8 +426,8 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
           const int jj = jj0 + i;
-          const float sc = bf16_bits_to_f32(lds_u16(buf + s_off + 2 * jj));
-          const float mn = bf16_bits_to_f32(lds_u16(buf + s_off + S::row_stride + 2 * jj));
+          const float sc = bf16_bits_to_f32(lds_u16(sbuf + s_off + 2 * jj));
+          const float mn = bf16_bits_to_f32(lds_u16(sbuf + s_off + S::row_stride + 2 * jj));
 #pragma unroll
           for (int bb = 0; bb < NBB; ++bb) {
             float dv;
@@ -634,8 +660,8 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint1
   GemvMaps maps;
   cudaError_t e;
   e = encode_tensor_map(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
-                        static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, w, 16u * gpc,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+                        static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, 32u, 16u * gpc,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales,
                         static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),

@@ -21,6 +21,7 @@ cudaError_t set_max_dynamic_smem(const void* func, int bytes);
 
 // Bits of the per-device status word (read and cleared by w4a16_device_status).
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusLayout = 2u;  // a kernel found its shared memory misaligned, skipped
 
 // Default limit of a bounded wait (nanoseconds of %globaltimer).
 constexpr uint64_t kDefaultWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s

@@ -39,10 +39,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // acc += sum_j (1024 + q_j) * x_j for the 8 codes of word w (FP16 halves).
 __device__ __forceinline__ float dot8_mixed_f16(uint32_t w, uint32_t x01, uint32_t x23,
                                                 uint32_t x45, uint32_t x67, float acc) {
-  const uint32_t p0 = (w & 0x000F000Fu) | 0x64006400u;
-  const uint32_t p1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t magic = 0x64006400u;
+  const uint32_t p0 = and_or<0x000F000Fu>(w, magic);
+  const uint32_t p1 = and_or<0x000F000Fu>(w >> 4, magic);
+  const uint32_t p2 = and_or<0x000F000Fu>(w >> 8, magic);
+  const uint32_t p3 = and_or<0x000F000Fu>(w >> 12, magic);
   asm("{\n\t"
       ".reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
       "mov.b32 {a0, a1}, %1;\n\tmov.b32 {a2, a3}, %2;\n\t"

@@ -60,10 +60,11 @@ struct Q4Layout {
 // (1024 + q) / (1024 + 16 q) FP16 pairs for the 8 codes of `w` (q_j in bits 4j..4j+3).
 __device__ __forceinline__ void q4_pairs(uint32_t w, uint32_t (&p)[4]) {
   const uint32_t w8 = w >> 8;
-  p[0] = (w & 0x000F000Fu) | 0x64006400u;
-  p[1] = (w & 0x00F000F0u) | 0x64006400u;
-  p[2] = (w8 & 0x000F000Fu) | 0x64006400u;
-  p[3] = (w8 & 0x00F000F0u) | 0x64006400u;
+  const uint32_t magic = 0x64006400u;
+  p[0] = and_or<0x000F000Fu>(w, magic);
+  p[1] = and_or<0x00F000F0u>(w, magic);
+  p[2] = and_or<0x000F000Fu>(w8, magic);
+  p[3] = and_or<0x00F000F0u>(w8, magic);
 }
 
 __device__ __forceinline__ void q4_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,

@@ -44,7 +44,9 @@ typedef enum {
   W4A16_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned                */
   W4A16_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
   W4A16_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (device status) */
-  W4A16_ERR_WORKSPACE = 6    /* workspace pointer/size does not meet the query  */
+  W4A16_ERR_WORKSPACE = 6,   /* workspace pointer/size does not meet the query  */
+  W4A16_ERR_LAYOUT = 7       /* a kernel found its shared memory misaligned and
+                                skipped its work (device status)                  */
 } w4a16_status;
 
 /* Human-readable name of a status (static string, never NULL). */
@@ -148,8 +150,9 @@ w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t*
 /*
  * w4a16_device_status -- synchronizes `stream`, then reads and clears the current
  * device's status word. Returns W4A16_ERR_TIMEOUT if any kernel of this library gave
- * up a bounded wait since the last query, W4A16_ERR_CUDA if the synchronization
- * failed, W4A16_OK otherwise. (The pages have no counterpart; this is the library's
+ * up a bounded wait since the last query, W4A16_ERR_LAYOUT if a kernel found its
+ * dynamic shared memory less than 128-byte aligned and skipped its work (its output is
+ * then not written), W4A16_ERR_CUDA if the synchronization failed, W4A16_OK otherwise. (The pages have no counterpart; this is the library's
  * failure-detection hook.)
  */
 w4a16_status w4a16_device_status(w4a16_stream_t stream);

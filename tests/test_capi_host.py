@@ -56,7 +56,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for code, name in enumerate(["W4A16_OK", "W4A16_ERR_INVALID_ARG", "W4A16_ERR_UNSUPPORTED",
                                  "W4A16_ERR_MISALIGNED", "W4A16_ERR_CUDA", "W4A16_ERR_TIMEOUT",
-                                 "W4A16_ERR_WORKSPACE"]):
+                                 "W4A16_ERR_WORKSPACE", "W4A16_ERR_LAYOUT"]):
         assert lib.w4a16_status_string(code).decode() == name
     assert lib.w4a16_status_string(99).decode() == "W4A16_ERR_UNKNOWN"
 
