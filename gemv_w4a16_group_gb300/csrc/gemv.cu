@@ -266,46 +266,65 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
   }
 
   // ---------------- consumer warps ----------------
+  // x -> FP16 in B-fragment order, per (row m, group g) scale 2^e and the sums X, T. An
+  // item is 16 consecutive x values (packed rows R = 2p and R + 1); the 8 items of a group
+  // sit on 8 adjacent lanes. Item i = m * half + p (p fastest), half = rows_pad / 2; this
+  // thread's items are tid + t * NC. Their indices do not depend on the previous kernel, so
+  // the first four are worked out before waiting on it.
+  const int half = rows_pad >> 1;
+  const int items = MR * half;
+  const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
+  constexpr int kBatch = 2;  // items per thread whose loads are issued together
+  int im0[kBatch], ip0[kBatch];
+#pragma unroll
+  for (int t = 0; t < kBatch; ++t) {
+    const int i = t * NC + tid;
+    im0[t] = i / half;
+    ip0[t] = i - im0[t] * half;
+  }
   pdl_wait();  // x, y and the workspace may belong to the previous kernel on the stream
   {
-    // x -> FP16 in B-fragment order, per (row m, group g) scale 2^e and the sums X, T.
-    // Item i = m * rows_pad + R (R fastest): the 16 lanes of a group are adjacent.
     const int rows = K >> 3;
-    const int items = MR * rows_pad;
-    const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
-    // Loads of up to 4 items per thread are issued before any of them is used.
-    for (int base = 0; base < items_pad; base += 4 * NC) {
-      uint4 xin[4];
+    // Loads of up to kBatch items per thread are issued before any of them is used.
+    for (int base = 0; base < items_pad; base += kBatch * NC) {
+      uint4 xin[kBatch][2];
+      int im[kBatch], ip[kBatch];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kBatch; ++t) {
         const int i = base + t * NC + tid;
-        const int m = i / rows_pad, R = i - m * rows_pad;
-        xin[t] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < items && m < M && R < rows)
-          xin[t] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(m) * K + 8 * R));
+        im[t] = base == 0 ? im0[t] : i / half;
+        ip[t] = base == 0 ? ip0[t] : i - im[t] * half;
+        const int R = 2 * ip[t];
+        xin[t][0] = xin[t][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < items && im[t] < M && R < rows) {
+          const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(im[t]) * K + 8 * R);
+          xin[t][0] = __ldg(src);
+          xin[t][1] = __ldg(src + 1);
+        }
       }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kBatch; ++t) {
         const int i = base + t * NC + tid;
         if (i >= items_pad) break;  // warp-uniform: items_pad and the strides are multiples of 32
-        const int m = i / rows_pad, R = i - m * rows_pad;
-        float v[8];
-        const uint32_t xw[4] = {xin[t].x, xin[t].y, xin[t].z, xin[t].w};
+        const int m = im[t], R = 2 * ip[t];
+        float v[16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          v[2 * h] = bf16_bits_to_f32(xw[h] & 0xFFFFu);
-          v[2 * h + 1] = __uint_as_float(xw[h] & 0xFFFF0000u);
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t xw[4] = {xin[t][r].x, xin[t][r].y, xin[t][r].z, xin[t][r].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            v[8 * r + 2 * h] = bf16_bits_to_f32(xw[h] & 0xFFFFu);
+            v[8 * r + 2 * h + 1] = __uint_as_float(xw[h] & 0xFFFF0000u);
+          }
         }
         float amax = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
-        float sum_even = (v[0] + v[2]) + (v[4] + v[6]);
-        float sum_odd = (v[1] + v[3]) + (v[5] + v[7]);
-        float sum = sum_even + sum_odd;
+        for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+        float sum_even = ((v[0] + v[2]) + (v[4] + v[6])) + ((v[8] + v[10]) + (v[12] + v[14]));
+        float sum_odd = ((v[1] + v[3]) + (v[5] + v[7])) + ((v[9] + v[11]) + (v[13] + v[15]));
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
+        for (int o = 1; o < 8; o <<= 1) {
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          sum += __shfl_xor_sync(0xffffffffu, sum, o);
           sum_even += __shfl_xor_sync(0xffffffffu, sum_even, o);
           sum_odd += __shfl_xor_sync(0xffffffffu, sum_odd, o);
         }
@@ -316,15 +335,19 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
           e = max(-100, min(100, 141 - static_cast<int>(__float_as_uint(amax) >> 23)));
         const float lo = pow2f(e), hi = pow2f(e - 4);
         if (i < items) {
-          uint4 out;
-          out.x = f16x2_bits(v[0] * lo, v[4] * lo);  // (x0, x4) 2^e
-          out.y = f16x2_bits(v[1] * hi, v[5] * hi);  // (x1, x5) 2^(e-4)
-          out.z = f16x2_bits(v[2] * lo, v[6] * lo);  // (x2, x6) 2^e
-          out.w = f16x2_bits(v[3] * hi, v[7] * hi);  // (x3, x7) 2^(e-4)
-          sXperm[R * MR + m] = out;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float* w = v + 8 * r;
+            uint4 out;
+            out.x = f16x2_bits(w[0] * lo, w[4] * lo);  // (x0, x4) 2^e
+            out.y = f16x2_bits(w[1] * hi, w[5] * hi);  // (x1, x5) 2^(e-4)
+            out.z = f16x2_bits(w[2] * lo, w[6] * lo);  // (x2, x6) 2^e
+            out.w = f16x2_bits(w[3] * hi, w[7] * hi);  // (x3, x7) 2^(e-4)
+            sXperm[(R + r) * MR + m] = out;
+          }
           if ((R & 15) == 0 && R < rows) {
             const int g = R >> 4;
-            sX[m * G + g] = sum;
+            sX[m * G + g] = sum_even + sum_odd;
             sT[m * G + g] = fmaf(1024.0f, sum_even, 64.0f * sum_odd);
             sU[m * G + g] = pow2f(-e);
           }
