@@ -28,7 +28,7 @@ __all__ = [
     "W4A16Error", "library_path", "w4a16_quantize", "w4a16_pack", "w4a16_matmul",
     "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
-    "testing_set_q4_variant",
+    "testing_set_q4_variant", "testing_set_skinny_range",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -75,6 +75,8 @@ def _load():
                  "w4a16_testing_set_q4_variant"):
         getattr(lib, name).argtypes = [I]
         getattr(lib, name).restype = I
+    lib.w4a16_testing_set_skinny_range.argtypes = [I, I]
+    lib.w4a16_testing_set_skinny_range.restype = I
     return lib
 
 
@@ -215,12 +217,20 @@ def w4a16_selftest_bounded_wait(limit_us: int, stream=None) -> int:
 
 
 def testing_force_kernel(kernel: int) -> int:
-    """0 = by M, 1 = the small-M GEMV kernel, 2 = the tcgen05 tensor-core kernel."""
+    """0 = by M, 1 = the small-M GEMV kernel, 2 = the tcgen05 tensor-core kernel, 3 = the
+    skinny kernel (M <= 32, needs the workspace reported for an M in the skinny range)."""
     return int(_lib.w4a16_testing_force_kernel(kernel))
 
 
 def testing_set_gemv_max_m(m: int) -> int:
     return int(_lib.w4a16_testing_set_gemv_max_m(m))
+
+
+def testing_set_skinny_range(lo: int, hi: int):
+    """Range of M sent to the skinny kernel by the by-M choice; negative values only query.
+    Returns the previous (lo, hi)."""
+    prev = int(_lib.w4a16_testing_set_skinny_range(lo, hi))
+    return prev >> 8, prev & 0xFF
 
 
 def testing_set_q4_variant(v: int) -> int:

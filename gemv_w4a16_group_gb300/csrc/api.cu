@@ -41,6 +41,26 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 int g_force_kernel = 0;
 // M at or below which the CUDA-core GEMV runs when the choice is by M.
 int g_gemv_max_m = 8;
+int g_skinny_min_m = 9;
+int g_skinny_max_m = 32;
+
+// The skinny kernel keeps its converted activations in the workspace past a reserve it
+// never writes: the split-K kernels keep their arrival counters (which must stay zero
+// between calls) at the start of the workspace, and any split plan that fits a workspace of
+// W bytes has at most W / 128 + 256 bytes of counters (its fp32 partials take at least 128
+// times the counters' bytes). So a workspace may be shared by skinny and split-K shapes.
+size_t skinny_reserve(size_t workspace_bytes) {
+  return ((workspace_bytes / 128 + 256 + 255) / 256) * 256;
+}
+
+// Smallest workspace (a multiple of 256 bytes) whose part past the reserve holds `bytes`.
+size_t skinny_workspace_total(size_t bytes) {
+  size_t w = ((bytes + 512 + 255) / 256) * 256;
+  while (w - skinny_reserve(w) < bytes) w += 256;
+  return w;
+}
+
+bool skinny_by_m(int M) { return M >= g_skinny_min_m && M <= g_skinny_max_m; }
 
 uint64_t g_wait_limit_ns = w4k::kDefaultWaitLimitNs;
 
@@ -114,6 +134,8 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw, w4a16_s
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
   if (M <= 0 || N <= 0 || K <= 0 || group != 128 || K % group != 0) return 0;
   size_t bytes = 0;
+  w4k::SkinnyPlan sk;
+  if (skinny_by_m(M) && w4k::skinny_plan(M, N, K, &sk)) return skinny_workspace_total(sk.ws_bytes);
   if (M <= g_gemv_max_m && w4k::gemv_supports(M, K))
     w4k::gemv_split_plan(M, N, K, &bytes);
   else
@@ -136,7 +158,24 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
   uint32_t* status = status_word_ptr();
   if (status == nullptr) return W4A16_ERR_CUDA;
   int kernel = g_force_kernel;
-  if (kernel == 0) kernel = (M <= g_gemv_max_m && w4k::gemv_supports(M, K)) ? 1 : 2;
+  w4k::SkinnyPlan sk;
+  const bool sk_plan = w4k::skinny_plan(M, N, K, &sk);
+  const size_t sk_reserve = skinny_reserve(workspace_bytes);
+  const bool sk_room = workspace != nullptr && workspace_bytes >= sk_reserve &&
+                       workspace_bytes - sk_reserve >= sk.ws_bytes;
+  if (kernel == 0) {
+    if (skinny_by_m(M) && sk_plan && sk_room)
+      kernel = 3;
+    else
+      kernel = (M <= g_gemv_max_m && w4k::gemv_supports(M, K)) ? 1 : 2;
+  }
+  if (kernel == 3) {
+    if (!sk_plan) return W4A16_ERR_UNSUPPORTED;
+    if (!sk_room) return W4A16_ERR_WORKSPACE;
+    return from_cuda(w4k::launch_w4a16_skinny(x, q, scales, mins, y, M, N, K,
+                                              static_cast<char*>(workspace) + sk_reserve, sk,
+                                              status, g_wait_limit_ns, s));
+  }
   if (kernel == 1) {
     // The GEMV takes up to gemv_max_rows() rows per launch; larger M (forced) loops.
     const int step = w4k::gemv_max_rows();
@@ -235,7 +274,7 @@ w4a16_status w4a16_selftest_bounded_wait(uint32_t limit_us, w4a16_stream_t strea
 
 // Test and benchmark hooks (declared in w4a16_testing.h, not part of the public header).
 int w4a16_testing_force_kernel(int kernel) {
-  if (kernel < 0 || kernel > 2) return -1;
+  if (kernel < 0 || kernel > 3) return -1;
   const int prev = g_force_kernel;
   g_force_kernel = kernel;
   return prev;
@@ -244,6 +283,15 @@ int w4a16_testing_force_kernel(int kernel) {
 int w4a16_testing_set_gemv_max_m(int m) {
   const int prev = g_gemv_max_m;
   if (m >= 0) g_gemv_max_m = m;
+  return prev;
+}
+
+int w4a16_testing_set_skinny_range(int lo, int hi) {
+  const int prev = (g_skinny_min_m << 8) | g_skinny_max_m;
+  if (lo >= 0 && hi >= 0 && lo <= 255 && hi <= w4k::kSkinnyMaxRows) {
+    g_skinny_min_m = lo;
+    g_skinny_max_m = hi;
+  }
   return prev;
 }
 

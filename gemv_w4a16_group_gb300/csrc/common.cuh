@@ -122,6 +122,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Contiguous copy of `bytes` from global memory into this CTA's shared memory, completing
+// on `bar`. Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // x (innermost) must be a multiple of 16 bytes / element size.
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y) {
@@ -269,6 +280,55 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
   return r;
+}
+
+// ---------------------------------------------------------------------------
+// FP16 code pairs and the legacy tensor-core MMA (GEMV and skinny kernels)
+// ---------------------------------------------------------------------------
+// (1024 + q) / (1024 + 16 q) FP16 pairs for the 8 codes of `w` (q_j in bits 4j..4j+3):
+// p0 = (q0, q4), p1 = (16 q1, 16 q5), p2 = (q2, q6), p3 = (16 q3, 16 q7).
+__device__ __forceinline__ void code_pairs_f16(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t magic = 0x64006400u;
+  p[0] = and_or<0x000F000Fu>(w, magic);
+  p[1] = and_or<0x00F000F0u>(w, magic);
+  p[2] = and_or<0x000F000Fu>(w8, magic);
+  p[3] = and_or<0x00F000F0u>(w8, magic);
+}
+
+// D += A (16x16, FP16) * B (16x8, FP16), fp32 accumulators; fragment layout of mma.sync
+// m16n8k16 (row-major A, column-major B).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
 }
 
 // Offsets used by codes_to_f32_offset for code j of a word.

@@ -79,6 +79,28 @@ cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K
                             uint32_t* status, uint64_t wait_limit_ns, const TcSplit& split,
                             cudaStream_t stream);
 
+// Skinny W4A16 matmul for 1 <= M <= kSkinnyMaxRows (one to four n8 tiles of batch rows on
+// mma.sync): a prep kernel converts x into the caller's workspace (FP16 fragments and
+// per-group constants), then one CTA per SM streams its columns' weights and that x. Needs at
+// least 32 columns per SM and at most 192; skinny_plan() tells and sizes the workspace.
+constexpr int kSkinnyMaxRows = 32;
+struct SkinnyPlan {
+  int nt = 0;       // n8 tiles of batch rows
+  int qw = 0;       // 32-column quarters per CTA
+  int col_q = 0;    // columns per CTA: 8 col_q, the first col_r CTAs 8 (col_q + 1)
+  int col_r = 0;
+  int ctas = 0;
+  int stages = 0;
+  int rows_pad = 0;       // packed rows of x fragments (K/8 rounded up to whole chunks)
+  size_t xs_bytes = 0;    // fragments, then the per-group constants
+  size_t ws_bytes = 0;
+};
+bool skinny_plan(int M, int N, int K, SkinnyPlan* plan);
+cudaError_t launch_w4a16_skinny(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
+                                const uint16_t* mins, uint16_t* y, int M, int N, int K,
+                                void* workspace, const SkinnyPlan& plan, uint32_t* status,
+                                uint64_t wait_limit_ns, cudaStream_t stream);
+
 // Q4 block-32 GEMV.
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                               uint16_t* y, int N, int K, int variant, cudaStream_t stream);

@@ -16,13 +16,19 @@ extern "C" {
 
 /* Kernel w4a16_matmul uses: 0 = chosen by M (default), 1 = the small-M GEMV kernel
  * (forced for M > 8 it runs once per block of 8 rows), 2 = the TMA + tcgen05
- * tensor-core kernel. Returns the previous choice, or -1 if `kernel` is out of range
- * (nothing changes then). */
+ * tensor-core kernel, 3 = the skinny kernel (M <= 32; needs the workspace that
+ * w4a16_matmul_workspace_bytes reports for an M in the skinny range). Returns the previous
+ * choice, or -1 if `kernel` is out of range (nothing changes then). */
 int w4a16_testing_force_kernel(int kernel);
 
 /* Largest M that the by-M choice sends to the GEMV kernel (default 8, its maximum). A
  * negative value only queries. Returns the previous value. */
 int w4a16_testing_set_gemv_max_m(int m);
+
+/* Range of M that the by-M choice sends to the skinny kernel when the shape fits it and the
+ * workspace is large enough (default 9..32; hi at most 32). Negative values only query.
+ * Returns the previous range as (lo << 8) | hi. */
+int w4a16_testing_set_skinny_range(int lo, int hi);
 
 /* Kernel of q4b32_gemv: 2 = TMA-staged tensor-pipe kernel (default; shapes it does not
  * take fall back to 1), 1 = CUDA-core kernel with mixed FP16 FMAs, 0 = CUDA-core kernel
