@@ -206,7 +206,8 @@ def roofline_us(bytes_, flops, peaks):
 # --------------------------------------------------------------------------- #
 
 def workspace_for(M, N, K, device):
-    """The split-K workspace the library asks for at this shape (zero-filled), or None."""
+    """The workspace the library asks for at this shape (zero-filled), or None: split-K
+    partials and counters, or the skinny kernel's converted activations."""
     import gemv_w4a16_group_gb300 as w4
 
     need = w4.w4a16_matmul_workspace_bytes(M, N, K)
@@ -548,19 +549,22 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
-PROFILE_CASES = ("gemv_m1", "gemv_m8", "tc_m16", "tc_m4096", "q4b32_gemv", "quantize", "pack")
+PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
+                 "q4b32_gemv", "quantize", "pack")
 
 
 def profile_case(args):
     """A few launches of one workload, untimed, for a profiler (ncu -k ... -c ...): the
-    Llama-3-8B up-projection (14336 x 4096) at M = 1, 8, 16 or 4096 with 6 rotating weight
-    copies (174 MB > L2), the Q4 block-32 GEMV (16384 x 16384), or quantize / pack."""
+    Llama-3-8B up-projection (14336 x 4096) at M = 1, 8, 16 or 32 (skinny kernel), 16
+    (tensor-core kernel) or 4096 with 6 rotating weight copies (174 MB > L2), the Q4
+    block-32 GEMV (16384 x 16384), or quantize / pack."""
     import gemv_w4a16_group_gb300 as w4
 
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     case, n = args.case, args.launches
-    if case in ("gemv_m1", "gemv_m8", "tc_m16", "tc_m4096", "quantize", "pack"):
+    if case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
+                "quantize", "pack"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
         if case == "quantize":
@@ -571,7 +575,10 @@ def profile_case(args):
                 w4.w4a16_pack(codes, qw=qw)
         else:
             del w, codes
-            M = {"gemv_m1": 1, "gemv_m8": 8, "tc_m16": 16, "tc_m4096": 4096}[case]
+            M = {"gemv_m1": 1, "gemv_m8": 8, "skinny_m16": 16, "skinny_m32": 32, "tc_m16": 16,
+                 "tc_m4096": 4096}[case]
+            if case == "tc_m16":  # the tensor-core kernel, not the skinny one the size picks
+                w4.testing_force_kernel(2)
             cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
             x = workloads.activations_bf16(M, K, seed=M).to(device)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=device)

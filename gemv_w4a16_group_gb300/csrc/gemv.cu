@@ -221,11 +221,19 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
 
   // ---------------- consumer warps ----------------
   // x -> FP16 in B-fragment order, per (row m, group g) scale 2^e and the sums X, T. An
-  // item is 16 consecutive x values (packed rows R = 2p and R + 1); the 8 items of a group
-  // sit on 8 adjacent lanes. Item i = m * half + p (p fastest), half = rows_pad / 2; this
-  // thread's items are tid + t * NC. Their indices do not depend on the previous kernel, so
-  // the first four are worked out before waiting on it.
-  const int half = rows_pad >> 1;
+  // item is 16 consecutive x values (packed rows R = r_lo + 2p and R + 1); the 8 items of a
+  // group sit on 8 adjacent lanes. Item i = m * half + p (p fastest), half = (r_hi - r_lo) / 2;
+  // this thread's items are tid + t * NC. Their indices do not depend on the previous
+  // kernel, so the first kBatch are worked out before waiting on it.
+  // A CTA that owns a single unit of a split plan reads only its own k-range of x, so it
+  // converts only those rows (whole chunks: the 8 items of a group stay together).
+  int r_lo = 0, r_hi = rows_pad;
+  if (splits > 1 && static_cast<int>(gridDim.x) >= nunits) {
+    const int kr = static_cast<int>(blockIdx.x) % splits;
+    r_lo = kr * per_unit * ROWS;
+    r_hi = min(kchunks, (kr + 1) * per_unit) * ROWS;
+  }
+  const int half = (r_hi - r_lo) >> 1;
   const int items = MR * half;
   const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
   constexpr int kBatch = 2;  // items per thread whose loads are issued together
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
         const int i = base + t * NC + tid;
         im[t] = base == 0 ? im0[t] : i / half;
         ip[t] = base == 0 ? ip0[t] : i - im[t] * half;
-        const int R = 2 * ip[t];
+        const int R = r_lo + 2 * ip[t];
         xin[t][0] = xin[t][1] = make_uint4(0u, 0u, 0u, 0u);
         if (i < items && im[t] < M && R < rows) {
           const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(im[t]) * K + 8 * R);
@@ -260,7 +268,7 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
       for (int t = 0; t < kBatch; ++t) {
         const int i = base + t * NC + tid;
         if (i >= items_pad) break;  // warp-uniform: items_pad and the strides are multiples of 32
-        const int m = im[t], R = 2 * ip[t];
+        const int m = im[t], R = r_lo + 2 * ip[t];
         float v[16];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {

@@ -58,7 +58,10 @@ struct SkShape {
   static constexpr uint32_t tx_bytes = word_bytes + 2u * row_bytes + x_bytes + c_bytes;
   static constexpr uint32_t stage_bytes =
       (word_bytes + 2u * row_stride + x_bytes + c_bytes + 1023u) & ~1023u;
-  static constexpr uint32_t red_bytes = static_cast<uint32_t>(W) * MRP * 4u;  // [W][MRP] fp32
+  // Group partials [MRP][W + 1] fp32: the extra column puts the rows 2c of a warp's lanes in
+  // different banks.
+  static constexpr int RED_LD = W + 1;
+  static constexpr uint32_t red_bytes = (static_cast<uint32_t>(RED_LD) * MRP * 4u + 15u) & ~15u;
   static constexpr int kMinBlocks = NT == 1 ? 2 : 1;
   static_assert(GPC * QW == kSkConsumerWarps, "one (group, quarter) per consumer warp");
   static_assert(box_bytes % 1024u == 0u, "swizzled word boxes start on 1024-byte boundaries");
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kSkThreads, SkShape<NT, QW>::kMinBlocks)
   }
   uint8_t* smem = smem_raw + pad;
   const uint32_t ring_bytes = static_cast<uint32_t>(stages) * S::stage_bytes;
-  float* sRed = reinterpret_cast<float*>(smem + ring_bytes);  // [W][MRP]
+  float* sRed = reinterpret_cast<float*>(smem + ring_bytes);  // [MRP][W + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes + S::red_bytes);
   uint64_t* empty = full + kSkMaxStages;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kSkMaxStages);
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(kSkThreads, SkShape<NT, QW>::kMinBlocks)
         for (int col = 0; col < 4; ++col)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            float* dst = sRed + (qq * 32 + gq * 4 + col) * MRP + 8 * j + 2 * c + r;
+            float* dst = sRed + (8 * j + 2 * c + r) * S::RED_LD + qq * 32 + gq * 4 + col;
             *dst = gg == 0 ? yacc[j][col][r] : *dst + yacc[j][col][r];
           }
     }
@@ -362,7 +365,8 @@ __global__ void __launch_bounds__(kSkThreads, SkShape<NT, QW>::kMinBlocks)
     const int m = i / S::W, col = i - m * S::W;
     const int nn = col0 + col;
     if (m < M && nn < col_end)
-      y[static_cast<size_t>(m) * N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(sRed[col * MRP + m]));
+      y[static_cast<size_t>(m) * N + nn] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(sRed[m * S::RED_LD + col]));
   }
 }
 
