@@ -552,9 +552,10 @@ int stages_for(int MR, int K, uint32_t budget) {
 
 template <int QW, int CW>
 int stages_of(int MR, int K) {
-  // Two CTAs per SM when the ring can still hold two stages, else the whole SM.
+  // Two CTAs per SM when the ring can still hold three stages, else the whole SM (with x
+  // for four or eight rows in shared memory, two stages were slower than one CTA per SM).
   const int two = CW <= 12 ? stages_for<QW, CW>(MR, K, kSmemTwoCtas) : 0;
-  return two >= 2 ? two : stages_for<QW, CW>(MR, K, kSmemOneCta);
+  return two >= 3 ? two : stages_for<QW, CW>(MR, K, kSmemOneCta);
 }
 
 template <int MR, int QW, int CW>
@@ -627,6 +628,10 @@ GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed) {
   const int per_unit = (kchunks + splits - 1) / splits;
   splits = (kchunks + per_unit - 1) / per_unit;  // no empty k-range
   if (splits < 2) return split;
+  // The last CTA of a slab adds the partials after a fence and an atomic: about 1.5 us on
+  // the critical path, worth it only when a CTA skips three chunks or more (4096 x 4096:
+  // 6.3 us split in two vs 4.7 us whole; 1536 x 8960: 5.8 us split in six vs 7.6 us whole).
+  if (kchunks - per_unit < 3) return split;
   split.splits = splits;
   split.partial_offset = ((static_cast<size_t>(plan.nslab) * 4 + 255) / 256) * 256;
   *bytes_needed = split.partial_offset + static_cast<size_t>(splits) * mr_of(M) * N * 4;

@@ -324,3 +324,28 @@ def test_matmul_split_k_workspace(w4, M, N, K):
         assert w4.w4a16_device_status() == 0
     finally:
         w4.testing_set_gemv_max_m(prev)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1536, 8960), (2, 4096, 14336), (4, 1536, 8960),
+                                   (8, 512, 8192), (1, 4096, 4096), (3, 256, 8192)])
+def test_gemv_split_k_workspace(w4, M, N, K):
+    """GEMV launches (M <= 8) that split K over CTAs through the workspace (and one shape,
+    4096 x 4096, whose plan no longer splits): the oracle's tolerance, the same bits twice,
+    and the arrival counters (at most 64 slabs here: the first 256 bytes) left at zero."""
+    need = w4.w4a16_matmul_workspace_bytes(M, N, K)
+    w, codes, s_np, m_np, qw_np = quantized(N, K, seed=3 * M + N)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(M, K, seed=K + M)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    y1 = w4.w4a16_matmul(x.cuda(), qw, s, m, workspace=ws if need else None)
+    y2 = w4.w4a16_matmul(x.cuda(), qw, s, m, workspace=ws if need else None)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    cols = None if N * K <= 2**24 else workloads.sample_indices(N, 128, seed=M).numpy()
+    y_ref, a_ref = oracle.w4a16_matmul(bits(x), qw_np, s_np, m_np, cols=cols)
+    yv = y1.float().cpu().numpy()
+    if cols is not None:
+        yv = yv[:, cols]
+    assert oracle.within_tolerance(yv, y_ref, a_ref).all()
+    assert torch.count_nonzero(ws[:256]).item() == 0
+    assert w4.w4a16_device_status() == 0
