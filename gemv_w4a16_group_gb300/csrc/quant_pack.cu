@@ -16,40 +16,73 @@
 
 namespace w4k {
 
-// One warp per (row n, group g) of 128 weights: 4 consecutive weights per lane.
+// rint(fl(d / s)), the code rule of both quantizers (fp32 quotient, rounded to nearest
+// even), with one multiply instead of a correctly rounded division per weight. rs = fl(1/s).
+// t = fl(d rs) has relative error at most 2^-23, and fl(d / s) is within half an ulp of d / s,
+// so for |d / s| <= 16 the two lie within 2^-19 + 2^-20 < 2^-17 of each other: rounding t to
+// an integer gives the same result unless t is within 2^-17 of a half-integer (|t - rint(t)|
+// above 1/2 - 2^-17), and there the quotient is computed exactly (this also catches every
+// exact tie). Past 16 both clamp to the same end code; the exact fallback is always right.
+__device__ __forceinline__ float rint_quotient(float d, float s, float rs) {
+  const float t = __fmul_rn(d, rs);
+  const float r = rintf(t);
+  if (fabsf(__fsub_rn(t, r)) > 0.5f - 0x1p-17f) return rintf(__fdiv_rn(d, s));
+  return r;
+}
+
+// A warp takes four consecutive groups of 128 weights of one row (consecutive warps:
+// consecutive groups, so reads are contiguous), 4 consecutive weights of each per lane; the
+// four loads of a lane are issued before any is used.
+constexpr int kQGroupsPerWarp = 4;
+
 __global__ void __launch_bounds__(256)
 w4a16_quantize_kernel(const float* __restrict__ w, int N, int K, uint8_t* __restrict__ codes,
                       uint16_t* __restrict__ scales, uint16_t* __restrict__ mins) {
   const int groups = K >> 7;
-  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (gw >= static_cast<long long>(groups) * N) return;
+  const int per_row = (groups + kQGroupsPerWarp - 1) / kQGroupsPerWarp;  // warps per row
+  const long long wi = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wi >= static_cast<long long>(per_row) * N) return;
   const int lane = threadIdx.x & 31;
-  const int g = static_cast<int>(gw / N);
-  const int n = static_cast<int>(gw % N);  // consecutive warps: consecutive n, same g
-  const size_t off = static_cast<size_t>(n) * K + static_cast<size_t>(g) * 128 + lane * 4;
-  const float4 v = __ldcs(reinterpret_cast<const float4*>(w + off));
-  float lo = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
-  float hi = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  const int n = static_cast<int>(wi / per_row);
+  const int g0 = static_cast<int>(wi - static_cast<long long>(n) * per_row) * kQGroupsPerWarp;
+  float4 v[kQGroupsPerWarp];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  for (int j = 0; j < kQGroupsPerWarp; ++j) {
+    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g0 + j < groups)  // warp-uniform
+      v[j] = __ldcs(reinterpret_cast<const float4*>(
+          w + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + j) * 128 + lane * 4));
   }
-  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-  const __nv_bfloat16 s_b = __float2bfloat16_rn(s32);
-  const __nv_bfloat16 m_b = __float2bfloat16_rn(lo);
-  const float s = __bfloat162float(s_b);
-  const float m = __bfloat162float(m_b);
-  auto code = [&](float x) -> uint32_t {
-    if (s == 0.0f) return 0u;
-    const float r = rintf(__fdiv_rn(__fsub_rn(x, m), s));
-    return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 15.0f));
-  };
-  const uint32_t packed = code(v.x) | (code(v.y) << 8) | (code(v.z) << 16) | (code(v.w) << 24);
-  *reinterpret_cast<uint32_t*>(codes + off) = packed;
-  if (lane == 0) {
-    scales[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(s_b);
-    mins[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(m_b);
+#pragma unroll
+  for (int j = 0; j < kQGroupsPerWarp; ++j) {
+    const int g = g0 + j;
+    if (g >= groups) break;  // warp-uniform
+    float lo = fminf(fminf(v[j].x, v[j].y), fminf(v[j].z, v[j].w));
+    float hi = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    const __nv_bfloat16 s_b = __float2bfloat16_rn(s32);
+    const __nv_bfloat16 m_b = __float2bfloat16_rn(lo);
+    const float s = __bfloat162float(s_b);
+    const float m = __bfloat162float(m_b);
+    const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    auto code = [&](float x) -> uint32_t {
+      if (s == 0.0f) return 0u;
+      const float d = __fsub_rn(x, m);
+      return static_cast<uint32_t>(fminf(fmaxf(rint_quotient(d, s, rs), 0.0f), 15.0f));
+    };
+    const uint32_t packed =
+        code(v[j].x) | (code(v[j].y) << 8) | (code(v[j].z) << 16) | (code(v[j].w) << 24);
+    *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(n) * K +
+                                 static_cast<size_t>(g) * 128 + lane * 4) = packed;
+    if (lane == 0) {
+      scales[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(s_b);
+      mins[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(m_b);
+    }
   }
 }
 
@@ -92,35 +125,46 @@ w4a16_pack_kernel(const uint8_t* __restrict__ codes, int N, int K, uint32_t* __r
   }
 }
 
-// Q4: 8 lanes per block of 32 weights, 4 weights per lane.
+// Q4: a warp takes 512 consecutive weights as four slots of 128 (8 lanes per block of 32,
+// 4 weights per lane in each slot); the four loads of a lane are issued before any is used.
 __global__ void __launch_bounds__(256)
 q4b32_quantize_kernel(const float* __restrict__ w, int N, int K, uint8_t* __restrict__ codes,
                       uint16_t* __restrict__ scales) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(N) * (K >> 2);  // float4 units
-  const bool ok = i < total;
-  const long long e = ok ? i * 4 : 0;  // element index n*K + k
-  const float4 v = ok ? __ldcs(reinterpret_cast<const float4*>(w + e)) : make_float4(0, 0, 0, 0);
-  float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  const long long total = static_cast<long long>(N) * K;  // weights
+  const long long base = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 512;
+  const int lane = threadIdx.x & 31;
+  float4 v[4];
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const __half s_h = __float2half_rn(__fdiv_rn(a, 8.0f));
-  const float s = __half2float(s_h);
-  auto code = [&](float x) -> uint32_t {
-    if (s == 0.0f) return 8u;
-    const float r = rintf(__fdiv_rn(x, s)) + 8.0f;
-    return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 15.0f));
-  };
-  if (!ok) return;
-  const uint32_t b0 = code(v.x) | (code(v.y) << 4);
-  const uint32_t b1 = code(v.z) | (code(v.w) << 4);
-  *reinterpret_cast<uint16_t*>(codes + e / 2) = static_cast<uint16_t>(b0 | (b1 << 8));
-  if ((threadIdx.x & 7) == 0) scales[e / 32] = __half_as_ushort(s_h);
+  for (int j = 0; j < 4; ++j) {
+    const long long e = base + j * 128 + lane * 4;  // blocks of 32 never straddle rows
+    v[j] = e < total ? __ldcs(reinterpret_cast<const float4*>(w + e)) : make_float4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const long long e = base + j * 128 + lane * 4;
+    float a = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const __half s_h = __float2half_rn(__fdiv_rn(a, 8.0f));
+    const float s = __half2float(s_h);
+    const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    auto code = [&](float x) -> uint32_t {
+      if (s == 0.0f) return 8u;
+      const float r = rint_quotient(x, s, rs) + 8.0f;
+      return static_cast<uint32_t>(fminf(fmaxf(r, 0.0f), 15.0f));
+    };
+    if (e >= total) continue;
+    const uint32_t b0 = code(v[j].x) | (code(v[j].y) << 4);
+    const uint32_t b1 = code(v[j].z) | (code(v[j].w) << 4);
+    *reinterpret_cast<uint16_t*>(codes + e / 2) = static_cast<uint16_t>(b0 | (b1 << 8));
+    if ((lane & 7) == 0) scales[e / 32] = __half_as_ushort(s_h);
+  }
 }
 
 cudaError_t launch_w4a16_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   uint16_t* mins, cudaStream_t stream) {
-  const long long warps = static_cast<long long>(K >> 7) * N;
+  const long long warps =
+      static_cast<long long>(((K >> 7) + kQGroupsPerWarp - 1) / kQGroupsPerWarp) * N;
   const long long blocks = (warps + 7) / 8;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   w4a16_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, codes, scales,
@@ -139,8 +183,8 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
 
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   cudaStream_t stream) {
-  const long long total = static_cast<long long>(N) * (K >> 2);
-  const long long blocks = (total + 255) / 256;
+  const long long total = static_cast<long long>(N) * K;  // weights, 512 per warp
+  const long long blocks = (total + 8 * 512 - 1) / (8 * 512);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   q4b32_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, codes, scales);
   return cudaGetLastError();

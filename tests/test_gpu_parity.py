@@ -349,3 +349,21 @@ def test_gemv_split_k_workspace(w4, M, N, K):
     assert oracle.within_tolerance(yv, y_ref, a_ref).all()
     assert torch.count_nonzero(ws[:256]).item() == 0
     assert w4.w4a16_device_status() == 0
+
+
+def test_q4_quantize_exact_ties(w4):
+    """Q4 blocks whose quotients w / s are exact half-integers (s = 0.125 exactly), plus the
+    +-8 s ends that clamp: codes and scales bit-exact against the oracle (rounding to even)."""
+    N, K = 4, 128
+    ties = (np.arange(-8, 8) + 0.5) * 0.125                       # 16 exact ties
+    w = np.zeros((N, K), dtype=np.float32)
+    for n in range(N):
+        for b in range(K // 32):
+            blk = np.concatenate([ties, ties[::-1]]).astype(np.float32)
+            blk[(n + b) % 32] = 1.0 if (n + b) % 2 == 0 else -1.0  # max |w| = 8 s
+            w[n, 32 * b:32 * (b + 1)] = blk
+    codes, sc = oracle.q4b32_quantize(w)
+    gc, gs = w4.q4b32_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(gc.cpu().numpy(), codes)
+    assert np.array_equal(bits(gs), sc)
