@@ -13,6 +13,8 @@ Array conventions (all numpy, C-contiguous):
     bits [K/G, N]; ``qw`` int32 [K/8, N]; ``x`` bf16 bits [M, K].
   * Q4 block-32: ``codes`` uint8 [N, K/2]; ``scales`` fp16 bits [N, K/32];
     ``x`` fp16 bits [K].
+  * W4A16 with a zero point: ``qw_rows`` uint32 [N, K/8]; ``scales``/``zeros``
+    fp16 bits [N, K/G] (the layout the format's page stores); w_hat = (q - z) s.
 """
 from __future__ import annotations
 
@@ -75,10 +77,14 @@ def _bind(lib):
     lib.oracle_q4b32_quantize.argtypes = [P, I, I, P, P]
     lib.oracle_q4b32_dequant.argtypes = [P, P, I, I, P]
     lib.oracle_q4b32_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
+    lib.oracle_w4a16zp_quantize.argtypes = [P, I, I, I, P, P, P]
+    lib.oracle_w4a16zp_dequant.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_w4a16zp_matmul.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
     for name in ("oracle_bf16_rne_array", "oracle_fp16_rne_array", "oracle_fp16_to_float_array",
                  "oracle_w4a16_quantize", "oracle_w4a16_pack", "oracle_w4a16_dequant",
                  "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_q4b32_quantize",
-                 "oracle_q4b32_dequant", "oracle_q4b32_gemv"):
+                 "oracle_q4b32_dequant", "oracle_q4b32_gemv", "oracle_w4a16zp_quantize",
+                 "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul"):
         getattr(lib, name).restype = None
     return lib
 
@@ -220,6 +226,69 @@ def w4a16_matmul(x_bits: np.ndarray, qw: np.ndarray, scales: np.ndarray, mins: n
         lib.oracle_w4a16_matmul_cols(_ptr(x_bits), _ptr(qw), _ptr(scales), _ptr(mins), M, N, K,
                                      group, _ptr(cols), len(cols), _ptr(y), _ptr(a))
     return y, a
+
+
+# --------------------------------------------------------------------------- #
+# W4A16 with a zero point
+# --------------------------------------------------------------------------- #
+
+def w4a16zp_quantize(w: np.ndarray, group: int = 128):
+    """fp32 [N, K] -> (qw_rows uint32 [N, K/8], scales fp16-bits [N, K/G],
+    zeros fp16-bits [N, K/G])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % group == 0 and group % 8 == 0
+    qw_rows = np.empty((N, K // 8), dtype=np.uint32)
+    scales = np.empty((N, K // group), dtype=np.uint16)
+    zeros = np.empty((N, K // group), dtype=np.uint16)
+    _load().oracle_w4a16zp_quantize(_ptr(w), N, K, group, _ptr(qw_rows), _ptr(scales),
+                                    _ptr(zeros))
+    return qw_rows, scales, zeros
+
+
+def w4a16zp_dequant(qw_rows: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+                    group: int = 128) -> np.ndarray:
+    """w_hat = (q - z) s, fp64 [N, K]."""
+    qw_rows = _c(qw_rows, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint16)
+    N, K = qw_rows.shape[0], qw_rows.shape[1] * 8
+    out = np.empty((N, K), dtype=np.float64)
+    _load().oracle_w4a16zp_dequant(_ptr(qw_rows), _ptr(scales), _ptr(zeros), N, K, group,
+                                   _ptr(out))
+    return out
+
+
+def w4a16zp_matmul(x_bits: np.ndarray, qw_rows: np.ndarray, scales: np.ndarray,
+                   zeros: np.ndarray, group: int = 128, cols=None):
+    """y_ref, abs_ref (fp64 [M, N] or [M, len(cols)]) for y = x . w_hat^T."""
+    x_bits = _c(x_bits, np.uint16)
+    if x_bits.ndim == 1:
+        x_bits = x_bits.reshape(1, -1)
+    qw_rows = _c(qw_rows, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint16)
+    M, K = x_bits.shape
+    N = qw_rows.shape[0]
+    assert qw_rows.shape[1] * 8 == K
+    if cols is None:
+        n_out, cols_p = N, None
+    else:
+        cols = _c(cols, np.int32)
+        n_out, cols_p = len(cols), _ptr(cols)
+    y = np.empty((M, n_out), dtype=np.float64)
+    a = np.empty((M, n_out), dtype=np.float64)
+    _load().oracle_w4a16zp_matmul(_ptr(x_bits), _ptr(qw_rows), _ptr(scales), _ptr(zeros), M, N,
+                                  K, group, cols_p, n_out, _ptr(y), _ptr(a))
+    return y, a
+
+
+def w4a16zp_kernel_layout(qw_rows: np.ndarray, scales: np.ndarray, zeros: np.ndarray):
+    """The same numbers in the matmul's input layout: words [K/8, N] (int32) and
+    scales / zeros [K/G, N]: the transpose of each array, nothing else."""
+    return (np.ascontiguousarray(_c(qw_rows, np.uint32).T).view(np.int32),
+            np.ascontiguousarray(_c(scales, np.uint16).T),
+            np.ascontiguousarray(_c(zeros, np.uint16).T))
 
 
 # --------------------------------------------------------------------------- #

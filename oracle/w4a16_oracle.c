@@ -33,6 +33,14 @@
  *   - Q4: scale = fp16_rne(fp32(max|w| / 8)); q = clamp(rne(w / s) + 8, 0, 15);
  *     a zero scale stores q = 8 (w_hat = 0).
  *   - Weights are finite.
+ *   - Zero-point format [P3]: s = fp16_rne(fp32((max - min) / 15)); a stored
+ *     s of zero becomes 1 (the pages' host code sets s = 1 when it is zero);
+ *     z = round(-min / s) against the stored s, stored as fp16;
+ *     q = clamp(round(w / s) + z, 0, 15) (the section's formula: the integer
+ *     z is added after rounding); round() here is half away from zero, the
+ *     rounding of the pages' own host code for this format (std::round).
+ *     Codes stay in the pages' layout: words [N, K/8], scales and zeros
+ *     [N, K/G].
  *
  * Parity pins (tests/test_oracle_pins.py): rounding helpers against PyTorch's
  * own conversions; hand-worked groups in tests/golden/; 4.25 bits/weight and
@@ -132,6 +140,13 @@ void oracle_fp16_to_float_array(const uint16_t* in, float* out, long n) {
 /* Round an fp32 value to the nearest integer, ties to even (the reading of
  * "round" in [P1] Step 2). */
 static float rne_int(float t) { return (float)round_half_even((double)t); }
+
+/* Round an fp32 value to the nearest integer, ties away from zero, keeping the
+ * sign of zero (-0.3 -> -0): the rounding of [P3]'s zero-point host code. */
+static float round_half_away(float t) {
+  double a = floor(fabs((double)t) + 0.5); /* exact: |t| < 2^53 */
+  return (float)copysign(a, (double)t);
+}
 
 /* ------------------------------------------------------------------------ */
 /* W4A16: quantize, pack, dequantize, matmul ([P1] Step 2).                  */
@@ -342,5 +357,93 @@ void oracle_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* 
     }
     y_ref[i] = acc;
     if (abs_ref) abs_ref[i] = acc_abs;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* W4A16 with a zero point ([P3] "The quantization formulas", "W4A16:        */
+/* dequantizing in registers"): w_hat = (q - z) * s, fp16 s and z.           */
+/* ------------------------------------------------------------------------ */
+
+/* w: fp32 [N, K]. qw_rows: uint32 [N, K/8], word (n, r) holds k = 8r + j in
+ * bits 4j..4j+3 (first element in the low 4 bits). scales, zeros: fp16 bit
+ * patterns [N, K/G] (one per row and group, as [P3] stores them). */
+void oracle_w4a16zp_quantize(const float* w, int N, int K, int G, uint32_t* qw_rows,
+                             uint16_t* scales, uint16_t* zeros) {
+  int groups = K / G;
+  memset(qw_rows, 0, (size_t)N * (K / 8) * sizeof(uint32_t));
+  for (int n = 0; n < N; ++n) {
+    for (int g = 0; g < groups; ++g) {
+      const float* wg = w + (size_t)n * K + (size_t)g * G;
+      float lo = wg[0], hi = wg[0];
+      for (int i = 1; i < G; ++i) {
+        if (wg[i] < lo) lo = wg[i];
+        if (wg[i] > hi) hi = wg[i];
+      }
+      volatile float range = hi - lo;     /* fp32 subtraction */
+      volatile float s32 = range / 15.0f; /* fp32 division by 2^4 - 1 */
+      uint16_t s_h = oracle_fp16_rne(s32);
+      if (oracle_fp16_to_float(s_h) == 0.0f) s_h = oracle_fp16_rne(1.0f);
+      float s = oracle_fp16_to_float(s_h);
+      volatile float neg_lo = -lo;
+      volatile float zq = neg_lo / s;     /* fp32 division */
+      uint16_t z_h = oracle_fp16_rne(round_half_away(zq));
+      float z = oracle_fp16_to_float(z_h);
+      scales[(size_t)n * groups + g] = s_h;
+      zeros[(size_t)n * groups + g] = z_h;
+      for (int i = 0; i < G; ++i) {
+        volatile float t = wg[i] / s;     /* fp32 division */
+        double r = (double)round_half_away(t) + (double)z;
+        int q = r < 0.0 ? 0 : (r > 15.0 ? 15 : (int)r);
+        int k = g * G + i;
+        qw_rows[(size_t)n * (K / 8) + k / 8] |= (uint32_t)q << (4 * (k % 8));
+      }
+    }
+  }
+}
+
+/* Code of weight (n, k) in the [N, K/8] word layout. */
+static int unpack_code_rows(const uint32_t* qw_rows, int K, int n, int k) {
+  return (int)((qw_rows[(size_t)n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xFu);
+}
+
+/* w_hat[n, k] = (q - z) * s in fp64 ([P3]: subtract the zero point, multiply by
+ * the scale). Exact: q - z is an integer below 2^17 and s has 11 significant
+ * bits. */
+void oracle_w4a16zp_dequant(const uint32_t* qw_rows, const uint16_t* scales,
+                            const uint16_t* zeros, int N, int K, int G, double* w_hat) {
+  int groups = K / G;
+  for (int n = 0; n < N; ++n) {
+    for (int k = 0; k < K; ++k) {
+      double s = (double)oracle_fp16_to_float(scales[(size_t)n * groups + k / G]);
+      double z = (double)oracle_fp16_to_float(zeros[(size_t)n * groups + k / G]);
+      w_hat[(size_t)n * K + k] = ((double)unpack_code_rows(qw_rows, K, n, k) - z) * s;
+    }
+  }
+}
+
+/* y_ref[m, i] = sum_k x[m, k] * w_hat[cols[i], k] in fp64 and abs_ref the sum
+ * of the magnitudes of the terms; cols == NULL means every column (ncols = N).
+ * x: bf16 bit patterns [M, K]; results [M, ncols]. */
+void oracle_w4a16zp_matmul(const uint16_t* x, const uint32_t* qw_rows, const uint16_t* scales,
+                           const uint16_t* zeros, int M, int N, int K, int G,
+                           const int32_t* cols, int ncols, double* y_ref, double* abs_ref) {
+  int groups = K / G;
+  if (!cols) ncols = N;
+  for (int m = 0; m < M; ++m) {
+    for (int i = 0; i < ncols; ++i) {
+      int n = cols ? cols[i] : i;
+      double acc = 0.0, acc_abs = 0.0;
+      for (int k = 0; k < K; ++k) {
+        double s = (double)oracle_fp16_to_float(scales[(size_t)n * groups + k / G]);
+        double z = (double)oracle_fp16_to_float(zeros[(size_t)n * groups + k / G]);
+        double w_hat = ((double)unpack_code_rows(qw_rows, K, n, k) - z) * s;
+        double xv = (double)oracle_bf16_to_float(x[(size_t)m * K + k]);
+        acc += xv * w_hat;
+        acc_abs += fabs(xv * w_hat);
+      }
+      y_ref[(size_t)m * ncols + i] = acc;
+      if (abs_ref) abs_ref[(size_t)m * ncols + i] = acc_abs;
+    }
   }
 }

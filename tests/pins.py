@@ -342,4 +342,155 @@ def pin_q4_round_trip_and_gemv():
     np.testing.assert_array_equal(y_rows, y_full[rows])
 
 
+# --------------------------------------------------------------------------- #
+# zero-point format: w_hat = (q - z) s, fp16 s and z, words [N, K/8]
+# --------------------------------------------------------------------------- #
+
+def _zp_codes(qw_rows):
+    """Codes [N, K] from words [N, K/8] (k = 8r + j in bits 4j..4j+3), with numpy."""
+    w = np.asarray(qw_rows, dtype=np.uint32)
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    return ((w[:, :, None] >> shifts) & 0xF).reshape(w.shape[0], -1).astype(np.int64)
+
+
+def _fp16_array(bits):
+    return torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16).copy()) \
+        .view(torch.float16).double().numpy()
+
+
+def _zp_w_hat(qw_rows, s, z, G):
+    """(q - z) s in fp64 from numpy unpacking and PyTorch's fp16 conversion."""
+    q = _zp_codes(qw_rows)
+    sv = np.repeat(_fp16_array(s), G, axis=1)
+    zv = np.repeat(_fp16_array(z), G, axis=1)
+    return (q - zv) * sv
+
+
+def pin_zp_hand_worked_groups():
+    """Hand-worked zero-point groups (tests/golden/w4a16zp_groups.txt): scale, zero,
+    codes and the packed word."""
+    for tag, rec in _records("w4a16zp_groups.txt"):
+        w = _weights_from(rec).reshape(1, -1)
+        qw_rows, scales, zeros = oracle.w4a16zp_quantize(w, group=w.shape[1])
+        assert int(scales[0, 0]) == int(rec["scale"][0], 16), (tag, hex(scales[0, 0]))
+        assert int(zeros[0, 0]) == int(rec["zero"][0], 16), (tag, hex(zeros[0, 0]))
+        assert int(qw_rows[0, 0]) == int(rec["word"][0], 16), (tag, hex(qw_rows[0, 0]))
+        assert _zp_codes(qw_rows)[0].tolist() == [int(v) for v in rec["q"]], tag
+
+
+def pin_zp_round_trip_on_grid():
+    """Weights (q - z) s with fp16 s, integer z in 0..15 and q = 0 and 15 in every group
+    quantize back to exactly (q, s, z) and rebuild bit for bit."""
+    rng = np.random.default_rng(17)
+    N, K, G = 20, 256, 64
+    groups = K // G
+    s_h = oracle.fp16_rne(2.0 ** rng.uniform(-10, -4, size=(N, groups)))
+    z = rng.integers(0, 16, size=(N, groups))
+    q = rng.integers(0, 16, size=(N, K))
+    q[:, ::G] = 0
+    q[:, 3::G] = 15
+    sv = np.repeat(_fp16_array(s_h), G, axis=1)
+    w = (q - np.repeat(z, G, axis=1)) * sv
+    w32 = w.astype(np.float32)
+    assert np.array_equal(w32.astype(np.float64), w), "grid values must be exact in fp32"
+    qw_rows, s2, z2 = oracle.w4a16zp_quantize(w32, group=G)
+    np.testing.assert_array_equal(s2, s_h)
+    np.testing.assert_array_equal(_fp16_array(z2), z.astype(np.float64))
+    np.testing.assert_array_equal(_zp_codes(qw_rows), q)
+    np.testing.assert_array_equal(oracle.w4a16zp_dequant(qw_rows, s2, z2, group=G), w)
+
+
+def pin_zp_codes_follow_the_formula():
+    """On random groups, every scale, zero and code equals the formula evaluated with
+    exact rationals (a rounding of the exact quotient: the fp32 quotient can only move a
+    result that lies within 2^-20 of a half-integer, and such cases are skipped)."""
+    w = workloads.weights(12, 512, seed=21).numpy()
+    w[3, :128] += 0.5  # one group entirely positive: negative zero point
+    G = 128
+    qw_rows, s, z = oracle.w4a16zp_quantize(w, group=G)
+    codes = _zp_codes(qw_rows)
+
+    def rha(t):  # half away from zero
+        a = math.floor(abs(t) + Fraction(1, 2))
+        return a if t >= 0 else -a
+
+    for n in range(w.shape[0]):
+        for g in range(w.shape[1] // G):
+            grp = w[n, g * G:(g + 1) * G]
+            lo, hi = Fraction(float(grp.min())), Fraction(float(grp.max()))
+            sf = Fraction(_fp16(s[n, g]))
+            assert abs(sf - (hi - lo) / 15) <= (hi - lo) / 15 / 2**10 + Fraction(1, 2**30)
+            zt = -lo / sf
+            if abs(abs(zt - math.floor(zt)) - Fraction(1, 2)) > Fraction(1, 2**20):
+                assert Fraction(_fp16(z[n, g])) == rha(zt), (n, g)
+            zf = Fraction(_fp16(z[n, g]))
+            for i, wv in enumerate(grp):
+                t = Fraction(float(wv)) / sf
+                if abs(abs(t - math.floor(t)) - Fraction(1, 2)) <= Fraction(1, 2**20):
+                    continue
+                want = min(15, max(0, rha(t) + zf))
+                assert codes[n, g * G + i] == want, (n, g, i, float(t))
+
+
+def pin_zp_one_hot_activation():
+    """x = e_k gives y[n] = (q - z) s exactly: pins the [N, K/8] word layout, nibble
+    order, the [N, K/G] scale/zero layout and the sign of the zero point."""
+    N, K, G = 24, 384, 128
+    w = workloads.weights(N, K, seed=5).numpy()
+    qw_rows, s, z = oracle.w4a16zp_quantize(w, group=G)
+    w_hat = _zp_w_hat(qw_rows, s, z, G)
+    one = _torch_bits(torch.tensor([1.0], dtype=torch.bfloat16))[0]
+    for k in (0, 1, 7, 8, 127, 128, 255, 383):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = one
+        y, a = oracle.w4a16zp_matmul(x, qw_rows, s, z, group=G)
+        np.testing.assert_array_equal(y[0], w_hat[:, k])
+        np.testing.assert_array_equal(a[0], np.abs(w_hat[:, k]))
+
+
+def pin_zp_matmul_exact_small():
+    """Small cases: the fp64 sum equals the exact rational sum over (q - z) s to fp64
+    rounding, and the sampled-column entry point matches the full one."""
+    rng = np.random.default_rng(23)
+    for (M, N, K, G) in ((1, 8, 64, 8), (3, 9, 64, 32), (2, 16, 128, 64)):
+        w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        qw_rows, s, z = oracle.w4a16zp_quantize(w, group=G)
+        q = _zp_codes(qw_rows)
+        x = workloads.bits16(workloads.activations_bf16(M, K, seed=N + K))
+        y, a = oracle.w4a16zp_matmul(x, qw_rows, s, z, group=G)
+        for r in range(M):
+            for n in range(N):
+                exact = sum(Fraction(_bf16(x[r, k])) *
+                            (int(q[n, k]) - Fraction(_fp16(z[n, k // G]))) *
+                            Fraction(_fp16(s[n, k // G])) for k in range(K))
+                assert abs(Fraction(y[r, n]) - exact) <= Fraction(a[r, n]) / 2**45, (M, N, r, n)
+        cols = np.array([N - 1, 0, 3], dtype=np.int32)
+        y2, a2 = oracle.w4a16zp_matmul(x, qw_rows, s, z, group=G, cols=cols)
+        np.testing.assert_array_equal(y2, y[:, cols])
+        np.testing.assert_array_equal(a2, a[:, cols])
+
+
+def pin_zp_matches_library_matmul_and_error_band():
+    """torch.matmul (fp64) on independently rebuilt weights agrees to ~1e-12, and the
+    zero-point format's error on N(0, 0.02^2) weights is the same ~10 % band as the
+    minimum form (16 levels over the group's range); the kernel layout is a transpose."""
+    N, K, G, M = 128, 1024, 128, 4
+    w = workloads.weights(N, K, seed=8).numpy()
+    qw_rows, s, z = oracle.w4a16zp_quantize(w, group=G)
+    w_hat = _zp_w_hat(qw_rows, s, z, G)
+    np.testing.assert_array_equal(oracle.w4a16zp_dequant(qw_rows, s, z, group=G), w_hat)
+    x = workloads.bits16(workloads.activations_bf16(M, K, seed=8))
+    y, a = oracle.w4a16zp_matmul(x, qw_rows, s, z, group=G)
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double()
+    ref = (xv @ torch.from_numpy(w_hat).T).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    y_o = xv.numpy() @ w.astype(np.float64).T
+    rel = np.linalg.norm(y - y_o) / np.linalg.norm(y_o)
+    assert 0.06 < rel < 0.14, rel
+    qk, sk, zk = oracle.w4a16zp_kernel_layout(qw_rows, s, z)
+    assert qk.shape == (K // 8, N) and sk.shape == (K // G, N) and zk.shape == (K // G, N)
+    assert int(qk[5, 7]) & 0xFFFFFFFF == int(qw_rows[7, 5]) and sk[2, 9] == s[9, 2]
+    assert zk[3, 1] == z[1, 3]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

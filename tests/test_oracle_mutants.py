@@ -46,6 +46,27 @@ MUTANTS = [
      "double qv = (double)(q4_code(codes, K, n, k) - 7);", None),
     ("q4_scale_divides_by_7", "volatile float s32 = amax / 8.0f;", "volatile float s32 = amax / 7.0f;", None),
     ("q4_zero_block_code_0", "if (s == 0.0f) {\n          q[i] = 8;", "if (s == 0.0f) {\n          q[i] = 0;", None),
+    ("zp_round_half_even", "return (float)copysign(a, (double)t);",
+     "return (float)round_half_even((double)t);", None),
+    ("zp_zero_added_before_rounding", "double r = (double)round_half_away(t) + (double)z;",
+     "double r = (double)round_half_away(t + z);", None),
+    ("zp_zero_sign_flipped", "volatile float neg_lo = -lo;", "volatile float neg_lo = lo;", None),
+    ("zp_dequant_adds_zero", "(double)unpack_code_rows(qw_rows, K, n, k) - z) * s;",
+     "(double)unpack_code_rows(qw_rows, K, n, k) + z) * s;", None),
+    ("zp_zero_scale_kept", "s_h = oracle_fp16_rne(1.0f);", "s_h = s_h;", None),
+    ("zp_scale_in_bf16", "uint16_t s_h = oracle_fp16_rne(s32);",
+     "uint16_t s_h = oracle_fp16_rne(oracle_bf16_to_float(oracle_bf16_rne(s32)));", None),
+    ("zp_matmul_scale_layout_transposed",
+     "double s = (double)oracle_fp16_to_float(scales[(size_t)n * groups + k / G]);\n"
+     "        double z = (double)oracle_fp16_to_float(zeros[(size_t)n * groups + k / G]);\n"
+     "        double w_hat = ((double)unpack_code_rows(qw_rows, K, n, k) - z) * s;\n"
+     "        double xv",
+     "double s = (double)oracle_fp16_to_float(scales[(size_t)(k / G) * N + n]);\n"
+     "        double z = (double)oracle_fp16_to_float(zeros[(size_t)(k / G) * N + n]);\n"
+     "        double w_hat = ((double)unpack_code_rows(qw_rows, K, n, k) - z) * s;\n"
+     "        double xv", None),
+    ("zp_nibble_order_reversed", "(uint32_t)q << (4 * (k % 8));", "(uint32_t)q << (4 * (7 - k % 8));",
+     None),
 ]
 
 
