@@ -10,8 +10,9 @@ around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than t
 
 The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
 the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
-quantize and GEMV (16384 x 16384), and the 196-matmul Qwen2.5-1.5B-shaped decode stack in
-one CUDA graph; each with its roofline fraction.
+quantize and GEMV (16384 x 16384), the zero-point format (quantize, layout move, matmul at
+M = 1, 16, 4096), and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
+each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
   python bench.py --case gemv_m1 --launches 6     # a few untimed launches, for ncu
@@ -427,6 +428,44 @@ def rows_ours(peaks, device, stream):
         "predicted_bf16_ridge_M": round(peaks["bf16_tflops"] * 1e12 * 2 / (2 * peaks["hbm_gbs"] * 1e9), 1),
         "measured_breakeven_vs_bf16_M": even[0] if even else None,
         "pages": "~28 (4-bit) and ~100 (BF16) at a ridge of 102 FLOP/B; break-even at 128 measured"}
+
+    # zero-point format on the up-projection: quantize, move to the matmul's layout, and the
+    # matmul at M = 1, 16 and 4096 (same kernels as the minimum form, FP16 scale and zero)
+    N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+    w = workloads.weights(N, K, seed=0).to(device)
+    qr, zs, zz = w4.w4a16zp_quantize(w)
+    us = graph_time_us(lambda i: w4.w4a16zp_quantize(w, qw_rows=qr, scales=zs, zeros=zz), 4, 5,
+                       stream)
+    b = N * K * 4 + N * K // 2 + 4 * N * (K // 128)
+    zp = {"shape": [N, K],
+          "quantize": {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                       "frac_hbm": round(b / us / 1e3 / hbm, 3)}}
+    del w
+    qk, sk, zk = w4.w4a16zp_prepare(qr, zs, zz)
+    us = graph_time_us(lambda i: w4.w4a16zp_prepare(qr, zs, zz, qw=qk, scales_t=sk, zeros_t=zk),
+                       4, 5, stream)
+    b = 2 * (N * K // 2 + 4 * N * (K // 128))
+    zp["prepare"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                     "frac_hbm": round(b / us / 1e3 / hbm, 3)}
+    del qr, zs, zz
+    cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(ROTATE)]
+    mm = []
+    for M in (1, 16, 4096):
+        x = workloads.activations_bf16(M, K, seed=M).to(device)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+        ws = workspace_for(M, N, K, device)
+        big = M >= 1024
+        us = graph_time_us(lambda i: w4.w4a16zp_matmul(x, *cps[i % ROTATE], y=y, workspace=ws),
+                           ROTATE if big else 4 * ROTATE, 2 if big else 10, stream)
+        bts, fl = w4a16_bytes(M, N, K), 2 * M * N * K
+        roof = roofline_us(bts, fl, peaks)
+        mm.append({"M": M, "us": round(us, 2), "TFLOPS": round(fl / us / 1e6, 1),
+                   "GBps": round(bts / us / 1e3, 1), "roofline_us": round(roof, 2),
+                   "frac": round(roof / us, 3)})
+        del x, y
+    zp["matmul"] = mm
+    rows["zero_point"] = zp
+    del cps, qk, sk, zk
 
     # Q4 block-32, 16384 x 16384
     qc_cfg = workloads.Q4_SQUARE

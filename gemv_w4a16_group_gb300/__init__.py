@@ -14,6 +14,10 @@ Formats ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2;
     y bfloat16 [M, N]; w_hat = q * scale + min.
   * Q4 block-32: codes uint8 [N, K/2] (low nibble = even k); scales float16 [N, K/32];
     x float16 [K]; y float16 [N]; w_hat = (q - 8) * scale.
+  * W4A16 with a zero point ("Quantization and GEMV", "The quantization formulas"):
+    quantized into words int32 [N, K/8] and float16 scales / zeros [N, K/128] (the page's
+    layout), moved by ``w4a16zp_prepare`` into qw [K/8, N] and scales / zeros [K/128, N]
+    for ``w4a16zp_matmul``; w_hat = (q - zero) * scale.
 """
 from __future__ import annotations
 
@@ -28,7 +32,8 @@ __all__ = [
     "W4A16Error", "library_path", "w4a16_quantize", "w4a16_pack", "w4a16_matmul",
     "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
-    "testing_set_q4_variant", "testing_set_skinny_range",
+    "testing_set_q4_variant", "testing_set_skinny_range", "w4a16zp_quantize",
+    "w4a16zp_prepare", "w4a16zp_matmul",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -62,6 +67,9 @@ def _load():
         "q4b32_gemv": [P, P, P, P, I, I, P],
         "w4a16_device_status": [P],
         "w4a16_selftest_bounded_wait": [U32, P],
+        "w4a16zp_quantize": [P, I, I, I, P, P, P, P],
+        "w4a16zp_prepare": [P, P, P, I, I, I, P, P, P, P],
+        "w4a16zp_matmul": [P, P, P, P, P, I, I, I, I, P, S, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -177,6 +185,68 @@ def w4a16_matmul_noalloc(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor
         _dev(scales, "scales", torch.bfloat16, (K // group, N)),
         _dev(mins, "mins", torch.bfloat16, (K // group, N)),
         _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, _stream(stream)))
+    return y
+
+
+def w4a16zp_quantize(w: torch.Tensor, group: int = 128, qw_rows=None, scales=None, zeros=None,
+                     stream=None):
+    """fp32 [N, K] -> (words int32 [N, K/8], scales fp16 [N, K/group], zeros fp16
+    [N, K/group]), the zero-point format in the layout its page stores."""
+    N, K = w.shape
+    if qw_rows is None:
+        qw_rows = torch.empty((N, K // 8), dtype=torch.int32, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // group), dtype=torch.float16, device=w.device)
+    if zeros is None:
+        zeros = torch.empty((N, K // group), dtype=torch.float16, device=w.device)
+    _check("w4a16zp_quantize", _lib.w4a16zp_quantize(
+        _dev(w, "w", torch.float32), N, K, group,
+        _dev(qw_rows, "qw_rows", torch.int32, (N, K // 8)),
+        _dev(scales, "scales", torch.float16, (N, K // group)),
+        _dev(zeros, "zeros", torch.float16, (N, K // group)), _stream(stream)))
+    return qw_rows, scales, zeros
+
+
+def w4a16zp_prepare(qw_rows: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                    group: int = 128, qw=None, scales_t=None, zeros_t=None, stream=None):
+    """Words [N, K/8] and scales / zeros [N, K/group] -> the matmul's qw int32 [K/8, N] and
+    scales / zeros fp16 [K/group, N]."""
+    N, K = qw_rows.shape[0], qw_rows.shape[1] * 8
+    dev = qw_rows.device
+    if qw is None:
+        qw = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    if scales_t is None:
+        scales_t = torch.empty((K // group, N), dtype=torch.float16, device=dev)
+    if zeros_t is None:
+        zeros_t = torch.empty((K // group, N), dtype=torch.float16, device=dev)
+    _check("w4a16zp_prepare", _lib.w4a16zp_prepare(
+        _dev(qw_rows, "qw_rows", torch.int32, (N, K // 8)),
+        _dev(scales, "scales", torch.float16, (N, K // group)),
+        _dev(zeros, "zeros", torch.float16, (N, K // group)), N, K, group,
+        _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales_t, "scales_t", torch.float16, (K // group, N)),
+        _dev(zeros_t, "zeros_t", torch.float16, (K // group, N)), _stream(stream)))
+    return qw, scales_t, zeros_t
+
+
+def w4a16zp_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                   group: int = 128, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] (bf16) = x [M, K] (bf16) . w_hat^T, w_hat = (q - zero) * scale; qw, scales
+    and zeros as ``w4a16zp_prepare`` returns them. Workspace as for ``w4a16_matmul``."""
+    M, K = x.shape
+    N = qw.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("w4a16zp_matmul", _lib.w4a16zp_matmul(
+        _dev(x, "x", torch.bfloat16), _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.float16, (K // group, N)),
+        _dev(zeros, "zeros", torch.float16, (K // group, N)),
+        _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
     return y
 
 

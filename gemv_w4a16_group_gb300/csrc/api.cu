@@ -143,9 +143,15 @@ size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group) {
   return bytes;
 }
 
-w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
-                          const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
-                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Both weight formats: zp selects FP16 scales and zero points over BF16 scales and minimums.
+w4a16_status matmul_impl(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                         const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
+                         void* workspace, size_t workspace_bytes, w4a16_stream_t stream,
+                         bool zp) {
   if (!x || !qw || !scales || !mins || !y) return W4A16_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
   if (group != 128 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
@@ -174,7 +180,7 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
     if (!sk_room) return W4A16_ERR_WORKSPACE;
     return from_cuda(w4k::launch_w4a16_skinny(x, q, scales, mins, y, M, N, K,
                                               static_cast<char*>(workspace) + sk_reserve, sk,
-                                              status, g_wait_limit_ns, s));
+                                              status, g_wait_limit_ns, s, zp));
   }
   if (kernel == 1) {
     // The GEMV takes up to gemv_max_rows() rows per launch; larger M (forced) loops.
@@ -194,14 +200,14 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
       }
       cudaError_t e = w4k::launch_w4a16_gemv(x + static_cast<size_t>(m0) * K, q, scales, mins,
                                              y + static_cast<size_t>(m0) * N, mb, N, K, split,
-                                             status, g_wait_limit_ns, s);
+                                             status, g_wait_limit_ns, s, zp);
       if (e != cudaSuccess) return W4A16_ERR_CUDA;
     }
     return W4A16_OK;
   }
   const int bm = w4k::tc_block_m(M);
   w4k::TcMaps maps;
-  cudaError_t e = w4k::make_tc_maps(x, q, scales, mins, M, N, K, bm, &maps);
+  cudaError_t e = w4k::make_tc_maps(x, q, scales, mins, M, N, K, bm, &maps, zp);
   if (e != cudaSuccess) return W4A16_ERR_CUDA;
   // Split K across CTAs when the caller's workspace holds the plan's partial tiles.
   size_t need = 0;
@@ -214,7 +220,53 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
   } else {
     split = w4k::TcSplit();
   }
-  return from_cuda(w4k::launch_w4a16_tc(maps, y, M, N, K, bm, status, g_wait_limit_ns, split, s));
+  return from_cuda(
+      w4k::launch_w4a16_tc(maps, y, M, N, K, bm, status, g_wait_limit_ns, split, s, zp));
+}
+
+}  // namespace
+
+extern "C" {
+
+w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                          const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
+                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  return matmul_impl(x, qw, scales, mins, y, M, N, K, group, workspace, workspace_bytes, stream,
+                     false);
+}
+
+w4a16_status w4a16zp_quantize(const float* w, int N, int K, int group, uint32_t* qw_rows,
+                              uint16_t* scales, uint16_t* zeros, w4a16_stream_t stream) {
+  if (!w || !qw_rows || !scales || !zeros) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || group <= 0 || K % group != 0 || group % 8 != 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (group != 128) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(qw_rows) || !aligned16(scales) || !aligned16(zeros))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w4a16zp_quantize(w, N, K, qw_rows, scales, zeros,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16zp_prepare(const uint32_t* qw_rows, const uint16_t* scales,
+                             const uint16_t* zeros, int N, int K, int group, int32_t* qw,
+                             uint16_t* scales_t, uint16_t* zeros_t, w4a16_stream_t stream) {
+  if (!qw_rows || !scales || !zeros || !qw || !scales_t || !zeros_t) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || group <= 0 || K % group != 0 || group % 8 != 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (group != 128) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(qw_rows) || !aligned16(scales) || !aligned16(zeros) || !aligned16(qw) ||
+      !aligned16(scales_t) || !aligned16(zeros_t))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w4a16zp_prepare(qw_rows, scales, zeros, N, K,
+                                               reinterpret_cast<uint32_t*>(qw), scales_t,
+                                               zeros_t, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16zp_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                            const uint16_t* zeros, uint16_t* y, int M, int N, int K, int group,
+                            void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  return matmul_impl(x, qw, scales, zeros, y, M, N, K, group, workspace, workspace_bytes, stream,
+                     true);
 }
 
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,

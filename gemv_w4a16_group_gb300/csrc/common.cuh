@@ -254,8 +254,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 // The fp32 pattern 0x43000000 | (v << 16) is 128 + v for 0 <= v < 16, and
 // 0x45000000 | (v << 12) is 2048 + v: a 4-bit code placed in the mantissa under a
 // fixed exponent is an exact float with a known offset ("Low-Precision Kernels ...",
-// "Where the time goes at M = 1": OR the 4 bits into the mantissa of a number with a
-// fixed exponent; "Quantization and GEMV", "What production kernels do").
+// "Where the time goes at M = 1": the code goes into the low mantissa bits of a float
+// whose exponent is fixed; "Quantization and GEMV", "What production kernels do").
 //
 // codes_to_f32_offset: word w holds codes q0..q7 (q_j in bits 4j..4j+3). Returns
 // f[j] = B_j + q_j with B_j = 2048 for even j and 128 for odd j, using four shifts and
@@ -348,6 +348,25 @@ __device__ __forceinline__ void codes_to_bf16x2_consecutive(uint32_t w, uint32_t
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+// Scale s and offset of one group in fp32, so that w_hat = q s + offset. Minimum form: BF16
+// s and minimum. Zero-point form ("Quantization and GEMV", "The quantization formulas":
+// w_hat = (q - z) s): FP16 s and z, offset -s z, exact in fp32 (two 11-bit significands).
+template <bool ZP>
+__device__ __forceinline__ void group_scale_offset(uint32_t sbits, uint32_t obits, float& sc,
+                                                   float& off) {
+  if constexpr (ZP) {
+    sc = f16_bits_to_f32(sbits);
+    off = -sc * f16_bits_to_f32(obits);
+  } else {
+    sc = bf16_bits_to_f32(sbits);
+    off = bf16_bits_to_f32(obits);
+  }
 }
 
 }  // namespace w4k

@@ -73,7 +73,8 @@ struct Smem {
   static_assert(x_bytes % 1024 == 0, "x stage must keep 1024-byte alignment");
 };
 
-template <int BM>
+// ZP: FP16 scales and zero points (w_hat = (q - z) s) instead of BF16 scales and minimums.
+template <int BM, bool ZP>
 __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
     w4a16_tc_kernel(const __grid_constant__ TcMaps maps, uint16_t* __restrict__ y, int M, int N,
                     int K, uint32_t* __restrict__ status, uint64_t limit_ns,
@@ -209,6 +210,14 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
         break;
       }
       const uint32_t sb = ssc[s * kBN + row], mb = smn[s * kBN + row];
+      // Zero point: w_hat = (128 + q) s - (128 + z) s in one fp32 FMA per weight (exact for
+      // |z| < 8064, where (128 + z) s has at most 24 significant bits), then one rounding to
+      // BF16, the same single rounding the minimum form's BF16 FMA makes.
+      float zs = 0.f, zc = 0.f;
+      if constexpr (ZP) {
+        zs = f16_bits_to_f32(sb);
+        zc = -zs * (128.0f + f16_bits_to_f32(mb));
+      }
       const uint32_t s2u = sb | (sb << 16), m2u = mb | (mb << 16);
       const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
       const __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&m2u);
@@ -223,9 +232,16 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
         codes_to_bf16x2_consecutive(w, p);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p[i]), off);
-          const __nv_bfloat162 wv = __hfma2(q2, s2, m2);  // q*s + min, one rounding
-          out[4 * cc + i] = *reinterpret_cast<const uint32_t*>(&wv);
+          if constexpr (ZP) {
+            const float lo = __uint_as_float(p[i] << 16), hi = __uint_as_float(p[i] & 0xFFFF0000u);
+            const __nv_bfloat162 wv = __floats2bfloat162_rn(fmaf(lo, zs, zc), fmaf(hi, zs, zc));
+            out[4 * cc + i] = *reinterpret_cast<const uint32_t*>(&wv);
+          } else {
+            const __nv_bfloat162 q2 =
+                __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p[i]), off);
+            const __nv_bfloat162 wv = __hfma2(q2, s2, m2);  // q*s + min, one rounding
+            out[4 * cc + i] = *reinterpret_cast<const uint32_t*>(&wv);
+          }
         }
       }
       if constexpr (kParts == 1)
@@ -361,11 +377,11 @@ cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base
   return encode_tensor_map(map, dt, base, inner, outer, row_bytes, box_inner, box_outer, swz);
 }
 
-template <int BM>
+template <int BM, bool ZP>
 cudaError_t launch_bm(const TcMaps& maps, uint16_t* y, int M, int N, int K, uint32_t* status,
                       uint64_t limit_ns, const TcSplit& split, cudaStream_t stream) {
   using L = Smem<BM>;
-  auto kern = w4a16_tc_kernel<BM>;
+  auto kern = w4a16_tc_kernel<BM, ZP>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                        static_cast<int>(L::alloc));
   if (e != cudaSuccess) return e;
@@ -393,7 +409,10 @@ int tc_block_m(int M) {
 }
 
 cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
-                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps) {
+                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps,
+                         bool zero_point) {
+  const CUtensorMapDataType st =
+      zero_point ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cudaError_t e;
   e = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kBK,
@@ -403,26 +422,30 @@ cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* 
                 static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, kBN, kBK / 8,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  e = encode_2d(&maps->scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales, static_cast<uint64_t>(N),
+  e = encode_2d(&maps->scales, st, scales, static_cast<uint64_t>(N),
                 static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kBN, 1,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  return encode_2d(&maps->mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins, static_cast<uint64_t>(N),
+  return encode_2d(&maps->mins, st, mins, static_cast<uint64_t>(N),
                    static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, kBN, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
                             uint32_t* status, uint64_t limit_ns, const TcSplit& split,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool zero_point) {
+#define W4K_TC_BM(BM)                                                                        \
+  return zero_point ? launch_bm<BM, true>(maps, y, M, N, K, status, limit_ns, split, stream) \
+                    : launch_bm<BM, false>(maps, y, M, N, K, status, limit_ns, split, stream);
   switch (bm) {
-    case 16: return launch_bm<16>(maps, y, M, N, K, status, limit_ns, split, stream);
-    case 32: return launch_bm<32>(maps, y, M, N, K, status, limit_ns, split, stream);
-    case 64: return launch_bm<64>(maps, y, M, N, K, status, limit_ns, split, stream);
-    case 128: return launch_bm<128>(maps, y, M, N, K, status, limit_ns, split, stream);
-    case 256: return launch_bm<256>(maps, y, M, N, K, status, limit_ns, split, stream);
+    case 16: W4K_TC_BM(16)
+    case 32: W4K_TC_BM(32)
+    case 64: W4K_TC_BM(64)
+    case 128: W4K_TC_BM(128)
+    case 256: W4K_TC_BM(256)
     default: return cudaErrorInvalidValue;
   }
+#undef W4K_TC_BM
 }
 
 int tc_ctas_per_sm(int bm) {

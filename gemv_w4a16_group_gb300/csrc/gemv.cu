@@ -116,11 +116,13 @@ __device__ __forceinline__ void consumer_bar() {
 
 struct GemvMaps {
   CUtensorMap qw;      // int32 [K/8, N], box {32, ROWS}, 128-byte swizzle
-  CUtensorMap scales;  // bf16 [K/128, N], box {W, GPC}
-  CUtensorMap mins;    // bf16 [K/128, N], box {W, GPC}
+  CUtensorMap scales;  // bf16 (fp16 with a zero point) [K/128, N], box {W, GPC}
+  CUtensorMap mins;    // bf16 minimums (fp16 zero points) [K/128, N], box {W, GPC}
 };
 
-template <int MR, int QW, int CW>
+// ZP: the zero-point format (FP16 scale and zero point, w_hat = (q - z) s); otherwise the
+// minimum format (BF16 scale and minimum). Only the fold's reading of the two differs.
+template <int MR, int QW, int CW, bool ZP>
 __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBlocks)
     gemv_w4a16_kernel(const __grid_constant__ GemvMaps maps, const uint16_t* __restrict__ x,
                       uint16_t* __restrict__ y, int M, int N, int K, int stages, int splits,
@@ -411,8 +413,9 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
           const int jj = jj0 + i;
-          const float sc = bf16_bits_to_f32(lds_u16(sbuf + s_off + 2 * jj));
-          const float mn = bf16_bits_to_f32(lds_u16(sbuf + s_off + S::row_stride + 2 * jj));
+          float sc, mn;
+          group_scale_offset<ZP>(lds_u16(sbuf + s_off + 2 * jj),
+                                 lds_u16(sbuf + s_off + S::row_stride + 2 * jj), sc, mn);
 #pragma unroll
           for (int bb = 0; bb < NBB; ++bb) {
             float dv;
@@ -558,7 +561,7 @@ int stages_of(int MR, int K) {
   return two >= 3 ? two : stages_for<QW, CW>(MR, K, kSmemOneCta);
 }
 
-template <int MR, int QW, int CW>
+template <int MR, int QW, int CW, bool ZP>
 cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N,
                          int K, const GemvSplit& split, const GemvPlan& plan, uint32_t* status,
                          uint64_t limit_ns, int sms, cudaStream_t stream) {
@@ -568,7 +571,7 @@ cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, i
   const int G = K >> 7;
   const int rows_pad = ((G + S::GPC - 1) / S::GPC) * S::ROWS;
   const GemvLayout L(S::stage_bytes, rows_pad, MR, G, stages, CW);
-  auto kern = gemv_w4a16_kernel<MR, QW, CW>;
+  auto kern = gemv_w4a16_kernel<MR, QW, CW, ZP>;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern),
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
@@ -579,13 +582,13 @@ cudaError_t launch_shape(const GemvMaps& maps, const uint16_t* x, uint16_t* y, i
                          split.counter, status, limit_ns);
 }
 
-template <int MR>
+template <int MR, bool ZP>
 cudaError_t launch_mr(const GemvMaps& maps, const uint16_t* x, uint16_t* y, int M, int N, int K,
                       const GemvSplit& split, const GemvPlan& plan, uint32_t* status,
                       uint64_t limit_ns, int sms, cudaStream_t stream) {
 #define W4K_GEMV_CASE(QW, CW)                                                                  \
   if (plan.qw == QW && plan.cw == CW)                                                         \
-    return launch_shape<MR, QW, CW>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, \
+    return launch_shape<MR, QW, CW, ZP>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, \
                                     stream);
   W4K_GEMV_CASE(4, 24)
   W4K_GEMV_CASE(3, 24)
@@ -641,32 +644,41 @@ GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed) {
 cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                               const uint16_t* mins, uint16_t* y, int M, int N, int K,
                               const GemvSplit& split, uint32_t* status, uint64_t limit_ns,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool zero_point) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const GemvPlan plan = make_plan(N, sms);
   if (plan.col_q > 0 && split.splits != 1) return cudaErrorInvalidValue;
   const uint32_t w = 32u * plan.qw, gpc = static_cast<uint32_t>(plan.cw / plan.qw);
+  const CUtensorMapDataType st =
+      zero_point ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   GemvMaps maps;
   cudaError_t e;
   e = encode_tensor_map(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
                         static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, 32u, 16u * gpc,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales,
-                        static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
-                        static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
+  e = encode_tensor_map(&maps.scales, st, scales, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  e = encode_tensor_map(&maps.mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins,
-                        static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
-                        static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
+  e = encode_tensor_map(&maps.mins, st, mins, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N) * 2, w, gpc,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
+#define W4K_GEMV_MR(MR)                                                                      \
+  return zero_point                                                                          \
+             ? launch_mr<MR, true>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms,  \
+                                   stream)                                                   \
+             : launch_mr<MR, false>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, \
+                                    stream);
   switch (mr_of(M)) {
-    case 1: return launch_mr<1>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
-    case 2: return launch_mr<2>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
-    case 4: return launch_mr<4>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
-    default: return launch_mr<8>(maps, x, y, M, N, K, split, plan, status, limit_ns, sms, stream);
+    case 1: W4K_GEMV_MR(1)
+    case 2: W4K_GEMV_MR(2)
+    case 4: W4K_GEMV_MR(4)
+    default: W4K_GEMV_MR(8)
   }
+#undef W4K_GEMV_MR
 }
 
 }  // namespace w4k

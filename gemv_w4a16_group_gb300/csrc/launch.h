@@ -32,12 +32,21 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
                               cudaStream_t stream);
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                                   cudaStream_t stream);
+// Zero-point format: quantize into [N, K/8] words and [N, K/128] FP16 scales and zeros, and
+// transpose those into the matmul's [K/8, N] and [K/128, N].
+cudaError_t launch_w4a16zp_quantize(const float* w, int N, int K, uint32_t* qw_rows,
+                                    uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
+cudaError_t launch_w4a16zp_prepare(const uint32_t* qw_rows, const uint16_t* scales,
+                                   const uint16_t* zeros, int N, int K, uint32_t* qw,
+                                   uint16_t* scales_t, uint16_t* zeros_t, cudaStream_t stream);
 
-// GEMV / skinny kernel for M <= 8 (weights staged by TMA, codes widened into tensor memory,
-// inner products on tcgen05.mma, per-group fold in fp32). With a split plan (splits > 1) the K range of each 128-column slab
-// is divided over thread blocks: fp32 partials [splits][mr][N] and one arrival counter per
-// slab (zero before the launch; the kernel leaves it zero). gemv_supports() tells whether
-// M and K fit its limits.
+// GEMV for M <= 8 (weights staged by TMA, codes widened to FP16 pairs in registers, inner
+// products on mma.sync, per-group fold in fp32). With a split plan (splits > 1) the K range
+// of each slab is divided over thread blocks: fp32 partials [splits][mr][N] and one arrival
+// counter per slab (zero before the launch; the kernel leaves it zero). gemv_supports()
+// tells whether M and K fit its limits. zero_point: `scales` and `mins` hold FP16 scales
+// and zero points (w_hat = (q - z) s) instead of BF16 scales and minimums; the same holds
+// for the skinny and tensor-core launchers below.
 struct GemvSplit {
   int splits = 1;
   float* partial = nullptr;
@@ -50,14 +59,14 @@ GemvSplit gemv_split_plan(int M, int N, int K, size_t* bytes_needed);
 cudaError_t launch_w4a16_gemv(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                               const uint16_t* mins, uint16_t* y, int M, int N, int K,
                               const GemvSplit& split, uint32_t* status, uint64_t wait_limit_ns,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool zero_point = false);
 
 // TMA + tcgen05 kernel: y^T tile = W_hat tile (tensor memory) x x^T tile (shared memory).
 struct TcMaps {
   CUtensorMap x;       // bf16 [M, K], box {64, BM}, 128-byte swizzle
   CUtensorMap qw;      // int32 [K/8, N], box {128, 8}
-  CUtensorMap scales;  // bf16 [K/128, N], box {128, 1}
-  CUtensorMap mins;    // bf16 [K/128, N], box {128, 1}
+  CUtensorMap scales;  // bf16 (fp16 with a zero point) [K/128, N], box {128, 1}
+  CUtensorMap mins;    // bf16 minimums (fp16 zero points) [K/128, N], box {128, 1}
 };
 // Split-K over gridDim.z CTAs: fp32 partial tiles [splits][ceil(M/bm)*bm][N] and one
 // arrival counter per output tile (zero before the launch; the kernel leaves it zero).
@@ -74,10 +83,11 @@ TcSplit tc_split_plan(int M, int N, int K, size_t* bytes_needed);
 // Device address of the library's status word on the current device (nullptr on error).
 uint32_t* status_word();
 cudaError_t make_tc_maps(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
-                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps);
+                         const uint16_t* mins, int M, int N, int K, int bm, TcMaps* maps,
+                         bool zero_point = false);
 cudaError_t launch_w4a16_tc(const TcMaps& maps, uint16_t* y, int M, int N, int K, int bm,
                             uint32_t* status, uint64_t wait_limit_ns, const TcSplit& split,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool zero_point = false);
 
 // Skinny W4A16 matmul for 1 <= M <= kSkinnyMaxRows (one to four n8 tiles of batch rows on
 // mma.sync): a prep kernel converts x into the caller's workspace (FP16 fragments and
@@ -99,7 +109,8 @@ bool skinny_plan(int M, int N, int K, SkinnyPlan* plan);
 cudaError_t launch_w4a16_skinny(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                                 const uint16_t* mins, uint16_t* y, int M, int N, int K,
                                 void* workspace, const SkinnyPlan& plan, uint32_t* status,
-                                uint64_t wait_limit_ns, cudaStream_t stream);
+                                uint64_t wait_limit_ns, cudaStream_t stream,
+                                bool zero_point = false);
 
 // Q4 block-32 GEMV.
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,

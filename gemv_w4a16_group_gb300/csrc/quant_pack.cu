@@ -1,12 +1,13 @@
 // Offline weight preparation on the GPU: group-128 asymmetric 4-bit quantization, packing
-// eight codes per int32 along K, and Q4 block-32 quantization.
+// eight codes per int32 along K, the zero-point variant and its move into the matmul's
+// layout, and Q4 block-32 quantization.
 //
 // W4A16 format ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2):
-// each group of 128 consecutive weights along K gets scale = (max - min) / 15 and a
-// minimum, both stored as BF16; each weight becomes q = round((w - min) / scale) in
-// 0..15; eight codes are packed into one 32-bit word along K, giving a K/8 x N matrix.
+// a group is 128 neighbouring weights along K with scale (max - min) / 15 and its
+// minimum, both kept in BF16; a weight's code is round((w - min) / scale), 0..15; words of
+// eight codes along K form a K/8 x N matrix.
 // Q4 format ("Why My 4-Bit CUDA Kernel Wasn't Faster"): 32 weights share one FP16
-// scale; 16 bytes of codes, low nibble = even weight, decode (q - 8) * s.
+// scale; the 32 codes fill 16 bytes, low nibble = even weight, decode (q - 8) * s.
 //
 // Every step is an IEEE fp32 operation rounded to nearest even (__fsub_rn, __fdiv_rn,
 // rintf, __float2bfloat16_rn, __float2half_rn), so the GPU result is bit-identical to a
@@ -83,6 +84,99 @@ w4a16_quantize_kernel(const float* __restrict__ w, int N, int K, uint8_t* __rest
       scales[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(s_b);
       mins[static_cast<size_t>(g) * N + n] = __bfloat16_as_ushort(m_b);
     }
+  }
+}
+
+// round(fl(d / s)) with ties away from zero (std::round, the rounding of the zero-point
+// format's host code), by the same argument as rint_quotient: for |t| < 32, t = fl(d rs) lies
+// within 3 * 33 * 2^-24 < 2^-17 of fl(d / s), so both round to the same integer unless t is
+// within 2^-17 of a half-integer; there, and for larger quotients, the quotient is exact.
+__device__ __forceinline__ float round_quotient_away(float d, float s, float rs) {
+  const float t = __fmul_rn(d, rs);
+  const float r = rintf(t);
+  if (fabsf(t) < 32.0f && fabsf(__fsub_rn(t, r)) <= 0.5f - 0x1p-17f) return r;
+  return roundf(__fdiv_rn(d, s));
+}
+
+// Zero-point W4A16 ("Quantization and GEMV", "The quantization formulas"): per group of 128
+// weights of a row, s = fp16((max - min) / 15) (1 when that is 0), z = fp16(round(-min / s)),
+// q = clamp(round(w / s) + z, 0, 15), in the layout the page stores: words [N, K/8] (first
+// weight in the lowest nibble), scales and zeros [N, K/128]. Same warp split as the
+// minimum-form quantizer; lanes 2i and 2i + 1 hold the 8 weights of word i of a group.
+__global__ void __launch_bounds__(256)
+w4a16zp_quantize_kernel(const float* __restrict__ w, int N, int K, uint32_t* __restrict__ qw_rows,
+                        uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros) {
+  const int groups = K >> 7;
+  const int per_row = (groups + kQGroupsPerWarp - 1) / kQGroupsPerWarp;
+  const long long wi = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wi >= static_cast<long long>(per_row) * N) return;
+  const int lane = threadIdx.x & 31;
+  const int n = static_cast<int>(wi / per_row);
+  const int g0 = static_cast<int>(wi - static_cast<long long>(n) * per_row) * kQGroupsPerWarp;
+  float4 v[kQGroupsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kQGroupsPerWarp; ++j) {
+    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g0 + j < groups)  // warp-uniform
+      v[j] = __ldcs(reinterpret_cast<const float4*>(
+          w + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + j) * 128 + lane * 4));
+  }
+#pragma unroll
+  for (int j = 0; j < kQGroupsPerWarp; ++j) {
+    const int g = g0 + j;
+    if (g >= groups) break;  // warp-uniform
+    float lo = fminf(fminf(v[j].x, v[j].y), fminf(v[j].z, v[j].w));
+    float hi = fmaxf(fmaxf(v[j].x, v[j].y), fmaxf(v[j].z, v[j].w));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    __half s_h = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+    if (__half2float(s_h) == 0.0f) s_h = __float2half_rn(1.0f);
+    const float s = __half2float(s_h);
+    const __half z_h = __float2half_rn(roundf(__fdiv_rn(-lo, s)));
+    const float z = __half2float(z_h);
+    const float rs = __frcp_rn(s);
+    auto code = [&](float x) -> uint32_t {
+      const float q = round_quotient_away(x, s, rs) + z;  // integers: exact
+      return static_cast<uint32_t>(fminf(fmaxf(q, 0.0f), 15.0f));
+    };
+    const uint32_t nib = code(v[j].x) | (code(v[j].y) << 4) | (code(v[j].z) << 8) |
+                         (code(v[j].w) << 12);
+    const uint32_t upper = __shfl_down_sync(0xffffffffu, nib, 1);
+    if ((lane & 1) == 0)
+      qw_rows[static_cast<size_t>(n) * (K >> 3) + static_cast<size_t>(g) * 16 + (lane >> 1)] =
+          nib | (upper << 16);
+    if (lane == 0) {
+      scales[static_cast<size_t>(n) * groups + g] = __half_as_ushort(s_h);
+      zeros[static_cast<size_t>(n) * groups + g] = __half_as_ushort(z_h);
+    }
+  }
+}
+
+// Transpose of a rows x cols matrix of T (4 or 2 bytes) into cols x rows, 64 x 64 tiles
+// through shared memory so that reads and writes are both coalesced. Prepares the
+// zero-point format's [N, K/8] words and [N, K/128] scales and zeros for the matmul,
+// which reads [K/8, N] and [K/128, N].
+template <typename T>
+__global__ void __launch_bounds__(256)
+transpose_kernel(const T* __restrict__ in, int rows, int cols, T* __restrict__ out) {
+  __shared__ T tile[64][65];
+  const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const int tid = threadIdx.x;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int rl = (tid >> 6) + 4 * i, cl = tid & 63;
+    if (r0 + rl < rows && c0 + cl < cols)
+      tile[rl][cl] = in[static_cast<size_t>(r0 + rl) * cols + c0 + cl];
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int cl = (tid >> 6) + 4 * i, rl = tid & 63;
+    if (r0 + rl < rows && c0 + cl < cols)
+      out[static_cast<size_t>(c0 + cl) * rows + r0 + rl] = tile[rl][cl];
   }
 }
 
@@ -179,6 +273,35 @@ cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   w4a16_pack_kernel<<<grid, 256, 0, stream>>>(codes, N, K, qw);
   return cudaGetLastError();
+}
+
+cudaError_t launch_w4a16zp_quantize(const float* w, int N, int K, uint32_t* qw_rows,
+                                    uint16_t* scales, uint16_t* zeros, cudaStream_t stream) {
+  const long long warps =
+      static_cast<long long>(((K >> 7) + kQGroupsPerWarp - 1) / kQGroupsPerWarp) * N;
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  w4a16zp_quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, qw_rows,
+                                                                              scales, zeros);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_transpose(const T* in, int rows, int cols, T* out, cudaStream_t stream) {
+  const dim3 grid((cols + 63) / 64, (rows + 63) / 64);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  transpose_kernel<T><<<grid, 256, 0, stream>>>(in, rows, cols, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w4a16zp_prepare(const uint32_t* qw_rows, const uint16_t* scales,
+                                   const uint16_t* zeros, int N, int K, uint32_t* qw,
+                                   uint16_t* scales_t, uint16_t* zeros_t, cudaStream_t stream) {
+  cudaError_t e = launch_transpose<uint32_t>(qw_rows, N, K >> 3, qw, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_transpose<uint16_t>(scales, N, K >> 7, scales_t, stream);
+  if (e != cudaSuccess) return e;
+  return launch_transpose<uint16_t>(zeros, N, K >> 7, zeros_t, stream);
 }
 
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,

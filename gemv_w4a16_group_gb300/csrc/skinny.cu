@@ -155,11 +155,12 @@ __global__ void __launch_bounds__(kSkPrepThreads)
 
 struct SkMaps {
   CUtensorMap qw;      // int32 [K/8, N], box {32, ROWS}, 128-byte swizzle
-  CUtensorMap scales;  // bf16 [K/128, N], box {W, GPC}
-  CUtensorMap mins;    // bf16 [K/128, N], box {W, GPC}
+  CUtensorMap scales;  // bf16 (fp16 with a zero point) [K/128, N], box {W, GPC}
+  CUtensorMap mins;    // bf16 minimums (fp16 zero points) [K/128, N], box {W, GPC}
 };
 
-template <int NT, int QW>
+// ZP: FP16 scales and zero points (w_hat = (q - z) s) instead of BF16 scales and minimums.
+template <int NT, int QW, bool ZP>
 __global__ void __launch_bounds__(kSkThreads, SkShape<NT, QW>::kMinBlocks)
     w4a16_skinny_kernel(const __grid_constant__ SkMaps maps, const uint4* __restrict__ xs,
                         const float4* __restrict__ cst, uint16_t* __restrict__ y, int M, int N,
@@ -317,10 +318,11 @@ __global__ void __launch_bounds__(kSkThreads, SkShape<NT, QW>::kMinBlocks)
       // Fold the group: y += (s U) D + (min X - s T). d[j][t][2h + r] is column 4gq + 2t + h,
       // batch row 8j + 2c + r.
       const uint2 sv = lds64(buf + s_off), mv = lds64(buf + s_off + S::row_stride);
-      const float sc[4] = {bf16_bits_to_f32(sv.x & 0xFFFFu), bf16_bits_to_f32(sv.x >> 16),
-                           bf16_bits_to_f32(sv.y & 0xFFFFu), bf16_bits_to_f32(sv.y >> 16)};
-      const float mn[4] = {bf16_bits_to_f32(mv.x & 0xFFFFu), bf16_bits_to_f32(mv.x >> 16),
-                           bf16_bits_to_f32(mv.y & 0xFFFFu), bf16_bits_to_f32(mv.y >> 16)};
+      float sc[4], mn[4];
+      group_scale_offset<ZP>(sv.x & 0xFFFFu, mv.x & 0xFFFFu, sc[0], mn[0]);
+      group_scale_offset<ZP>(sv.x >> 16, mv.x >> 16, sc[1], mn[1]);
+      group_scale_offset<ZP>(sv.y & 0xFFFFu, mv.y & 0xFFFFu, sc[2], mn[2]);
+      group_scale_offset<ZP>(sv.y >> 16, mv.y >> 16, sc[3], mn[3]);
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const float4 cr[2] = {lds128f(buf + c_lane + j * 128),
@@ -403,11 +405,11 @@ int sk_stages_of(int nt, int qw) {
   return 0;
 }
 
-template <int NT, int QW>
+template <int NT, int QW, bool ZP>
 cudaError_t sk_launch_shape(const SkMaps& maps, const uint4* xs, const float4* cst, uint16_t* y,
                             int M, int N, int K, const SkinnyPlan& plan, uint32_t* status,
                             uint64_t limit_ns, cudaStream_t stream) {
-  auto kern = w4a16_skinny_kernel<NT, QW>;
+  auto kern = w4a16_skinny_kernel<NT, QW, ZP>;
   const uint32_t smem = sk_smem_total<NT, QW>(plan.stages);
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -447,19 +449,21 @@ bool skinny_plan(int M, int N, int K, SkinnyPlan* plan) {
 cudaError_t launch_w4a16_skinny(const uint16_t* x, const uint32_t* qw, const uint16_t* scales,
                                 const uint16_t* mins, uint16_t* y, int M, int N, int K,
                                 void* workspace, const SkinnyPlan& plan, uint32_t* status,
-                                uint64_t wait_limit_ns, cudaStream_t stream) {
+                                uint64_t wait_limit_ns, cudaStream_t stream, bool zero_point) {
   const uint32_t w = 32u * plan.qw, gpc = static_cast<uint32_t>(kSkConsumerWarps / plan.qw);
+  const CUtensorMapDataType st =
+      zero_point ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   SkMaps maps;
   cudaError_t e;
   e = encode_tensor_map(&maps.qw, CU_TENSOR_MAP_DATA_TYPE_INT32, qw, static_cast<uint64_t>(N),
                         static_cast<uint64_t>(K / 8), static_cast<uint64_t>(N) * 4, 32u, 16u * gpc,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, scales,
+  e = encode_tensor_map(&maps.scales, st, scales,
                         static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
                         static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  e = encode_tensor_map(&maps.mins, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mins,
+  e = encode_tensor_map(&maps.mins, st, mins,
                         static_cast<uint64_t>(N), static_cast<uint64_t>(K / 128),
                         static_cast<uint64_t>(N) * 2, w, gpc, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
@@ -476,8 +480,10 @@ cudaError_t launch_w4a16_skinny(const uint16_t* x, const uint32_t* qw, const uin
   if (e != cudaSuccess) return e;
 #define W4K_SK_CASE(NT, QW)                                                                  \
   if (plan.nt == NT && plan.qw == QW)                                                        \
-    return sk_launch_shape<NT, QW>(maps, xs, cst, y, M, N, K, plan, status, wait_limit_ns,   \
-                                   stream);
+    return zero_point ? sk_launch_shape<NT, QW, true>(maps, xs, cst, y, M, N, K, plan, status, \
+                                                      wait_limit_ns, stream)                 \
+                      : sk_launch_shape<NT, QW, false>(maps, xs, cst, y, M, N, K, plan,      \
+                                                       status, wait_limit_ns, stream);
   W4K_SK_CASE(1, 2) W4K_SK_CASE(1, 3) W4K_SK_CASE(1, 4) W4K_SK_CASE(1, 6)
   W4K_SK_CASE(2, 2) W4K_SK_CASE(2, 3) W4K_SK_CASE(2, 4) W4K_SK_CASE(2, 6)
   W4K_SK_CASE(4, 2) W4K_SK_CASE(4, 3) W4K_SK_CASE(4, 4) W4K_SK_CASE(4, 6)

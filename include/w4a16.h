@@ -8,7 +8,9 @@
  *   are packed per int32 along K into a K/8 x N matrix ("Low-Precision Kernels: INT4,
  *   INT8 and FP8 Matmuls, Measured", Step 2). A second format is the 18-byte Q4 block
  *   of 32 codes plus an FP16 scale, w_hat = (q - 8) * s ("Why My 4-Bit CUDA Kernel
- *   Wasn't Faster", "Why fewer bytes should have helped").
+ *   Wasn't Faster", "Why fewer bytes should have helped"). A third is the zero-point
+ *   form w_hat = (q - z) * s with FP16 scale and zero point per group of 128
+ *   ("Quantization and GEMV", "The quantization formulas").
  *
  * Conventions shared by every entry point
  *   - Every array pointer is DEVICE memory owned by the caller. The library keeps no
@@ -54,9 +56,9 @@ const char* w4a16_status_string(w4a16_status status);
 
 /*
  * w4a16_quantize -- fp32 weights to 4-bit codes with a BF16 scale and minimum per
- * group ("Low-Precision Kernels ...", Step 2: "each group of 128 consecutive weights
- * along the input dimension K gets scale = (max - min) / 15, and each weight becomes
- * an integer q = round((w - min) / scale) from 0 to 15").
+ * group ("Low-Precision Kernels ...", Step 2: a group is 128 neighbouring weights
+ * along K, its scale is (max - min) / 15 and a weight's code is the integer
+ * round((w - min) / scale), 0..15).
  *   w      fp32 [N, K]        (one output feature per row, K contiguous)
  *   codes  uint8 [N, K]       (one code 0..15 per byte)
  *   scales bf16 [K/group, N]  s = bf16_rne(fp32(max - min) / 15)
@@ -70,8 +72,9 @@ w4a16_status w4a16_quantize(const float* w, int N, int K, int group, uint8_t* co
 
 /*
  * w4a16_pack -- eight codes per int32 along K ("Low-Precision Kernels ...", Step 2:
- * "an N x K weight becomes a K/8 x N packed matrix"; its listing: "row 8r + j =
- * nibble j of word r"; "Quantization and GEMV": first element in the low 4 bits).
+ * the N x K weights turn into a K/8 x N matrix of words, its listing takes k = 8r + j
+ * from nibble j of word r; "Quantization and GEMV": the lowest nibble is the first
+ * weight).
  *   codes uint8 [N, K] (values 0..15; higher bits are ignored)
  *   qw    int32 [K/8, N]: word (r, n) = sum_j codes[n, 8r + j] << 4j
  * Requires N > 0, K > 0, K % 8 == 0.
@@ -110,6 +113,49 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);
 
 /*
+ * Zero-point format ("Quantization and GEMV", "The quantization formulas" and "W4A16:
+ * dequantizing in registers"): w_hat = (q - z) * s with one FP16 scale s and one FP16
+ * zero point z per group of 128 weights along K (4.25 bits per weight).
+ *
+ * w4a16zp_quantize -- fp32 weights to codes, scales and zero points in the layout that
+ * page stores them in.
+ *   w       fp32 [N, K]
+ *   qw_rows uint32 [N, K/8]    word (n, r) holds k = 8r + j in bits 4j..4j+3
+ *   scales  fp16 [N, K/group]  s = fp16_rne(fp32(max - min) / 15); 1 if that is 0
+ *   zeros   fp16 [N, K/group]  z = fp16_rne(round(fp32(-min / s)))
+ * Per weight: q = clamp(round(fp32(w / s)) + z, 0, 15), round() half away from zero (the
+ * page's host code uses std::round), s and z as stored. A group whose zero point is beyond
+ * FP16's range (all weights far from zero next to their spread) is outside the format.
+ * Requires N > 0, K > 0, group == 128, K % group == 0.
+ */
+w4a16_status w4a16zp_quantize(const float* w, int N, int K, int group, uint32_t* qw_rows,
+                              uint16_t* scales, uint16_t* zeros, w4a16_stream_t stream);
+
+/*
+ * w4a16zp_prepare -- the same numbers in the matmul's layout (a transpose of each array):
+ *   qw_rows [N, K/8], scales [N, K/group], zeros [N, K/group]  (as above)
+ *   -> qw int32 [K/8, N], scales_t fp16 [K/group, N], zeros_t fp16 [K/group, N]
+ * Inputs and outputs must not overlap. Requires N > 0, K > 0, group == 128,
+ * K % group == 0.
+ */
+w4a16_status w4a16zp_prepare(const uint32_t* qw_rows, const uint16_t* scales,
+                             const uint16_t* zeros, int N, int K, int group, int32_t* qw,
+                             uint16_t* scales_t, uint16_t* zeros_t, w4a16_stream_t stream);
+
+/*
+ * w4a16zp_matmul -- y = x . W_hat^T with w_hat[n, k] = (q - z) * s: the same kernels,
+ * kernel choice, workspace rules (w4a16_matmul_workspace_bytes), tolerance and
+ * determinism as w4a16_matmul. In the fold -s z stands for the minimum; it is exact in
+ * fp32 (two 11-bit significands).
+ *   x bf16 [M, K]; qw int32 [K/8, N]; scales, zeros fp16 [K/group, N] (w4a16zp_prepare);
+ *   y bf16 [M, N]
+ * Requires M > 0, N > 0, K > 0, group == 128, K % group == 0, N % 8 == 0.
+ */
+w4a16_status w4a16zp_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                            const uint16_t* zeros, uint16_t* y, int M, int N, int K, int group,
+                            void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
+/*
  * w4a16_matmul_noalloc -- the same product as w4a16_matmul for callers that cannot
  * allocate device memory or lend the library a buffer (for example a plugin inside a
  * runtime that owns all device memory, or a loop that must not pay for an allocation).
@@ -130,7 +176,7 @@ w4a16_status w4a16_matmul_noalloc(const uint16_t* x, const int32_t* qw, const ui
 
 /*
  * q4b32_quantize -- fp32 weights to Q4 blocks of 32 ("Why My 4-Bit CUDA Kernel Wasn't
- * Faster": 16 bytes of codes plus a 2-byte scale the 32 weights share).
+ * Faster": an 18-byte block, 32 codes in 16 bytes and one 2-byte scale for all 32).
  *   w      fp32 [N, K]
  *   codes  uint8 [N, K/2]  byte j of block b holds weight 32b+2j in its low nibble
  *                          and weight 32b+2j+1 in its high nibble
@@ -143,8 +189,8 @@ w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16
 
 /*
  * q4b32_gemv -- y[n] = sum_b s[n, b] * sum_j (q[n, b, j] - 8) * x[32 b + j]
- * ("Why My 4-Bit CUDA Kernel Wasn't Faster": pull the code, subtract the bias,
- * multiply by the scale; codes and scales in separate arrays).
+ * ("Why My 4-Bit CUDA Kernel Wasn't Faster": a weight is rebuilt as its code minus
+ * the bias, times the block's scale; codes and scales in separate arrays).
  *   x fp16 [K]; codes uint8 [N, K/2]; scales fp16 [N, K/32]; y fp16 [N]
  * fp32 accumulation, y rounded to nearest even; the same tolerance as w4a16_matmul.
  * Requires N > 0, K > 0, K % 32 == 0.

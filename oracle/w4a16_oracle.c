@@ -14,16 +14,17 @@
  *   [P1] "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured",
  *        Step 2 (group-128 scale/min, q = round((w-min)/scale), 8 nibbles per
  *        int32 along K, K/8 x N packed matrix, K/128 x N scales and minimums;
- *        the Triton listing's unpack "row 8r+j = nibble j of word r" and its
- *        dequantize "q*s + m").
+ *        the Triton listing's unpacking, which takes k = 8r + j from nibble j
+ *        of word r, and its dequantization q*s + m).
  *   [P2] "Why My 4-Bit CUDA Kernel Wasn't Faster", sections "Why fewer bytes
  *        should have helped" and "Loading the same bytes differently" (18-byte
  *        block of 32 codes + 2-byte FP16 scale; decode = code minus bias, times
  *        scale; low nibble is the even weight, high nibble the odd one).
  *   [P3] "Quantization and GEMV", section "W4A16: dequantizing in registers"
- *        (first element in the low 4 bits) and "The quantization formulas".
+ *        (k = 8r + j at bits 4j..4j+3: the lowest nibble holds the first
+ *        weight) and "The quantization formulas".
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent (each also listed in the design notes):
  *   - round() is round-half-to-even (IEEE default; PyTorch's torch.round).
  *   - s and min are rounded to BF16 first; q is computed against the stored
  *     BF16 values, in fp32: t = (w - min_bf16) / s_bf16, then RNE, then clamp
@@ -194,7 +195,8 @@ void oracle_w4a16_quantize(const float* w, int N, int K, int G, uint8_t* codes,
 
 /* Pack 8 codes per 32-bit word along K: word (r, n) holds k = 8r + j in bits
  * 4j..4j+3, first element in the low nibble ([P1] Step 2 listing comment
- * "row 8r + j = nibble j of word r"; [P3] "first element in the low 4 bits").
+ * places k = 8r + j in nibble j of word r; [P3] puts the first weight in the lowest
+ * nibble).
  * qw: int32 [K/8, N], N contiguous. */
 void oracle_w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw) {
   for (int r = 0; r < K / 8; ++r) {
@@ -366,7 +368,7 @@ void oracle_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* 
 /* ------------------------------------------------------------------------ */
 
 /* w: fp32 [N, K]. qw_rows: uint32 [N, K/8], word (n, r) holds k = 8r + j in
- * bits 4j..4j+3 (first element in the low 4 bits). scales, zeros: fp16 bit
+ * bits 4j..4j+3 (the lowest nibble holds the first weight). scales, zeros: fp16 bit
  * patterns [N, K/G] (one per row and group, as [P3] stores them). */
 void oracle_w4a16zp_quantize(const float* w, int N, int K, int G, uint32_t* qw_rows,
                              uint16_t* scales, uint16_t* zeros) {

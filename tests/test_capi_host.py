@@ -37,6 +37,9 @@ def lib(cuda_lib):
     lib.w4a16_status_string.restype = ctypes.c_char_p
     lib.w4a16_matmul_workspace_bytes.argtypes = [I, I, I, I]
     lib.w4a16_matmul_workspace_bytes.restype = S
+    lib.w4a16zp_quantize.argtypes = [P, I, I, I, P, P, P, P]
+    lib.w4a16zp_prepare.argtypes = [P, P, P, I, I, I, P, P, P, P]
+    lib.w4a16zp_matmul.argtypes = [P, P, P, P, P, I, I, I, I, P, S, P]
     return lib
 
 
@@ -44,7 +47,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("w4a16_quantize", "w4a16_pack", "w4a16_matmul", "q4b32_gemv",
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
-                     "w4a16_status_string"):
+                     "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
+                     "w4a16zp_matmul"):
         assert required in names
 
 
@@ -93,6 +97,24 @@ def test_quantize_pack_q4_reject_bad_arguments_on_host(lib):
     assert lib.q4b32_gemv(A, A, A + 8, B, 4, 64, None) == MISALIGNED
     assert lib.w4a16_selftest_bounded_wait(0, None) == INVALID
     assert lib.w4a16_selftest_bounded_wait(2_000_000, None) == INVALID
+
+
+def test_zero_point_entry_points_reject_bad_arguments_on_host(lib):
+    q, p, m = lib.w4a16zp_quantize, lib.w4a16zp_prepare, lib.w4a16zp_matmul
+    assert q(A, 4, 256, 128, None, A, A, None) == INVALID
+    assert q(A, 4, 250, 128, A, A, A, None) == INVALID
+    assert q(A, 4, 256, 64, A, A, A, None) == UNSUPPORTED
+    assert q(A, 4, 256, 128, A, A + 2, A, None) == MISALIGNED
+    assert p(A, A, A, 4, 256, 128, A, A, None, None) == INVALID
+    assert p(A, A, A, 0, 256, 128, A, A, A, None) == INVALID
+    assert p(A, A, A, 4, 256, 32, A, A, A, None) == UNSUPPORTED
+    assert p(A, A, A, 4, 256, 128, A, A + 8, A, None) == MISALIGNED
+    good = (A, A, A, A, B)
+    assert m(None, A, A, A, B, 1, 256, 512, 128, None, 0, None) == INVALID
+    assert m(*good, 1, 256, 500, 128, None, 0, None) == INVALID
+    assert m(*good, 1, 260, 512, 128, None, 0, None) == UNSUPPORTED
+    assert m(A, A, A, A + 2, B, 1, 256, 512, 128, None, 0, None) == MISALIGNED
+    assert m(*good, 1, 256, 512, 128, A, 0, None) == WORKSPACE
 
 
 def test_workspace_query_is_host_only(lib):
