@@ -158,7 +158,8 @@ def test_zp_llama_up_proj_by_m(w4, M):
     run_and_check(w4, M, N, K, seed=M, cols=cols)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1536, 8960), (3, 1536, 1536), (64, 1536, 1536)])
+@pytest.mark.parametrize("M,N,K", [(1, 1536, 8960), (8, 1536, 8960), (2, 4096, 14336),
+                                   (64, 1536, 1536)])
 def test_zp_split_k(w4, M, N, K):
     """Shapes whose plans split K with a workspace (GEMV and tcgen05 partial sums)."""
     assert w4.w4a16_matmul_workspace_bytes(M, N, K) > 0
