@@ -15,6 +15,8 @@ Array conventions (all numpy, C-contiguous):
     ``x`` fp16 bits [K].
   * W4A16 with a zero point: ``qw_rows`` uint32 [N, K/8]; ``scales``/``zeros``
     fp16 bits [N, K/G] (the layout the format's page stores); w_hat = (q - z) s.
+  * W8A16: ``q`` int8 [N, K]; ``s`` fp32 [N] (one per row); ``x`` bf16 bits [K];
+    w_hat = q s.
 """
 from __future__ import annotations
 
@@ -80,11 +82,14 @@ def _bind(lib):
     lib.oracle_w4a16zp_quantize.argtypes = [P, I, I, I, P, P, P]
     lib.oracle_w4a16zp_dequant.argtypes = [P, P, P, I, I, I, P]
     lib.oracle_w4a16zp_matmul.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
+    lib.oracle_w8a16_quantize.argtypes = [P, I, I, P, P]
+    lib.oracle_w8a16_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
     for name in ("oracle_bf16_rne_array", "oracle_fp16_rne_array", "oracle_fp16_to_float_array",
                  "oracle_w4a16_quantize", "oracle_w4a16_pack", "oracle_w4a16_dequant",
                  "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_q4b32_quantize",
                  "oracle_q4b32_dequant", "oracle_q4b32_gemv", "oracle_w4a16zp_quantize",
-                 "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul"):
+                 "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul", "oracle_w8a16_quantize",
+                 "oracle_w8a16_gemv"):
         getattr(lib, name).restype = None
     return lib
 
@@ -289,6 +294,39 @@ def w4a16zp_kernel_layout(qw_rows: np.ndarray, scales: np.ndarray, zeros: np.nda
     return (np.ascontiguousarray(_c(qw_rows, np.uint32).T).view(np.int32),
             np.ascontiguousarray(_c(scales, np.uint16).T),
             np.ascontiguousarray(_c(zeros, np.uint16).T))
+
+
+# --------------------------------------------------------------------------- #
+# W8A16 (symmetric per-row INT8)
+# --------------------------------------------------------------------------- #
+
+def w8a16_quantize(w: np.ndarray):
+    """fp32 [N, K] -> (q int8 [N, K], s fp32 [N])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.int8)
+    s = np.empty(N, dtype=np.float32)
+    _load().oracle_w8a16_quantize(_ptr(w), N, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def w8a16_gemv(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, rows=None):
+    """y_ref, abs_ref (fp64 [N] or [len(rows)]) for y = W_hat . x."""
+    x_bits = _c(x_bits, np.uint16).ravel()
+    q = _c(q, np.int8)
+    s = _c(s, np.float32)
+    N, K = q.shape
+    assert x_bits.shape[0] == K and s.shape[0] == N
+    if rows is None:
+        n_out, rows_p = N, None
+    else:
+        rows = _c(rows, np.int32)
+        n_out, rows_p = len(rows), _ptr(rows)
+    y = np.empty(n_out, dtype=np.float64)
+    a = np.empty(n_out, dtype=np.float64)
+    _load().oracle_w8a16_gemv(_ptr(x_bits), _ptr(q), _ptr(s), N, K, rows_p, n_out, _ptr(y),
+                              _ptr(a))
+    return y, a
 
 
 # --------------------------------------------------------------------------- #

@@ -20,7 +20,9 @@
  *        should have helped" and "Loading the same bytes differently" (18-byte
  *        block of 32 codes + 2-byte FP16 scale; decode = code minus bias, times
  *        scale; low nibble is the even weight, high nibble the odd one).
- *   [P3] "Quantization and GEMV", section "W4A16: dequantizing in registers"
+ *   [P3] "Quantization and GEMV", exercise 1 (W8A16 GEMV: symmetric per-row
+ *        INT8, s = max|w| / 127, one 16-byte load of 16 codes per lane, the
+ *        row's scale applied after the sum) and section "W4A16: dequantizing in registers"
  *        (k = 8r + j at bits 4j..4j+3: the lowest nibble holds the first
  *        weight) and "The quantization formulas".
  *
@@ -42,6 +44,10 @@
  *     rounding of the pages' own host code for this format (std::round).
  *     Codes stay in the pages' layout: words [N, K/8], scales and zeros
  *     [N, K/G].
+ *   - W8A16 [P3 exercise 1]: per row s = fp32(max|w| / 127), kept in fp32 (no
+ *     storage type is given); q = clamp(round(fl(w / s)), -127, 127) with the
+ *     same half-away rounding; a row of zeros stores s = 0 and q = 0. x and y
+ *     are BF16 as in the W4A16 path.
  *
  * Parity pins (tests/test_oracle_pins.py): rounding helpers against PyTorch's
  * own conversions; hand-worked groups in tests/golden/; 4.25 bits/weight and
@@ -447,5 +453,50 @@ void oracle_w4a16zp_matmul(const uint16_t* x, const uint32_t* qw_rows, const uin
       y_ref[(size_t)m * ncols + i] = acc;
       if (abs_ref) abs_ref[(size_t)m * ncols + i] = acc_abs;
     }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* W8A16 ([P3] exercise 1): symmetric per-row INT8, w_hat = q * s.          */
+/* ------------------------------------------------------------------------ */
+
+/* w: fp32 [N, K]; q: int8 [N, K]; s: fp32 [N]. */
+void oracle_w8a16_quantize(const float* w, int N, int K, int8_t* q, float* s) {
+  for (int n = 0; n < N; ++n) {
+    const float* row = w + (size_t)n * K;
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k)
+      if (fabsf(row[k]) > amax) amax = fabsf(row[k]);
+    volatile float s32 = amax / 127.0f; /* fp32 division */
+    s[n] = s32;
+    for (int k = 0; k < K; ++k) {
+      int v = 0;
+      if (s32 != 0.0f) {
+        volatile float t = row[k] / s32; /* fp32 division */
+        double r = (double)round_half_away(t);
+        v = r < -127.0 ? -127 : (r > 127.0 ? 127 : (int)r);
+      }
+      q[(size_t)n * K + k] = (int8_t)v;
+    }
+  }
+}
+
+/* y_ref[i] = sum_k x[k] * q[n, k] * s[n] for n = rows[i] (every row when rows
+ * is NULL) in fp64, and abs_ref the sum of the magnitudes of the terms.
+ * x: bf16 bit patterns [K]. */
+void oracle_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s, int N, int K,
+                       const int32_t* rows, int nrows, double* y_ref, double* abs_ref) {
+  if (!rows) nrows = N;
+  for (int i = 0; i < nrows; ++i) {
+    int n = rows ? rows[i] : i;
+    double acc = 0.0, acc_abs = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double w_hat = (double)q[(size_t)n * K + k] * (double)s[n];
+      double xv = (double)oracle_bf16_to_float(x[k]);
+      acc += xv * w_hat;
+      acc_abs += fabs(xv * w_hat);
+    }
+    y_ref[i] = acc;
+    if (abs_ref) abs_ref[i] = acc_abs;
   }
 }

@@ -493,4 +493,94 @@ def pin_zp_matches_library_matmul_and_error_band():
     assert zk[3, 1] == z[1, 3]
 
 
+# --------------------------------------------------------------------------- #
+# W8A16: symmetric per-row INT8, w_hat = q s
+# --------------------------------------------------------------------------- #
+
+def _half_away(t):
+    a = math.floor(abs(t) + Fraction(1, 2))
+    return a if t >= 0 else -a
+
+
+def pin_w8_hand_worked_rows():
+    """Hand-worked rows (tests/golden/w8a16_rows.txt): the fp32 scale and every code."""
+    for tag, rec in _records("w8a16_rows.txt"):
+        w = _weights_from(rec).reshape(1, -1)
+        q, s = oracle.w8a16_quantize(w)
+        assert int(s.view(np.uint32)[0]) == int(rec["scale"][0], 16), (tag, s[0])
+        assert q[0].tolist() == [int(v) for v in rec["q"]], (tag, q[0].tolist())
+
+
+def pin_w8_round_trip_on_grid():
+    """Rows q s with s a power of two and |q| = 127 present quantize back to exactly
+    (q, s) and rebuild bit for bit."""
+    rng = np.random.default_rng(31)
+    N, K = 16, 256
+    e = rng.integers(-14, -4, size=N)
+    q = rng.integers(-127, 128, size=(N, K))
+    q[:, 0] = np.where(rng.random(N) < 0.5, 127, -127)
+    w = q * np.exp2(e)[:, None]
+    w32 = w.astype(np.float32)
+    assert np.array_equal(w32.astype(np.float64), w)
+    q2, s2 = oracle.w8a16_quantize(w32)
+    np.testing.assert_array_equal(q2, q.astype(np.int8))
+    np.testing.assert_array_equal(s2.astype(np.float64), np.exp2(e))
+    one = _torch_bits(torch.tensor([1.0], dtype=torch.bfloat16))[0]
+    for k in (0, 5, 255):
+        x = np.zeros(K, dtype=np.uint16)
+        x[k] = one
+        y, a = oracle.w8a16_gemv(x, q2, s2)
+        np.testing.assert_array_equal(y, w[:, k])
+        np.testing.assert_array_equal(a, np.abs(w[:, k]))
+
+
+def pin_w8_codes_follow_the_formula():
+    """On random rows the scale is max|w| / 127 to fp32 rounding and each code is the
+    exact quotient rounded half away from zero (quotients within 2^-16 of a half-integer,
+    where the fp32 quotient may decide otherwise, are skipped)."""
+    w = workloads.weights(6, 512, seed=33).numpy()
+    q, s = oracle.w8a16_quantize(w)
+    for n in range(w.shape[0]):
+        amax = Fraction(float(np.abs(w[n]).max()))
+        sf = Fraction(float(s[n]))
+        assert abs(sf - amax / 127) <= amax / 127 / 2**23
+        for k in range(w.shape[1]):
+            t = Fraction(float(w[n, k])) / sf
+            if abs(abs(t - math.floor(t)) - Fraction(1, 2)) <= Fraction(1, 2**16):
+                continue
+            assert int(q[n, k]) == max(-127, min(127, _half_away(t))), (n, k, float(t))
+
+
+def pin_w8_gemv_exact_small_and_library():
+    """Small cases equal the exact rational sum; a larger one equals torch.matmul (fp64)
+    on the rebuilt weights; the row subset entry point matches; INT8 per-row quantization
+    of N(0, 0.02^2) weights gives an output error near 1 % (0.3-2 % accepted)."""
+    rng = np.random.default_rng(35)
+    for (N, K) in ((3, 64), (9, 96)):
+        w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        q, s = oracle.w8a16_quantize(w)
+        x = workloads.bits16(workloads.activations_bf16(1, K, seed=N))[0]
+        y, a = oracle.w8a16_gemv(x, q, s)
+        for n in range(N):
+            exact = sum(Fraction(_bf16(x[k])) * int(q[n, k]) * Fraction(float(s[n]))
+                        for k in range(K))
+            assert abs(Fraction(y[n]) - exact) <= Fraction(a[n]) / 2**45, (N, K, n)
+    N, K = 128, 2048
+    w = workloads.weights(N, K, seed=36).numpy()
+    q, s = oracle.w8a16_quantize(w)
+    x = workloads.bits16(workloads.activations_bf16(1, K, seed=36))[0]
+    y, a = oracle.w8a16_gemv(x, q, s)
+    w_hat = torch.from_numpy(q.astype(np.float64)) * torch.from_numpy(s.astype(np.float64))[:, None]
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double()
+    ref = (w_hat @ xv).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    rows = np.array([N - 1, 0, 17], dtype=np.int32)
+    y2, a2 = oracle.w8a16_gemv(x, q, s, rows=rows)
+    np.testing.assert_array_equal(y2, y[rows])
+    np.testing.assert_array_equal(a2, a[rows])
+    y_o = w.astype(np.float64) @ xv.numpy()
+    rel = np.linalg.norm(y - y_o) / np.linalg.norm(y_o)
+    assert 0.003 < rel < 0.02, rel
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -65,6 +65,16 @@ MUTANTS = [
      "        double z = (double)oracle_fp16_to_float(zeros[(size_t)(k / G) * N + n]);\n"
      "        double w_hat = ((double)unpack_code_rows(qw_rows, K, n, k) - z) * s;\n"
      "        double xv", None),
+    ("w8_scale_divides_by_128", "volatile float s32 = amax / 127.0f;",
+     "volatile float s32 = amax / 128.0f;", None),
+    ("w8_round_half_even", "double r = (double)round_half_away(t);\n        v = r < -127.0",
+     "double r = round_half_even((double)t);\n        v = r < -127.0", None),
+    ("w8_codes_truncated", "double r = (double)round_half_away(t);\n        v = r < -127.0",
+     "double r = (double)truncf(t);\n        v = r < -127.0", None),
+    ("w8_scale_of_next_row", "double w_hat = (double)q[(size_t)n * K + k] * (double)s[n];",
+     "double w_hat = (double)q[(size_t)n * K + k] * (double)s[(n + 1) % N];", None),
+    ("w8_amax_without_abs", "if (fabsf(row[k]) > amax) amax = fabsf(row[k]);",
+     "if (row[k] > amax) amax = row[k];", None),
     ("zp_nibble_order_reversed", "(uint32_t)q << (4 * (k % 8));", "(uint32_t)q << (4 * (7 - k % 8));",
      None),
 ]
