@@ -11,7 +11,7 @@ around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than t
 The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
 the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
 quantize and GEMV (16384 x 16384), the zero-point format (quantize, layout move, matmul at
-M = 1, 16, 4096), and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
+M = 1, 16, 4096), the W8A16 per-row INT8 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
 each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -467,6 +467,25 @@ def rows_ours(peaks, device, stream):
     rows["zero_point"] = zp
     del cps, qk, sk, zk
 
+    # W8A16 (per-row INT8) on the up-projection: quantize and the M = 1 GEMV
+    N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+    w = workloads.weights(N, K, seed=0).to(device)
+    q8, s8 = w4.w8a16_quantize(w)
+    us = graph_time_us(lambda i: w4.w8a16_quantize(w, q=q8, scales=s8), 4, 5, stream)
+    b = N * K * 4 + N * K + 4 * N
+    w8 = {"shape": [N, K], "quantize": {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                                         "frac_hbm": round(b / us / 1e3 / hbm, 3)}}
+    del w
+    cps8 = [(q8.clone(), s8.clone()) for _ in range(8)]  # 8 x 58.7 MB > 2 x L2
+    x8 = workloads.activations_bf16(1, K, seed=1)[0].to(device)
+    y8 = torch.empty(N, dtype=torch.bfloat16, device=device)
+    us = graph_time_us(lambda i: w4.w8a16_gemv(x8, *cps8[i % 8], y=y8), 16, 10, stream)
+    b = N * K + 4 * N
+    w8["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                  "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
+    rows["w8a16"] = w8
+    del cps8, q8, s8
+
     # Q4 block-32, 16384 x 16384
     qc_cfg = workloads.Q4_SQUARE
     N, K = qc_cfg["N"], qc_cfg["K"]
@@ -589,21 +608,38 @@ def run_reference(args, world, rank):
 
 
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
-                 "q4b32_gemv", "quantize", "pack")
+                 "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1")
 
 
 def profile_case(args):
     """A few launches of one workload, untimed, for a profiler (ncu -k ... -c ...): the
     Llama-3-8B up-projection (14336 x 4096) at M = 1, 8, 16 or 32 (skinny kernel), 16
     (tensor-core kernel) or 4096 with 6 rotating weight copies (174 MB > L2), the Q4
-    block-32 GEMV (16384 x 16384), or quantize / pack."""
+    block-32 GEMV (16384 x 16384), quantize / pack, the W8A16 GEMV or the zero-point
+    matmul at M = 1 on the same layer."""
     import gemv_w4a16_group_gb300 as w4
 
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     case, n = args.case, args.launches
-    if case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
-                "quantize", "pack"):
+    if case in ("w8a16_gemv", "zp_m1"):
+        N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+        w = workloads.weights(N, K, seed=0).to(device)
+        x = workloads.activations_bf16(1, K, seed=1).to(device)
+        if case == "w8a16_gemv":
+            q8, s8 = w4.w8a16_quantize(w)
+            del w
+            cps = [(q8.clone(), s8.clone()) for _ in range(4)]
+            for i in range(n):
+                w4.w8a16_gemv(x[0], *cps[i % 4])
+        else:
+            qk, sk, zk = w4.w4a16zp_prepare(*w4.w4a16zp_quantize(w))
+            del w
+            cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(6)]
+            for i in range(n):
+                w4.w4a16zp_matmul(x, *cps[i % 6])
+    elif case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
+                  "quantize", "pack"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
         if case == "quantize":

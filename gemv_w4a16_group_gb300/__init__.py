@@ -18,6 +18,8 @@ Formats ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2;
     quantized into words int32 [N, K/8] and float16 scales / zeros [N, K/128] (the page's
     layout), moved by ``w4a16zp_prepare`` into qw [K/8, N] and scales / zeros [K/128, N]
     for ``w4a16zp_matmul``; w_hat = (q - zero) * scale.
+  * W8A16 (the page's exercise 1): q int8 [N, K]; scales float32 [N]; x bfloat16 [K];
+    y bfloat16 [N]; w_hat = q * scale.
 """
 from __future__ import annotations
 
@@ -33,7 +35,7 @@ __all__ = [
     "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
     "testing_set_q4_variant", "testing_set_skinny_range", "w4a16zp_quantize",
-    "w4a16zp_prepare", "w4a16zp_matmul",
+    "w4a16zp_prepare", "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -70,6 +72,8 @@ def _load():
         "w4a16zp_quantize": [P, I, I, I, P, P, P, P],
         "w4a16zp_prepare": [P, P, P, I, I, I, P, P, P, P],
         "w4a16zp_matmul": [P, P, P, P, P, I, I, I, I, P, S, P],
+        "w8a16_quantize": [P, I, I, P, P, P],
+        "w8a16_gemv": [P, P, P, P, I, I, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -247,6 +251,32 @@ def w4a16zp_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, zero
         _dev(scales, "scales", torch.float16, (K // group, N)),
         _dev(zeros, "zeros", torch.float16, (K // group, N)),
         _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
+    return y
+
+
+def w8a16_quantize(w: torch.Tensor, q=None, scales=None, stream=None):
+    """fp32 [N, K] -> (q int8 [N, K], scales fp32 [N])."""
+    N, K = w.shape
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _check("w8a16_quantize", _lib.w8a16_quantize(
+        _dev(w, "w", torch.float32), N, K, _dev(q, "q", torch.int8, (N, K)),
+        _dev(scales, "scales", torch.float32, (N,)), _stream(stream)))
+    return q, scales
+
+
+def w8a16_gemv(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, y=None,
+               stream=None) -> torch.Tensor:
+    """y [N] (bf16) = (q * scales[:, None]) . x, x bf16 [K]."""
+    N, K = q.shape
+    if y is None:
+        y = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
+    _check("w8a16_gemv", _lib.w8a16_gemv(
+        _dev(x, "x", torch.bfloat16, (K,)), _dev(q, "q", torch.int8, (N, K)),
+        _dev(scales, "scales", torch.float32, (N,)), _dev(y, "y", torch.bfloat16, (N,)), N, K,
+        _stream(stream)))
     return y
 
 

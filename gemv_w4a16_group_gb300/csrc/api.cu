@@ -269,6 +269,26 @@ w4a16_status w4a16zp_matmul(const uint16_t* x, const int32_t* qw, const uint16_t
                      true);
 }
 
+w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scales,
+                            w4a16_stream_t stream) {
+  if (!w || !q || !scales) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 64 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(scales)) return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w8a16_quantize(w, N, K, q, scales,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
+                        int N, int K, w4a16_stream_t stream) {
+  if (!x || !q || !scales || !y) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 64 != 0) return W4A16_ERR_INVALID_ARG;
+  if (w4k::w8a16_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || !aligned16(y))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(
+      w4k::launch_w8a16_gemv(x, q, scales, y, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                             w4a16_stream_t stream) {
   if (!w || !codes || !scales) return W4A16_ERR_INVALID_ARG;

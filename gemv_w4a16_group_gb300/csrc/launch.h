@@ -123,6 +123,14 @@ cudaError_t launch_q4b32_gemv_tc(const uint16_t* x, const uint8_t* codes, const 
                                  uint16_t* y, int N, int K, uint32_t* status,
                                  uint64_t wait_limit_ns, cudaStream_t stream);
 
+// W8A16 (symmetric per-row INT8): quantize, one CTA per row; GEMV, 16 rows per CTA with x
+// (2 K bytes) in shared memory. K % 64 == 0.
+uint32_t w8a16_smem_bytes(int K);
+cudaError_t launch_w8a16_quantize(const float* w, int N, int K, int8_t* q, float* s,
+                                  cudaStream_t stream);
+cudaError_t launch_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s, uint16_t* y,
+                              int N, int K, cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -10,7 +10,8 @@
  *   of 32 codes plus an FP16 scale, w_hat = (q - 8) * s ("Why My 4-Bit CUDA Kernel
  *   Wasn't Faster", "Why fewer bytes should have helped"). A third is the zero-point
  *   form w_hat = (q - z) * s with FP16 scale and zero point per group of 128
- *   ("Quantization and GEMV", "The quantization formulas").
+ *   ("Quantization and GEMV", "The quantization formulas"), and the page's W8A16
+ *   exercise adds symmetric per-row INT8 weights, w_hat = q * s.
  *
  * Conventions shared by every entry point
  *   - Every array pointer is DEVICE memory owned by the caller. The library keeps no
@@ -197,6 +198,28 @@ w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16
  */
 w4a16_status q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
                         uint16_t* y, int N, int K, w4a16_stream_t stream);
+
+/*
+ * W8A16 ("Quantization and GEMV", exercise 1): symmetric per-row INT8 weights,
+ * w_hat = q * s, one fp32 scale per row (8 bits per weight plus 4 bytes per row).
+ *
+ * w8a16_quantize -- w fp32 [N, K] -> q int8 [N, K], scales fp32 [N]:
+ *   s = fl(max_k |w[n, k]| / 127); q = clamp(round(fl(w / s)), -127, 127) with round()
+ *   half away from zero (the page's host code uses std::round); a row of zeros stores
+ *   s = 0 and q = 0. Requires N > 0, K > 0, K % 64 == 0.
+ */
+w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scales,
+                            w4a16_stream_t stream);
+
+/*
+ * w8a16_gemv -- y[n] = s[n] * sum_k q[n, k] x[k] (the scale once per row, after the sum).
+ *   x bf16 [K]; q int8 [N, K]; scales fp32 [N]; y bf16 [N] (fp32 accumulation, rounded to
+ *   nearest even). The tolerance of w4a16_matmul applies. x is held in shared memory:
+ *   K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0,
+ *   K % 64 == 0.
+ */
+w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
+                        int N, int K, w4a16_stream_t stream);
 
 /*
  * w4a16_device_status -- synchronizes `stream`, then reads and clears the current

@@ -40,6 +40,8 @@ def lib(cuda_lib):
     lib.w4a16zp_quantize.argtypes = [P, I, I, I, P, P, P, P]
     lib.w4a16zp_prepare.argtypes = [P, P, P, I, I, I, P, P, P, P]
     lib.w4a16zp_matmul.argtypes = [P, P, P, P, P, I, I, I, I, P, S, P]
+    lib.w8a16_quantize.argtypes = [P, I, I, P, P, P]
+    lib.w8a16_gemv.argtypes = [P, P, P, P, I, I, P]
     return lib
 
 
@@ -48,7 +50,7 @@ def test_header_declares_the_boundary():
     for required in ("w4a16_quantize", "w4a16_pack", "w4a16_matmul", "q4b32_gemv",
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
                      "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
-                     "w4a16zp_matmul"):
+                     "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv"):
         assert required in names
 
 
@@ -115,6 +117,18 @@ def test_zero_point_entry_points_reject_bad_arguments_on_host(lib):
     assert m(*good, 1, 260, 512, 128, None, 0, None) == UNSUPPORTED
     assert m(A, A, A, A + 2, B, 1, 256, 512, 128, None, 0, None) == MISALIGNED
     assert m(*good, 1, 256, 512, 128, A, 0, None) == WORKSPACE
+
+
+def test_w8a16_rejects_bad_arguments_on_host(lib):
+    q, g = lib.w8a16_quantize, lib.w8a16_gemv
+    assert q(A, 4, 256, None, A, None) == INVALID
+    assert q(A, 4, 100, A, A, None) == INVALID          # K % 64
+    assert q(A, 0, 256, A, A, None) == INVALID
+    assert q(A, 4, 256, A, A + 4, None) == MISALIGNED
+    assert g(A, A, A, None, 4, 256, None) == INVALID
+    assert g(A, A, A, B, 4, 96, None) == INVALID         # K % 64
+    assert g(A, A, A, B, 4, 64 * 4096, None) == UNSUPPORTED  # x does not fit shared memory
+    assert g(A + 2, A, A, B, 4, 256, None) == MISALIGNED
 
 
 def test_workspace_query_is_host_only(lib):
