@@ -17,6 +17,8 @@ Array conventions (all numpy, C-contiguous):
     fp16 bits [N, K/G] (the layout the format's page stores); w_hat = (q - z) s.
   * W8A16: ``q`` int8 [N, K]; ``s`` fp32 [N] (one per row); ``x`` bf16 bits [K];
     w_hat = q s.
+  * NVFP4A16: ``codes`` uint8 [N, K/2] (E2M1, low nibble = even k); ``scales`` uint8
+    E4M3 [N, K/16]; ``S`` one fp32; ``x`` bf16 bits [K]; w_hat = e2m1 e4m3 S.
 """
 from __future__ import annotations
 
@@ -84,12 +86,25 @@ def _bind(lib):
     lib.oracle_w4a16zp_matmul.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
     lib.oracle_w8a16_quantize.argtypes = [P, I, I, P, P]
     lib.oracle_w8a16_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
+    F = ctypes.c_float
+    lib.oracle_e2m1_value.argtypes = [I]
+    lib.oracle_e2m1_value.restype = ctypes.c_double
+    lib.oracle_e4m3_value.argtypes = [I]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_e2m1_rne.argtypes = [F]
+    lib.oracle_e2m1_rne.restype = I
+    lib.oracle_e4m3_ceil.argtypes = [F]
+    lib.oracle_e4m3_ceil.restype = I
+    lib.oracle_nvfp4_quantize.argtypes = [P, I, I, P, P, P]
+    lib.oracle_nvfp4_dequant.argtypes = [P, P, F, I, I, P]
+    lib.oracle_nvfp4_gemv.argtypes = [P, P, P, F, I, I, P, I, P, P]
     for name in ("oracle_bf16_rne_array", "oracle_fp16_rne_array", "oracle_fp16_to_float_array",
                  "oracle_w4a16_quantize", "oracle_w4a16_pack", "oracle_w4a16_dequant",
                  "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_q4b32_quantize",
                  "oracle_q4b32_dequant", "oracle_q4b32_gemv", "oracle_w4a16zp_quantize",
                  "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul", "oracle_w8a16_quantize",
-                 "oracle_w8a16_gemv"):
+                 "oracle_w8a16_gemv", "oracle_nvfp4_quantize", "oracle_nvfp4_dequant",
+                 "oracle_nvfp4_gemv"):
         getattr(lib, name).restype = None
     return lib
 
@@ -326,6 +341,66 @@ def w8a16_gemv(x_bits: np.ndarray, q: np.ndarray, s: np.ndarray, rows=None):
     a = np.empty(n_out, dtype=np.float64)
     _load().oracle_w8a16_gemv(_ptr(x_bits), _ptr(q), _ptr(s), N, K, rows_p, n_out, _ptr(y),
                               _ptr(a))
+    return y, a
+
+
+# --------------------------------------------------------------------------- #
+# NVFP4 weights (E2M1 codes, E4M3 block scales, fp32 tensor scale)
+# --------------------------------------------------------------------------- #
+
+def e2m1_value(code: int) -> float:
+    return float(_load().oracle_e2m1_value(int(code)))
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def e2m1_rne(t: float) -> int:
+    return int(_load().oracle_e2m1_rne(float(t)))
+
+
+def e4m3_ceil(v: float) -> int:
+    return int(_load().oracle_e4m3_ceil(float(v)))
+
+
+def nvfp4_quantize(w: np.ndarray):
+    """fp32 [N, K] -> (codes u8 [N, K/2], scales u8 E4M3 [N, K/16], S float)."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 16 == 0
+    codes = np.empty((N, K // 2), dtype=np.uint8)
+    scales = np.empty((N, K // 16), dtype=np.uint8)
+    S = np.zeros(1, dtype=np.float32)
+    _load().oracle_nvfp4_quantize(_ptr(w), N, K, _ptr(codes), _ptr(scales), _ptr(S))
+    return codes, scales, float(S[0])
+
+
+def nvfp4_dequant(codes: np.ndarray, scales: np.ndarray, S: float) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((N, K), dtype=np.float64)
+    _load().oracle_nvfp4_dequant(_ptr(codes), _ptr(scales), float(S), N, K, _ptr(out))
+    return out
+
+
+def nvfp4_gemv(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, S: float, rows=None):
+    """y_ref, abs_ref (fp64 [N] or [len(rows)]) for y = W_hat . x."""
+    x_bits = _c(x_bits, np.uint16).ravel()
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    assert x_bits.shape[0] == K and scales.shape == (N, K // 16)
+    if rows is None:
+        n_out, rows_p = N, None
+    else:
+        rows = _c(rows, np.int32)
+        n_out, rows_p = len(rows), _ptr(rows)
+    y = np.empty(n_out, dtype=np.float64)
+    a = np.empty(n_out, dtype=np.float64)
+    _load().oracle_nvfp4_gemv(_ptr(x_bits), _ptr(codes), _ptr(scales), float(S), N, K, rows_p,
+                              n_out, _ptr(y), _ptr(a))
     return y, a
 
 

@@ -20,6 +20,10 @@
  *        should have helped" and "Loading the same bytes differently" (18-byte
  *        block of 32 codes + 2-byte FP16 scale; decode = code minus bias, times
  *        scale; low nibble is the even weight, high nibble the odd one).
+ *   [P4] "Hardware-invariant NVFP4 progress report 1", "The NVFP4 layout"
+ *        (E2M1 weights, largest value 6, an E4M3 scale per 16 weights and an
+ *        FP32 scale per tensor; NVFP4A16 decodes to 16-bit floats) and [P1]
+ *        Step 6 (4.5 bits per value).
  *   [P3] "Quantization and GEMV", exercise 1 (W8A16 GEMV: symmetric per-row
  *        INT8, s = max|w| / 127, one 16-byte load of 16 codes per lane, the
  *        row's scale applied after the sum) and section "W4A16: dequantizing in registers"
@@ -44,6 +48,17 @@
  *     rounding of the pages' own host code for this format (std::round).
  *     Codes stay in the pages' layout: words [N, K/8], scales and zeros
  *     [N, K/G].
+ *   - NVFP4 [P1 Step 6, P4 "The NVFP4 layout"]: E2M1 codes (2 exponent bits,
+ *     bias 1, 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per 16
+ *     weights along K and one fp32 scale per tensor, w_hat = e2m1 * e4m3 * S.
+ *     S = fl(amax / 2688) (2688 = 6 * 448 puts the largest block scale at
+ *     E4M3's largest finite value; 1 for an all-zero tensor); a block's scale
+ *     is the smallest E4M3 value >= fl(amax_b / fl(6 S)), at most 448 ([P4]
+ *     "What's left to tune": a scale that E4M3 rounds down would clip the
+ *     block's largest weight, so it is rounded up); codes round fl(w / fl(s_b S)) to
+ *     the nearest E2M1 value, ties to the even code, saturating at 6; a block
+ *     of zeros stores scale 0 and codes 0. Codes [N, K/2] (low nibble = even
+ *     k), scales [N, K/16].
  *   - W8A16 [P3 exercise 1]: per row s = fp32(max|w| / 127), kept in fp32 (no
  *     storage type is given); q = clamp(round(fl(w / s)), -127, 127) with the
  *     same half-away rounding; a row of zeros stores s = 0 and q = 0. x and y
@@ -495,6 +510,123 @@ void oracle_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s, int N
       double xv = (double)oracle_bf16_to_float(x[k]);
       acc += xv * w_hat;
       acc_abs += fabs(xv * w_hat);
+    }
+    y_ref[i] = acc;
+    if (abs_ref) abs_ref[i] = acc_abs;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 weights, 16-bit activations ([P4], [P1] Step 6).                   */
+/* ------------------------------------------------------------------------ */
+
+/* E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is
+ * subnormal (0 or 0.5). */
+double oracle_e2m1_value(int code) {
+  int e = (code >> 1) & 3, m = code & 1;
+  double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (code & 8) ? -mag : mag;
+}
+
+/* E4M3 (the finite-only FN variant): sign, 4 exponent bits (bias 7), 3
+ * mantissa bits; exponent 0 is subnormal (m * 2^-9); 0x7F / 0xFF are NaN, so
+ * the largest finite value is 0x7E = 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(int code) {
+  int e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return (code & 0x80) ? -mag : mag;
+}
+
+/* Nearest E2M1 code to t, ties to the code with mantissa bit 0, |t| >= 6
+ * gives 6; the sign is kept, zeros included. */
+int oracle_e2m1_rne(float t) {
+  int sign = signbit(t) ? 8 : 0;
+  double a = fabs((double)t);
+  int best = 7;
+  if (a < 6.0) {
+    best = 0;
+    for (int c = 0; c < 7; ++c) {
+      double lo = oracle_e2m1_value(c), hi = oracle_e2m1_value(c + 1);
+      double mid = 0.5 * (lo + hi);
+      if (a < mid) { best = c; break; }
+      if (a == mid) { best = (c & 1) ? c + 1 : c; break; }
+      best = c + 1;
+    }
+  }
+  return sign | best;
+}
+
+/* Smallest non-negative E4M3 code whose value is >= v (v >= 0), at most 0x7E. */
+int oracle_e4m3_ceil(float v) {
+  for (int c = 0; c <= 0x7E; ++c)
+    if (oracle_e4m3_value(c) >= (double)v) return c;
+  return 0x7E;
+}
+
+/* w: fp32 [N, K] (K % 16 == 0); codes: uint8 [N, K/2], byte j of a row holds
+ * k = 2j in its low nibble and k = 2j + 1 in its high nibble; scales: E4M3
+ * [N, K/16]; tensor_scale: one fp32. */
+void oracle_nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                           float* tensor_scale) {
+  float amax = 0.0f;
+  for (size_t i = 0; i < (size_t)N * K; ++i)
+    if (fabsf(w[i]) > amax) amax = fabsf(w[i]);
+  volatile float S = amax > 0.0f ? amax / 2688.0f : 1.0f; /* fp32 division */
+  *tensor_scale = S;
+  volatile float d6 = 6.0f * S;
+  for (int n = 0; n < N; ++n) {
+    for (int b = 0; b < K / 16; ++b) {
+      const float* wb = w + (size_t)n * K + (size_t)b * 16;
+      float bmax = 0.0f;
+      for (int j = 0; j < 16; ++j)
+        if (fabsf(wb[j]) > bmax) bmax = fabsf(wb[j]);
+      int sc = 0;
+      int q[16] = {0};
+      if (bmax > 0.0f) {
+        volatile float v = bmax / d6; /* fp32 division */
+        sc = oracle_e4m3_ceil(v);
+        volatile float den = (float)oracle_e4m3_value(sc) * S; /* fp32 product */
+        for (int j = 0; j < 16; ++j) {
+          volatile float t = wb[j] / den; /* fp32 division */
+          q[j] = oracle_e2m1_rne(t);
+        }
+      }
+      scales[(size_t)n * (K / 16) + b] = (uint8_t)sc;
+      for (int j = 0; j < 8; ++j)
+        codes[(size_t)n * (K / 2) + (size_t)b * 8 + j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+    }
+  }
+}
+
+/* w_hat[n, k] = e2m1(q) * e4m3(s_b) * S, exact in fp64. */
+static double nvfp4_w_hat(const uint8_t* codes, const uint8_t* scales, float S, int K, int n,
+                          int k) {
+  uint8_t byte = codes[(size_t)n * (K / 2) + k / 2];
+  int q = (k & 1) ? (byte >> 4) : (byte & 15);
+  return oracle_e2m1_value(q) * oracle_e4m3_value(scales[(size_t)n * (K / 16) + k / 16]) *
+         (double)S;
+}
+
+void oracle_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float S, int N, int K,
+                          double* w_hat) {
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) w_hat[(size_t)n * K + k] = nvfp4_w_hat(codes, scales, S, K, n, k);
+}
+
+/* y_ref[i] = sum_k x[k] * w_hat[n, k] for n = rows[i] (every row when rows is
+ * NULL), fp64; abs_ref the sum of the magnitudes. x: bf16 bit patterns [K]. */
+void oracle_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales, float S,
+                       int N, int K, const int32_t* rows, int nrows, double* y_ref,
+                       double* abs_ref) {
+  if (!rows) nrows = N;
+  for (int i = 0; i < nrows; ++i) {
+    int n = rows ? rows[i] : i;
+    double acc = 0.0, acc_abs = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double t = (double)oracle_bf16_to_float(x[k]) * nvfp4_w_hat(codes, scales, S, K, n, k);
+      acc += t;
+      acc_abs += fabs(t);
     }
     y_ref[i] = acc;
     if (abs_ref) abs_ref[i] = acc_abs;

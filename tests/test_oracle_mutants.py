@@ -75,6 +75,21 @@ MUTANTS = [
      "double w_hat = (double)q[(size_t)n * K + k] * (double)s[(n + 1) % N];", None),
     ("w8_amax_without_abs", "if (fabsf(row[k]) > amax) amax = fabsf(row[k]);",
      "if (row[k] > amax) amax = row[k];", None),
+    ("nv_ties_away", "if (a == mid) { best = (c & 1) ? c + 1 : c; break; }",
+     "if (a == mid) { best = c + 1; break; }", None),
+    ("nv_block_scale_nearest", "if (oracle_e4m3_value(c) >= (double)v) return c;",
+     "if (oracle_e4m3_value(c) >= (double)v) return (c > 0 && (double)v - oracle_e4m3_value(c - 1) < oracle_e4m3_value(c) - (double)v) ? c - 1 : c;",
+     None),
+    ("nv_tensor_scale_448", "amax / 2688.0f", "amax / 448.0f", None),
+    ("nv_nibbles_swapped", "(uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));",
+     "(uint8_t)(q[2 * j + 1] | (q[2 * j] << 4));", None),
+    ("nv_e4m3_bias_8", "ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)", None),
+    ("nv_e2m1_subnormal_1", "double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+     "double mag = e == 0 ? 1.0 * m : ldexp(1.0 + 0.5 * m, e - 1);", None),
+    ("nv_gemv_drops_tensor_scale",
+     "return oracle_e2m1_value(q) * oracle_e4m3_value(scales[(size_t)n * (K / 16) + k / 16]) *\n         (double)S;",
+     "return oracle_e2m1_value(q) * oracle_e4m3_value(scales[(size_t)n * (K / 16) + k / 16]);",
+     None),
     ("zp_nibble_order_reversed", "(uint32_t)q << (4 * (k % 8));", "(uint32_t)q << (4 * (7 - k % 8));",
      None),
 ]
