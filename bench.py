@@ -11,7 +11,7 @@ around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than t
 The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
 the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
 quantize and GEMV (16384 x 16384), the zero-point format (quantize, layout move, matmul at
-M = 1, 16, 4096), the W8A16 per-row INT8 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
+M = 1, 16, 4096), the W8A16 per-row INT8 and the NVFP4A16 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
 each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -486,6 +486,23 @@ def rows_ours(peaks, device, stream):
     rows["w8a16"] = w8
     del cps8, q8, s8
 
+    # NVFP4A16 on the up-projection: quantize and the M = 1 GEMV
+    w = workloads.weights(N, K, seed=0).to(device)
+    c4, s4, S4 = w4.nvfp4_quantize(w)
+    us = graph_time_us(lambda i: w4.nvfp4_quantize(w, codes=c4, scales=s4, tensor_scale=S4), 4, 5,
+                       stream)
+    b = N * K * 4 * 2 + N * K // 2 + N * K // 16  # two reads of w (amax, then codes)
+    nv = {"shape": [N, K], "quantize": {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                                         "frac_hbm": round(b / us / 1e3 / hbm, 3)}}
+    del w
+    cps4 = [(c4.clone(), s4.clone(), S4.clone()) for _ in range(ROTATE)]
+    us = graph_time_us(lambda i: w4.nvfp4_gemv(x8, *cps4[i % ROTATE], y=y8), 2 * ROTATE, 10, stream)
+    b = N * K // 2 + N * K // 16
+    nv["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                  "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
+    rows["nvfp4a16"] = nv
+    del cps4, c4, s4, S4, x8, y8
+
     # Q4 block-32, 16384 x 16384
     qc_cfg = workloads.Q4_SQUARE
     N, K = qc_cfg["N"], qc_cfg["K"]
@@ -608,7 +625,7 @@ def run_reference(args, world, rank):
 
 
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
-                 "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1")
+                 "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1", "nvfp4_gemv")
 
 
 def profile_case(args):
@@ -622,11 +639,17 @@ def profile_case(args):
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     case, n = args.case, args.launches
-    if case in ("w8a16_gemv", "zp_m1"):
+    if case in ("w8a16_gemv", "zp_m1", "nvfp4_gemv"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w = workloads.weights(N, K, seed=0).to(device)
         x = workloads.activations_bf16(1, K, seed=1).to(device)
-        if case == "w8a16_gemv":
+        if case == "nvfp4_gemv":
+            c4, s4, S4 = w4.nvfp4_quantize(w)
+            del w
+            cps = [(c4.clone(), s4.clone(), S4.clone()) for _ in range(6)]
+            for i in range(n):
+                w4.nvfp4_gemv(x[0], *cps[i % 6])
+        elif case == "w8a16_gemv":
             q8, s8 = w4.w8a16_quantize(w)
             del w
             cps = [(q8.clone(), s8.clone()) for _ in range(4)]

@@ -131,6 +131,16 @@ cudaError_t launch_w8a16_quantize(const float* w, int N, int K, int8_t* q, float
 cudaError_t launch_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s, uint16_t* y,
                               int N, int K, cudaStream_t stream);
 
+// NVFP4 weights (E2M1 codes [N, K/2], E4M3 block scales [N, K/16], one fp32 tensor scale):
+// quantize (amax, per-block codes, finalize; four stream-ordered steps) and the M = 1 GEMV.
+// K % 128 == 0.
+uint32_t nvfp4_smem_bytes(int K);
+cudaError_t launch_nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                                  float* tensor_scale, cudaStream_t stream);
+cudaError_t launch_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                              const float* tensor_scale, uint16_t* y, int N, int K,
+                              cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

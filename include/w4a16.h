@@ -11,7 +11,8 @@
  *   Wasn't Faster", "Why fewer bytes should have helped"). A third is the zero-point
  *   form w_hat = (q - z) * s with FP16 scale and zero point per group of 128
  *   ("Quantization and GEMV", "The quantization formulas"), and the page's W8A16
- *   exercise adds symmetric per-row INT8 weights, w_hat = q * s.
+ *   exercise adds symmetric per-row INT8 weights, w_hat = q * s; NVFP4 weights (E2M1
+ *   codes with E4M3 block scales and an fp32 tensor scale) run weight-only as well.
  *
  * Conventions shared by every entry point
  *   - Every array pointer is DEVICE memory owned by the caller. The library keeps no
@@ -220,6 +221,35 @@ w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scal
  */
 w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
                         int N, int K, w4a16_stream_t stream);
+
+/*
+ * NVFP4 weights with 16-bit activations ("Hardware-invariant NVFP4 progress report 1", "The
+ * NVFP4 layout"; "Low-Precision Kernels ...", Step 6): E2M1 codes (values 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6 and their negatives), one E4M3 scale per 16 weights along K and one fp32 scale
+ * per tensor; w_hat = e2m1(q) * e4m3(s_b) * S (4.5 bits per weight).
+ *
+ * nvfp4_quantize -- w fp32 [N, K] -> codes uint8 [N, K/2] (byte j of a row: k = 2j in the
+ *   low nibble, 2j + 1 in the high one), scales E4M3 bytes [N, K/16], tensor_scale one fp32:
+ *   S = fl(amax / 2688) (1 for an all-zero tensor); a block's scale is the smallest E4M3
+ *   value >= fl(amax_b / fl(6 S)) (at most 448), so that the block's largest weight is not
+ *   clipped; codes are fl(w / fl(s_b S)) rounded to the nearest E2M1 value, ties to the even
+ *   code, saturating at 6; a block of zeros stores scale 0 and codes 0. Four launches on
+ *   `stream` (the tensor_scale word holds amax in between). Requires N > 0, K > 0,
+ *   K % 128 == 0.
+ */
+w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                            float* tensor_scale, w4a16_stream_t stream);
+
+/*
+ * nvfp4_gemv -- y[n] = S * sum_b e4m3(s[n, b]) * sum_j e2m1(q[n, 16 b + j]) x[16 b + j]:
+ *   x bf16 [K]; codes, scales, tensor_scale as above (device memory); y bf16 [N] (fp32
+ *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. x is held
+ *   in shared memory: K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0,
+ *   K > 0, K % 128 == 0.
+ */
+w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                        const float* tensor_scale, uint16_t* y, int N, int K,
+                        w4a16_stream_t stream);
 
 /*
  * w4a16_device_status -- synchronizes `stream`, then reads and clears the current

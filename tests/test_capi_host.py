@@ -42,6 +42,8 @@ def lib(cuda_lib):
     lib.w4a16zp_matmul.argtypes = [P, P, P, P, P, I, I, I, I, P, S, P]
     lib.w8a16_quantize.argtypes = [P, I, I, P, P, P]
     lib.w8a16_gemv.argtypes = [P, P, P, P, I, I, P]
+    lib.nvfp4_quantize.argtypes = [P, I, I, P, P, P, P]
+    lib.nvfp4_gemv.argtypes = [P, P, P, P, P, I, I, P]
     return lib
 
 
@@ -50,7 +52,8 @@ def test_header_declares_the_boundary():
     for required in ("w4a16_quantize", "w4a16_pack", "w4a16_matmul", "q4b32_gemv",
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
                      "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
-                     "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv"):
+                     "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
+                     "nvfp4_gemv"):
         assert required in names
 
 
@@ -129,6 +132,17 @@ def test_w8a16_rejects_bad_arguments_on_host(lib):
     assert g(A, A, A, B, 4, 96, None) == INVALID         # K % 64
     assert g(A, A, A, B, 4, 64 * 4096, None) == UNSUPPORTED  # x does not fit shared memory
     assert g(A + 2, A, A, B, 4, 256, None) == MISALIGNED
+
+
+def test_nvfp4_rejects_bad_arguments_on_host(lib):
+    q, g = lib.nvfp4_quantize, lib.nvfp4_gemv
+    assert q(A, 4, 256, A, A, None, None) == INVALID
+    assert q(A, 4, 192, A, A, A, None) == INVALID          # K % 128
+    assert q(A, 4, 256, A, A, A + 4, None) == MISALIGNED
+    assert g(A, A, A, A, None, 4, 256, None) == INVALID
+    assert g(A, A, A, A, B, 4, 64, None) == INVALID        # K % 128
+    assert g(A, A, A, A, B, 4, 128 * 2048, None) == UNSUPPORTED
+    assert g(A, A, A + 1, A, B, 4, 256, None) == MISALIGNED
 
 
 def test_workspace_query_is_host_only(lib):

@@ -1,0 +1,107 @@
+"""NVFP4 weights with BF16 activations (E2M1 codes, E4M3 block scales of 16, one fp32 tensor
+scale) through the C ABI against the oracle.
+
+Quantize must match the oracle bit for bit (codes, block scales, tensor scale); the GEMV must
+meet |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k| on every output, at sizes spanning
+several 16-row tiles with a ragged last tile and at the full 14336 x 4096 layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemv_w4a16_group_gb300 as mod
+
+    return mod
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def special_weights(N, K, seed):
+    """Seeded N(0, 0.02^2) weights with 0.1 % outliers, plus a block of zeros, a block of
+    negative zeros, blocks of exact ties (x.25, x.75 and 2.5, 5 on the E2M1 grid) and a block
+    whose scale E4M3 would round down."""
+    w = workloads.weights(N, K, seed=seed, outlier_frac=0.001).numpy().copy()
+    if N >= 4 and K >= 64:
+        amax = float(np.abs(w).max())
+        S = np.float32(np.float32(amax) / np.float32(2688))
+        w[0, :16] = 0.0
+        w[0, 16:32] = -0.0
+        # a block whose largest |w| is 6 s_b with s_b = 0.25 S: quotients on the E2M1 grid
+        # and at its midpoints
+        grid = np.array([6, 2.5, 5, 0.25, 0.75, 1.25, 1.75, 3.5, -2.5, -5, -0.25, -6, 0, 1, 4, -1.5])
+        w[1, :16] = grid * 0.25 * S
+        w[2, :16] = np.linspace(-0.87, 0.87, 16) * 64 * S
+    return np.ascontiguousarray(w, dtype=np.float32)
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (100, 512), (1000, 4096), (7, 8192)])
+def test_nvfp4_quantize_bit_exact(w4, N, K):
+    w = special_weights(N, K, seed=N + K)
+    c_ref, s_ref, S_ref = oracle.nvfp4_quantize(w)
+    c, s, S = w4.nvfp4_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert S.cpu().numpy().view(np.uint32)[0] == np.float32(S_ref).view(np.uint32)
+    np.testing.assert_array_equal(s.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(c.cpu().numpy(), c_ref)
+
+
+def test_nvfp4_quantize_hand_worked_tensors(w4):
+    """The tensors of tests/golden/nvfp4_blocks.txt, each row repeated four times (K = 128)."""
+    import pins
+
+    for tag, rec in pins._records("nvfp4_blocks.txt"):
+        w = np.tile(pins._weights_from(rec), 4).reshape(1, -1).astype(np.float32)
+        c, s, S = w4.nvfp4_quantize(torch.from_numpy(w).cuda())
+        torch.cuda.synchronize()
+        assert S.cpu().numpy().view(np.uint32)[0] == int(rec["S"][0], 16), tag
+        assert [int(v) for v in s.cpu().numpy()[0, :2]] == [int(v, 16) for v in rec["scales"]], tag
+        assert [int(v) for v in c.cpu().numpy()[0, :16]] == [int(v, 16) for v in rec["bytes"]], tag
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (333, 1024), (1000, 4224), (4096, 4096),
+                                 (14336, 4096), (40, 65536)])
+def test_nvfp4_gemv_every_output(w4, N, K):
+    w = special_weights(N, K, seed=N * 5 + K)
+    c_np, s_np, S = oracle.nvfp4_quantize(w)
+    x = workloads.activations_bf16(1, K, seed=N)[0]
+    c, s = torch.from_numpy(c_np).cuda(), torch.from_numpy(s_np).cuda()
+    St = torch.tensor([S], dtype=torch.float32, device="cuda")
+    y = w4.nvfp4_gemv(x.cuda(), c, s, St)
+    y2 = w4.nvfp4_gemv(x.cuda(), c, s, St)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    y_ref, a_ref = oracle.nvfp4_gemv(bits(x), c_np, s_np, S)
+    yv = y.float().cpu().numpy()
+    ok = oracle.within_tolerance(yv, y_ref, a_ref)
+    if not ok.all():
+        bad = np.flatnonzero(~ok)[:5]
+        raise AssertionError(f"{int((~ok).sum())}/{ok.size} out of tolerance: "
+                             f"{[(int(n), float(yv[n]), float(y_ref[n])) for n in bad]}")
+
+
+def test_nvfp4_gemv_special_activations(w4):
+    """x with a zero chunk, a 2^20 range of magnitudes inside a chunk and a large value."""
+    N, K = 96, 1024
+    w = special_weights(N, K, seed=9)
+    c_np, s_np, S = oracle.nvfp4_quantize(w)
+    x = workloads.activations_bf16(1, K, seed=9)[0].clone()
+    x[:128] = 0
+    x[128:256] = x[128:256] * torch.logspace(-10, 10, 128, base=2.0).to(torch.bfloat16)
+    x[300] = 3.0e4
+    St = torch.tensor([S], dtype=torch.float32, device="cuda")
+    y = w4.nvfp4_gemv(x.cuda(), torch.from_numpy(c_np).cuda(), torch.from_numpy(s_np).cuda(), St)
+    torch.cuda.synchronize()
+    y_ref, a_ref = oracle.nvfp4_gemv(bits(x), c_np, s_np, S)
+    assert oracle.within_tolerance(y.float().cpu().numpy(), y_ref, a_ref).all()
