@@ -126,6 +126,7 @@ cudaError_t launch_q4b32_gemv_tc(const uint16_t* x, const uint8_t* codes, const 
 // W8A16 (symmetric per-row INT8): quantize, one CTA per row; GEMV, 16 rows per CTA with x
 // (2 K bytes) in shared memory. K % 64 == 0.
 uint32_t w8a16_smem_bytes(int K);
+int device_sm_count();  // SMs of the current device (cached per device)
 cudaError_t launch_w8a16_quantize(const float* w, int N, int K, int8_t* q, float* s,
                                   cudaStream_t stream);
 cudaError_t launch_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s, uint16_t* y,

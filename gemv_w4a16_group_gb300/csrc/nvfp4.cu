@@ -9,8 +9,9 @@
 // Codes: uint8 [N, K/2], byte j of a row holding k = 2j (low nibble) and 2j + 1; scales:
 // E4M3 bytes [N, K/16]; S: one fp32 in device memory.
 //
-// GEMV (M = 1). Same split as the W8A16 GEMV: a CTA owns 16 rows, its 8 warps take the
-// 128-k chunks in turn; lane (g, c) loads the 32 codes k = 128 ch + 32 c .. + 31 of rows g and
+// GEMV (M = 1). Same split as the W8A16 GEMV: a CTA works on 16 rows at a time (at most three
+// CTAs per SM, looping over row tiles), its 8 warps take the 128-k chunks in turn with four
+// chunks' loads in flight; lane (g, c) loads the 32 codes k = 128 ch + 32 c .. + 31 of rows g and
 // g + 8 with one 16-byte load each. sm_103a converts a byte of two E2M1 codes to an FP16 pair
 // in one instruction (cvt.rn.f16x2.e2m1x2), and the block scale multiplies the pair in FP16
 // exactly (an E2M1 value has 2 significant bits and an E4M3 scale 4, and their product lies
@@ -33,7 +34,8 @@ namespace {
 
 constexpr int kNvThreads = 256;
 constexpr int kNvWarps = kNvThreads / 32;
-constexpr int kNvUnroll = 1;  // two chunks in flight spill at the 48 registers of 5 CTAs/SM
+constexpr int kNvUnroll = 4;     // chunks whose loads a warp has in flight together
+constexpr int kNvMinBlocks = 3;  // resident CTAs per SM (79 registers a thread)
 
 __device__ __forceinline__ uint4 ldg_stream128_nv(const void* p) {
   uint4 v;
@@ -89,7 +91,7 @@ struct NvLayout {
   }
 };
 
-__global__ void __launch_bounds__(kNvThreads, 5)
+__global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
     nvfp4_gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                       const uint8_t* __restrict__ scales, const float* __restrict__ tensor_scale,
                       uint16_t* __restrict__ y, int N, int K) {
@@ -145,68 +147,72 @@ __global__ void __launch_bounds__(kNvThreads, 5)
   __syncthreads();
 
   const int g = lane >> 2, c = lane & 3;
-  const int n0 = blockIdx.x * 16;
-  const size_t ra = static_cast<size_t>(min(n0 + g, N - 1));
-  const size_t rb = static_cast<size_t>(min(n0 + g + 8, N - 1));
-  const uint8_t* pa = codes + ra * (K / 2) + 16 * c;
-  const uint8_t* pb = codes + rb * (K / 2) + 16 * c;
-  const uint8_t* qa = scales + ra * (K / 16) + 2 * c;
-  const uint8_t* qb = scales + rb * (K / 16) + 2 * c;
-  const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(64 * c);
-  float acc_a = 0.f, acc_b = 0.f;
-  for (int ch0 = warp; ch0 < chunks; ch0 += kNvWarps * kNvUnroll) {
-    uint4 wa[kNvUnroll], wb[kNvUnroll];
-    uint32_t sa[kNvUnroll], sb[kNvUnroll];
-#pragma unroll
-    for (int u = 0; u < kNvUnroll; ++u) {
-      const int ch = ch0 + u * kNvWarps;
-      if (ch < chunks) {
-        wa[u] = ldg_stream128_nv(pa + 64 * static_cast<size_t>(ch));
-        wb[u] = ldg_stream128_nv(pb + 64 * static_cast<size_t>(ch));
-        sa[u] = __ldg(reinterpret_cast<const unsigned short*>(qa + 8 * static_cast<size_t>(ch)));
-        sb[u] = __ldg(reinterpret_cast<const unsigned short*>(qb + 8 * static_cast<size_t>(ch)));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kNvUnroll; ++u) {
-      const int ch = ch0 + u * kNvWarps;
-      if (ch >= chunks) break;  // warp-uniform
-      // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
-      const uint32_t s2a = e4m3x2_f16(sa[u]), s2b = e4m3x2_f16(sb[u]);
-      const uint32_t sa_lo = __byte_perm(s2a, 0u, 0x1010), sa_hi = __byte_perm(s2a, 0u, 0x3232);
-      const uint32_t sb_lo = __byte_perm(s2b, 0u, 0x1010), sb_hi = __byte_perm(s2b, 0u, 0x3232);
-      const uint32_t ra4[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
-      const uint32_t rb4[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {  // word wi: MMAs 2 wi and 2 wi + 1
-        uint32_t pa4[4], pb4[4];
-        e2m1_pairs_f16(ra4[wi], pa4);
-        e2m1_pairs_f16(rb4[wi], pb4);
-        const uint32_t ska = wi < 2 ? sa_lo : sa_hi, skb = wi < 2 ? sb_lo : sb_hi;
-        const uint4 xb = lds128(xlane + 256u * ch + 16u * wi);  // k = 32 c + 8 wi .. + 7
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t a0 = hmul2_bits(pa4[2 * h], ska), a2 = hmul2_bits(pa4[2 * h + 1], ska);
-          const uint32_t a1 = hmul2_bits(pb4[2 * h], skb), a3 = hmul2_bits(pb4[2 * h + 1], skb);
-          mma_f16_16816(d, a0, a1, a2, a3, h ? xb.z : xb.x, h ? xb.w : xb.y);
+  const int ntiles = (N + 15) / 16;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // uniform per CTA
+    const int n0 = tile * 16;
+    const size_t ra = static_cast<size_t>(min(n0 + g, N - 1));
+    const size_t rb = static_cast<size_t>(min(n0 + g + 8, N - 1));
+    const uint8_t* pa = codes + ra * (K / 2) + 16 * c;
+    const uint8_t* pb = codes + rb * (K / 2) + 16 * c;
+    const uint8_t* qa = scales + ra * (K / 16) + 2 * c;
+    const uint8_t* qb = scales + rb * (K / 16) + 2 * c;
+    const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(64 * c);
+    float acc_a = 0.f, acc_b = 0.f;
+    for (int ch0 = warp; ch0 < chunks; ch0 += kNvWarps * kNvUnroll) {
+      uint4 wa[kNvUnroll], wb[kNvUnroll];
+      uint32_t sa[kNvUnroll], sb[kNvUnroll];
+  #pragma unroll
+      for (int u = 0; u < kNvUnroll; ++u) {
+        const int ch = ch0 + u * kNvWarps;
+        if (ch < chunks) {
+          wa[u] = ldg_stream128_nv(pa + 64 * static_cast<size_t>(ch));
+          wb[u] = ldg_stream128_nv(pb + 64 * static_cast<size_t>(ch));
+          sa[u] = __ldg(reinterpret_cast<const unsigned short*>(qa + 8 * static_cast<size_t>(ch)));
+          sb[u] = __ldg(reinterpret_cast<const unsigned short*>(qb + 8 * static_cast<size_t>(ch)));
         }
       }
-      const float u2 = cst[ch];
-      acc_a = fmaf(u2, d[0], acc_a);
-      acc_b = fmaf(u2, d[2], acc_b);
+  #pragma unroll
+      for (int u = 0; u < kNvUnroll; ++u) {
+        const int ch = ch0 + u * kNvWarps;
+        if (ch >= chunks) break;  // warp-uniform
+        // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
+        const uint32_t s2a = e4m3x2_f16(sa[u]), s2b = e4m3x2_f16(sb[u]);
+        const uint32_t sa_lo = __byte_perm(s2a, 0u, 0x1010), sa_hi = __byte_perm(s2a, 0u, 0x3232);
+        const uint32_t sb_lo = __byte_perm(s2b, 0u, 0x1010), sb_hi = __byte_perm(s2b, 0u, 0x3232);
+        const uint32_t ra4[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t rb4[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {  // word wi: MMAs 2 wi and 2 wi + 1
+          uint32_t pa4[4], pb4[4];
+          e2m1_pairs_f16(ra4[wi], pa4);
+          e2m1_pairs_f16(rb4[wi], pb4);
+          const uint32_t ska = wi < 2 ? sa_lo : sa_hi, skb = wi < 2 ? sb_lo : sb_hi;
+          const uint4 xb = lds128(xlane + 256u * ch + 16u * wi);  // k = 32 c + 8 wi .. + 7
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a0 = hmul2_bits(pa4[2 * h], ska), a2 = hmul2_bits(pa4[2 * h + 1], ska);
+            const uint32_t a1 = hmul2_bits(pb4[2 * h], skb), a3 = hmul2_bits(pb4[2 * h + 1], skb);
+            mma_f16_16816(d, a0, a1, a2, a3, h ? xb.z : xb.x, h ? xb.w : xb.y);
+          }
+        }
+        const float u2 = cst[ch];
+        acc_a = fmaf(u2, d[0], acc_a);
+        acc_b = fmaf(u2, d[2], acc_b);
+      }
     }
-  }
-  if (c == 0) {
-    red[warp * 16 + g] = acc_a;
-    red[warp * 16 + g + 8] = acc_b;
-  }
-  __syncthreads();
-  if (tid < 16 && n0 + tid < N) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kNvWarps; ++w) v += red[w * 16 + tid];
-    y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * __ldg(tensor_scale)));
+    if (c == 0) {
+      red[warp * 16 + g] = acc_a;
+      red[warp * 16 + g + 8] = acc_b;
+    }
+    __syncthreads();
+    if (tid < 16 && n0 + tid < N) {
+      float v = 0.f;
+  #pragma unroll
+      for (int w = 0; w < kNvWarps; ++w) v += red[w * 16 + tid];
+      y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * __ldg(tensor_scale)));
+    }
+    __syncthreads();  // red is rewritten by the next tile
   }
 }
 
@@ -227,6 +233,11 @@ __global__ void __launch_bounds__(kNvThreads)
   if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));  // m >= 0
 }
 
+// Value of a non-negative E4M3 code (exact in FP16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_f16(code) & 0xFFFFu)));
+}
+
 __device__ __forceinline__ float tensor_scale_of(float amax) {
   return amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
 }
@@ -236,7 +247,7 @@ __device__ __forceinline__ uint32_t e4m3_ceil(float v) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
   uint32_t code = r & 0xFFu;
-  const float back = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_f16(code) & 0xFFFFu)));
+  const float back = e4m3_to_f32(code);
   if (back < v && code < 0x7Eu) ++code;
   return code;
 }
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(kNvThreads)
   uint32_t sc = 0u, packed = 0u;
   if (bmax > 0.f) {
     sc = e4m3_ceil(__fdiv_rn(bmax, d6));
-    const float sval = __half2float(__ushort_as_half(static_cast<unsigned short>(e4m3x2_f16(sc) & 0xFFFFu)));
+    const float sval = e4m3_to_f32(sc);
     const float den = __fmul_rn(sval, S);
     const uint32_t b0 = e2m1x2_rn(__fdiv_rn(v.y, den), __fdiv_rn(v.x, den));
     const uint32_t b1 = e2m1x2_rn(__fdiv_rn(v.w, den), __fdiv_rn(v.z, den));
@@ -308,7 +319,11 @@ cudaError_t launch_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uin
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  nvfp4_gemv_kernel<<<static_cast<unsigned>((N + 15) / 16), kNvThreads, smem, stream>>>(
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int tiles = (N + 15) / 16;
+  const int grid = tiles < sms * kNvMinBlocks ? tiles : sms * kNvMinBlocks;
+  nvfp4_gemv_kernel<<<static_cast<unsigned>(grid), kNvThreads, smem, stream>>>(
       x, codes, scales, tensor_scale, y, N, K);
   return cudaGetLastError();
 }

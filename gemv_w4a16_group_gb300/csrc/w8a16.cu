@@ -10,10 +10,12 @@
 // place two bytes each under the FP16 exponent of 1024, giving 1152 + q exactly), and the
 // products run on the tensor pipe (mma.sync m16n8k16, FP16 x FP16 -> fp32).
 //
-// Work split. A CTA owns 16 rows (the MMA's 16 rows); its 8 warps take the 64-k chunks of
-// K in turn (warp w: chunks w, w + 8, ...). Lane (g, c) = (lane / 4, lane % 4) loads the 16
-// codes k = 64 ch + 16 c .. + 15 of rows g and g + 8 (16 bytes each, a warp reads 64
-// contiguous bytes of 16 rows). The MMA adds over k in any order as long as A and B agree:
+// Work split. A CTA works on 16 rows at a time (the MMA's 16 rows), its 8 warps taking the
+// 64-k chunks of K in turn (warp w: chunks w, w + 8, ...), four chunks' loads in flight per
+// warp; the grid is at most three CTAs per SM, each looping over row tiles, so that x is
+// converted once per CTA and the SMs' tile counts differ by at most one. Lane (g, c) =
+// (lane / 4, lane % 4) loads the 16 codes k = 64 ch + 16 c .. + 15 of rows g and g + 8 (16
+// bytes each, a warp reads 64 contiguous bytes of 16 rows). The MMA adds over k in any order as long as A and B agree:
 // in MMA i of a chunk, k-slots (2c, 2c + 1, 2c + 8, 2c + 9) of lane c's fragments hold
 // k = 64 ch + 16 c + 4 i + (0, 1, 2, 3), so the B fragment of lane (g, c) is the same 16
 // consecutive x values, read from shared memory in natural order.
@@ -32,7 +34,8 @@ namespace {
 
 constexpr int kW8Threads = 256;
 constexpr int kW8Warps = kW8Threads / 32;
-constexpr int kW8Unroll = 2;  // chunks whose loads a warp has in flight together
+constexpr int kW8Unroll = 4;  // chunks whose loads a warp has in flight together
+constexpr int kW8MinBlocks = 3;  // resident CTAs per SM (72 registers a thread)
 
 __device__ __forceinline__ uint4 ldg_stream128(const void* p) {
   uint4 v;
@@ -60,7 +63,7 @@ struct W8Layout {
   }
 };
 
-__global__ void __launch_bounds__(kW8Threads, 6)
+__global__ void __launch_bounds__(kW8Threads, kW8MinBlocks)
     w8a16_gemv_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ q,
                       const float* __restrict__ s, uint16_t* __restrict__ y, int N, int K) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -120,53 +123,57 @@ __global__ void __launch_bounds__(kW8Threads, 6)
   __syncthreads();
 
   const int g = lane >> 2, c = lane & 3;
-  const int n0 = blockIdx.x * 16;
-  const int8_t* pa = q + static_cast<size_t>(min(n0 + g, N - 1)) * K + 16 * c;
-  const int8_t* pb = q + static_cast<size_t>(min(n0 + g + 8, N - 1)) * K + 16 * c;
-  const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(32 * c);
-  float acc_a = 0.f, acc_b = 0.f;  // rows g and g + 8
-  for (int ch0 = warp; ch0 < chunks; ch0 += kW8Warps * kW8Unroll) {
-    uint4 wa[kW8Unroll], wb[kW8Unroll];
-#pragma unroll
-    for (int u = 0; u < kW8Unroll; ++u) {
-      const int ch = ch0 + u * kW8Warps;
-      if (ch < chunks) {
-        wa[u] = ldg_stream128(pa + 64 * static_cast<size_t>(ch));
-        wb[u] = ldg_stream128(pb + 64 * static_cast<size_t>(ch));
+  const int ntiles = (N + 15) / 16;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // uniform per CTA
+    const int n0 = tile * 16;
+    const int8_t* pa = q + static_cast<size_t>(min(n0 + g, N - 1)) * K + 16 * c;
+    const int8_t* pb = q + static_cast<size_t>(min(n0 + g + 8, N - 1)) * K + 16 * c;
+    const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(32 * c);
+    float acc_a = 0.f, acc_b = 0.f;  // rows g and g + 8
+    for (int ch0 = warp; ch0 < chunks; ch0 += kW8Warps * kW8Unroll) {
+      uint4 wa[kW8Unroll], wb[kW8Unroll];
+  #pragma unroll
+      for (int u = 0; u < kW8Unroll; ++u) {
+        const int ch = ch0 + u * kW8Warps;
+        if (ch < chunks) {
+          wa[u] = ldg_stream128(pa + 64 * static_cast<size_t>(ch));
+          wb[u] = ldg_stream128(pb + 64 * static_cast<size_t>(ch));
+        }
+      }
+  #pragma unroll
+      for (int u = 0; u < kW8Unroll; ++u) {
+        const int ch = ch0 + u * kW8Warps;
+        if (ch >= chunks) break;  // warp-uniform
+        const uint4 x0 = lds128(xlane + 128u * ch), x1 = lds128(xlane + 128u * ch + 16u);
+        const uint32_t xa[4][2] = {{x0.x, x0.y}, {x0.z, x0.w}, {x1.x, x1.y}, {x1.z, x1.w}};
+        const uint32_t ra[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t rb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t a0, a2, a1, a3;
+          int8_pairs_f16(ra[i], a0, a2);  // row g: k-slots (2c, 2c + 1), (2c + 8, 2c + 9)
+          int8_pairs_f16(rb[i], a1, a3);  // row g + 8
+          mma_f16_16816(d, a0, a1, a2, a3, xa[i][0], xa[i][1]);
+        }
+        // every B column holds x, so d[0] (row g) and d[2] (row g + 8) are the chunk's sums
+        const float2 cc = cst[ch];
+        acc_a = fmaf(cc.y, d[0] - cc.x, acc_a);
+        acc_b = fmaf(cc.y, d[2] - cc.x, acc_b);
       }
     }
-#pragma unroll
-    for (int u = 0; u < kW8Unroll; ++u) {
-      const int ch = ch0 + u * kW8Warps;
-      if (ch >= chunks) break;  // warp-uniform
-      const uint4 x0 = lds128(xlane + 128u * ch), x1 = lds128(xlane + 128u * ch + 16u);
-      const uint32_t xa[4][2] = {{x0.x, x0.y}, {x0.z, x0.w}, {x1.x, x1.y}, {x1.z, x1.w}};
-      const uint32_t ra[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
-      const uint32_t rb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t a0, a2, a1, a3;
-        int8_pairs_f16(ra[i], a0, a2);  // row g: k-slots (2c, 2c + 1), (2c + 8, 2c + 9)
-        int8_pairs_f16(rb[i], a1, a3);  // row g + 8
-        mma_f16_16816(d, a0, a1, a2, a3, xa[i][0], xa[i][1]);
-      }
-      // every B column holds x, so d[0] (row g) and d[2] (row g + 8) are the chunk's sums
-      const float2 cc = cst[ch];
-      acc_a = fmaf(cc.y, d[0] - cc.x, acc_a);
-      acc_b = fmaf(cc.y, d[2] - cc.x, acc_b);
+    if (c == 0) {
+      red[warp * 16 + g] = acc_a;
+      red[warp * 16 + g + 8] = acc_b;
     }
-  }
-  if (c == 0) {
-    red[warp * 16 + g] = acc_a;
-    red[warp * 16 + g + 8] = acc_b;
-  }
-  __syncthreads();
-  if (tid < 16 && n0 + tid < N) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kW8Warps; ++w) v += red[w * 16 + tid];
-    y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * s[n0 + tid]));
+    __syncthreads();
+    if (tid < 16 && n0 + tid < N) {
+      float v = 0.f;
+  #pragma unroll
+      for (int w = 0; w < kW8Warps; ++w) v += red[w * 16 + tid];
+      y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * s[n0 + tid]));
+    }
+    __syncthreads();  // red is rewritten by the next tile
   }
 }
 
@@ -217,6 +224,14 @@ __global__ void __launch_bounds__(kW8Threads)
 
 }  // namespace
 
+int device_sm_count() {
+  static int count[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (count[dev] == 0) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
+  return count[dev];
+}
+
 uint32_t w8a16_smem_bytes(int K) { return W8Layout(K).total; }
 
 cudaError_t launch_w8a16_quantize(const float* w, int N, int K, int8_t* q, float* s,
@@ -233,8 +248,11 @@ cudaError_t launch_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s
         set_max_dynamic_smem(reinterpret_cast<const void*>(w8a16_gemv_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  const unsigned grid = static_cast<unsigned>((N + 15) / 16);
-  w8a16_gemv_kernel<<<grid, kW8Threads, smem, stream>>>(x, q, s, y, N, K);
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int tiles = (N + 15) / 16;
+  const int grid = tiles < sms * kW8MinBlocks ? tiles : sms * kW8MinBlocks;
+  w8a16_gemv_kernel<<<static_cast<unsigned>(grid), kW8Threads, smem, stream>>>(x, q, s, y, N, K);
   return cudaGetLastError();
 }
 
