@@ -10,8 +10,8 @@
 // E4M3 bytes [N, K/16]; S: one fp32 in device memory.
 //
 // GEMV (M = 1). Same split as the W8A16 GEMV: a CTA works on 16 rows at a time (at most three
-// CTAs per SM, looping over row tiles), its 8 warps take the 128-k chunks in turn, each through
-// its own cp.async ring in shared memory with six chunks in flight; lane (g, c) loads the 32 codes k = 128 ch + 32 c .. + 31 of rows g and
+// CTAs per SM, looping over row tiles), its 8 warps take the 128-k chunks in turn with four
+// chunks' loads in flight; lane (g, c) loads the 32 codes k = 128 ch + 32 c .. + 31 of rows g and
 // g + 8 with one 16-byte load each. sm_103a converts a byte of two E2M1 codes to an FP16 pair
 // in one instruction (cvt.rn.f16x2.e2m1x2), and the block scale multiplies the pair in FP16
 // exactly (an E2M1 value has 2 significant bits and an E4M3 scale 4, and their product lies
@@ -34,11 +34,16 @@ namespace {
 
 constexpr int kNvThreads = 256;
 constexpr int kNvWarps = kNvThreads / 32;
-constexpr int kNvStages = 6;     // chunks in flight per warp (per-warp cp.async ring)
-constexpr int kNvMinBlocks = 3;  // resident CTAs per SM
-// One ring stage of a warp: codes of rows g and g + 8 (16 bytes per lane each), then the
-// 4-byte word holding each lane's two block scales of each row.
-constexpr uint32_t kNvStageBytes = 2u * 32u * 16u + 2u * 32u * 4u;
+constexpr int kNvUnroll = 4;     // chunks whose loads a warp has in flight together
+constexpr int kNvMinBlocks = 3;  // resident CTAs per SM (79 registers a thread)
+
+__device__ __forceinline__ uint4 ldg_stream128_nv(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 // FP16 pairs of the four bytes of `w` (byte j -> (code 2j, code 2j + 1)).
 __device__ __forceinline__ void e2m1_pairs_f16(uint32_t w, uint32_t (&p)[4]) {
@@ -78,20 +83,13 @@ __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
 }
 
 struct NvLayout {
-  uint32_t cst_off, red_off, ring_off, total;
+  uint32_t cst_off, red_off, total;
   __host__ __device__ explicit NvLayout(int K) {
     cst_off = static_cast<uint32_t>(K) * 2u;  // x as FP16 [K]
     red_off = cst_off + static_cast<uint32_t>(K / 128) * 4u;  // 2^-e per chunk
-    ring_off = (red_off + kNvWarps * 16u * 4u + 15u) & ~15u;  // warp partials, then rings
-    total = ring_off + kNvWarps * kNvStages * kNvStageBytes;
+    total = red_off + kNvWarps * 16u * 4u;
   }
 };
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 
 __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
     nvfp4_gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
@@ -150,70 +148,58 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
 
   const int g = lane >> 2, c = lane & 3;
   const int ntiles = (N + 15) / 16;
-  // This warp's chunks of a tile (warp, warp + 8, ...) and this CTA's tiles (blockIdx.x,
-  // + gridDim.x, ...): item j = (tile j / mine, chunk j % mine) of one stream per warp.
-  const int mine = warp < chunks ? (chunks - 1 - warp) / kNvWarps + 1 : 0;
-  const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
-                           ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
-  const int items = mine * my_tiles;
-  const uint32_t ring = smem_addr(smem + L.ring_off) + static_cast<uint32_t>(warp) * kNvStages * kNvStageBytes;
-  auto issue = [&](int j) {  // copies of item j into stage j % kNvStages
-    const int t = j / mine, ch = warp + (j - t * mine) * kNvWarps;
-    const int n0 = (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * 16;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // uniform per CTA
+    const int n0 = tile * 16;
     const size_t ra = static_cast<size_t>(min(n0 + g, N - 1));
     const size_t rb = static_cast<size_t>(min(n0 + g + 8, N - 1));
-    const uint32_t st = ring + static_cast<uint32_t>(j % kNvStages) * kNvStageBytes;
-    const size_t ko = 64 * static_cast<size_t>(ch) + 16 * c;
-    cp_async16(st + 16u * lane, codes + ra * (K / 2) + ko);
-    cp_async16(st + 512u + 16u * lane, codes + rb * (K / 2) + ko);
-    const size_t so = 8 * static_cast<size_t>(ch) + 4 * (c >> 1);  // scales 2c, 2c + 1 inside
-    cp_async4(st + 1024u + 4u * lane, scales + ra * (K / 16) + so);
-    cp_async4(st + 1152u + 4u * lane, scales + rb * (K / 16) + so);
-  };
-#pragma unroll
-  for (int j = 0; j < kNvStages - 1; ++j) {
-    if (j < items) issue(j);
-    cp_async_commit();
-  }
-  const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(64 * c);
-  const int shift = 16 * (c & 1);
-  int j = 0;
-  for (int t = 0; t < my_tiles; ++t) {  // uniform per CTA
-    const int n0 = (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * 16;
+    const uint8_t* pa = codes + ra * (K / 2) + 16 * c;
+    const uint8_t* pb = codes + rb * (K / 2) + 16 * c;
+    const uint8_t* qa = scales + ra * (K / 16) + 2 * c;
+    const uint8_t* qb = scales + rb * (K / 16) + 2 * c;
+    const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(64 * c);
     float acc_a = 0.f, acc_b = 0.f;
-    for (int ci = 0; ci < mine; ++ci, ++j) {
-      if (j + kNvStages - 1 < items) issue(j + kNvStages - 1);
-      cp_async_commit();
-      cp_async_wait<kNvStages - 1>();  // item j has landed (this lane's own copies)
-      const int ch = warp + ci * kNvWarps;
-      const uint32_t st = ring + static_cast<uint32_t>(j % kNvStages) * kNvStageBytes;
-      const uint4 wa = lds128(st + 16u * lane), wb = lds128(st + 512u + 16u * lane);
-      // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
-      const uint32_t s2a = e4m3x2_f16((lds32(st + 1024u + 4u * lane) >> shift) & 0xFFFFu);
-      const uint32_t s2b = e4m3x2_f16((lds32(st + 1152u + 4u * lane) >> shift) & 0xFFFFu);
-      const uint32_t sa_lo = __byte_perm(s2a, 0u, 0x1010), sa_hi = __byte_perm(s2a, 0u, 0x3232);
-      const uint32_t sb_lo = __byte_perm(s2b, 0u, 0x1010), sb_hi = __byte_perm(s2b, 0u, 0x3232);
-      const uint32_t ra4[4] = {wa.x, wa.y, wa.z, wa.w};
-      const uint32_t rb4[4] = {wb.x, wb.y, wb.z, wb.w};
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {  // word wi: MMAs 2 wi and 2 wi + 1
-        uint32_t pa4[4], pb4[4];
-        e2m1_pairs_f16(ra4[wi], pa4);
-        e2m1_pairs_f16(rb4[wi], pb4);
-        const uint32_t ska = wi < 2 ? sa_lo : sa_hi, skb = wi < 2 ? sb_lo : sb_hi;
-        const uint4 xb = lds128(xlane + 256u * ch + 16u * wi);  // k = 32 c + 8 wi .. + 7
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t a0 = hmul2_bits(pa4[2 * h], ska), a2 = hmul2_bits(pa4[2 * h + 1], ska);
-          const uint32_t a1 = hmul2_bits(pb4[2 * h], skb), a3 = hmul2_bits(pb4[2 * h + 1], skb);
-          mma_f16_16816(d, a0, a1, a2, a3, h ? xb.z : xb.x, h ? xb.w : xb.y);
+    for (int ch0 = warp; ch0 < chunks; ch0 += kNvWarps * kNvUnroll) {
+      uint4 wa[kNvUnroll], wb[kNvUnroll];
+      uint32_t sa[kNvUnroll], sb[kNvUnroll];
+  #pragma unroll
+      for (int u = 0; u < kNvUnroll; ++u) {
+        const int ch = ch0 + u * kNvWarps;
+        if (ch < chunks) {
+          wa[u] = ldg_stream128_nv(pa + 64 * static_cast<size_t>(ch));
+          wb[u] = ldg_stream128_nv(pb + 64 * static_cast<size_t>(ch));
+          sa[u] = __ldg(reinterpret_cast<const unsigned short*>(qa + 8 * static_cast<size_t>(ch)));
+          sb[u] = __ldg(reinterpret_cast<const unsigned short*>(qb + 8 * static_cast<size_t>(ch)));
         }
       }
-      const float u2 = cst[ch];
-      acc_a = fmaf(u2, d[0], acc_a);
-      acc_b = fmaf(u2, d[2], acc_b);
+  #pragma unroll
+      for (int u = 0; u < kNvUnroll; ++u) {
+        const int ch = ch0 + u * kNvWarps;
+        if (ch >= chunks) break;  // warp-uniform
+        // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
+        const uint32_t s2a = e4m3x2_f16(sa[u]), s2b = e4m3x2_f16(sb[u]);
+        const uint32_t sa_lo = __byte_perm(s2a, 0u, 0x1010), sa_hi = __byte_perm(s2a, 0u, 0x3232);
+        const uint32_t sb_lo = __byte_perm(s2b, 0u, 0x1010), sb_hi = __byte_perm(s2b, 0u, 0x3232);
+        const uint32_t ra4[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t rb4[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {  // word wi: MMAs 2 wi and 2 wi + 1
+          uint32_t pa4[4], pb4[4];
+          e2m1_pairs_f16(ra4[wi], pa4);
+          e2m1_pairs_f16(rb4[wi], pb4);
+          const uint32_t ska = wi < 2 ? sa_lo : sa_hi, skb = wi < 2 ? sb_lo : sb_hi;
+          const uint4 xb = lds128(xlane + 256u * ch + 16u * wi);  // k = 32 c + 8 wi .. + 7
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a0 = hmul2_bits(pa4[2 * h], ska), a2 = hmul2_bits(pa4[2 * h + 1], ska);
+            const uint32_t a1 = hmul2_bits(pb4[2 * h], skb), a3 = hmul2_bits(pb4[2 * h + 1], skb);
+            mma_f16_16816(d, a0, a1, a2, a3, h ? xb.z : xb.x, h ? xb.w : xb.y);
+          }
+        }
+        const float u2 = cst[ch];
+        acc_a = fmaf(u2, d[0], acc_a);
+        acc_b = fmaf(u2, d[2], acc_b);
+      }
     }
     if (c == 0) {
       red[warp * 16 + g] = acc_a;
@@ -222,7 +208,7 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
     __syncthreads();
     if (tid < 16 && n0 + tid < N) {
       float v = 0.f;
-#pragma unroll
+  #pragma unroll
       for (int w = 0; w < kNvWarps; ++w) v += red[w * 16 + tid];
       y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * __ldg(tensor_scale)));
     }
@@ -333,14 +319,10 @@ cudaError_t launch_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uin
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  // resident CTAs per SM: the register bound, and what shared memory allows
-  int per_sm = kNvMinBlocks;
-  const int by_smem = static_cast<int>((228u * 1024u) / (smem + 1024u));
-  if (by_smem < per_sm) per_sm = by_smem < 1 ? 1 : by_smem;
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int tiles = (N + 15) / 16;
-  const int grid = tiles < sms * per_sm ? tiles : sms * per_sm;
+  const int grid = tiles < sms * kNvMinBlocks ? tiles : sms * kNvMinBlocks;
   nvfp4_gemv_kernel<<<static_cast<unsigned>(grid), kNvThreads, smem, stream>>>(
       x, codes, scales, tensor_scale, y, N, K);
   return cudaGetLastError();

@@ -11,8 +11,8 @@
 // products run on the tensor pipe (mma.sync m16n8k16, FP16 x FP16 -> fp32).
 //
 // Work split. A CTA works on 16 rows at a time (the MMA's 16 rows), its 8 warps taking the
-// 64-k chunks of K in turn (warp w: chunks w, w + 8, ...); each warp streams its chunks through
-// its own ring of shared memory with cp.async, eight chunks in flight; the grid is at most three CTAs per SM, each looping over row tiles, so that x is
+// 64-k chunks of K in turn (warp w: chunks w, w + 8, ...), four chunks' loads in flight per
+// warp; the grid is at most three CTAs per SM, each looping over row tiles, so that x is
 // converted once per CTA and the SMs' tile counts differ by at most one. Lane (g, c) =
 // (lane / 4, lane % 4) loads the 16 codes k = 64 ch + 16 c .. + 15 of rows g and g + 8 (16
 // bytes each, a warp reads 64 contiguous bytes of 16 rows). The MMA adds over k in any order as long as A and B agree:
@@ -34,9 +34,16 @@ namespace {
 
 constexpr int kW8Threads = 256;
 constexpr int kW8Warps = kW8Threads / 32;
-constexpr int kW8Stages = 8;     // chunks in flight per warp (per-warp cp.async ring)
-constexpr int kW8MinBlocks = 3;  // resident CTAs per SM
-constexpr uint32_t kW8StageBytes = 2u * 32u * 16u;  // rows g and g + 8, 16 bytes per lane
+constexpr int kW8Unroll = 4;  // chunks whose loads a warp has in flight together
+constexpr int kW8MinBlocks = 3;  // resident CTAs per SM (72 registers a thread)
+
+__device__ __forceinline__ uint4 ldg_stream128(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 // FP16 pairs (1152 + q0, 1152 + q1) and (1152 + q2, 1152 + q3) of the four signed codes in
 // `w` (byte j = code j).
@@ -48,12 +55,11 @@ __device__ __forceinline__ void int8_pairs_f16(uint32_t w, uint32_t& lo, uint32_
 
 // Shared memory: x as FP16 [K] (2^e per chunk), per chunk {1152 X, 2^-e}, warp partials.
 struct W8Layout {
-  uint32_t cst_off, red_off, ring_off, total;
+  uint32_t cst_off, red_off, total;
   __host__ __device__ explicit W8Layout(int K) {
     cst_off = static_cast<uint32_t>(K) * 2u;
     red_off = cst_off + static_cast<uint32_t>(K / 64) * 8u;
-    ring_off = (red_off + kW8Warps * 16u * 4u + 15u) & ~15u;  // per-warp rings of codes
-    total = ring_off + kW8Warps * kW8Stages * kW8StageBytes;
+    total = red_off + kW8Warps * 16u * 4u;
   }
 };
 
@@ -118,55 +124,43 @@ __global__ void __launch_bounds__(kW8Threads, kW8MinBlocks)
 
   const int g = lane >> 2, c = lane & 3;
   const int ntiles = (N + 15) / 16;
-  // This warp's chunks of a tile (warp, warp + 8, ...) and this CTA's tiles (blockIdx.x,
-  // + gridDim.x, ...): item j = (tile j / mine, chunk j % mine) of one stream per warp.
-  const int mine = warp < chunks ? (chunks - 1 - warp) / kW8Warps + 1 : 0;
-  const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
-                           ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
-  const int items = mine * my_tiles;
-  const uint32_t ring = smem_addr(smem + L.ring_off) + static_cast<uint32_t>(warp) * kW8Stages * kW8StageBytes;
-  auto issue = [&](int j) {  // copies of item j into stage j % kW8Stages
-    const int t = j / mine, ch = warp + (j - t * mine) * kW8Warps;
-    const int n0 = (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * 16;
-    const size_t ko = 64 * static_cast<size_t>(ch) + 16 * c;
-    const uint32_t st = ring + static_cast<uint32_t>(j % kW8Stages) * kW8StageBytes;
-    cp_async16(st + 16u * lane, q + static_cast<size_t>(min(n0 + g, N - 1)) * K + ko);
-    cp_async16(st + 512u + 16u * lane, q + static_cast<size_t>(min(n0 + g + 8, N - 1)) * K + ko);
-  };
-#pragma unroll
-  for (int j = 0; j < kW8Stages - 1; ++j) {
-    if (j < items) issue(j);
-    cp_async_commit();
-  }
-  const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(32 * c);
-  int j = 0;
-  for (int t = 0; t < my_tiles; ++t) {  // uniform per CTA
-    const int n0 = (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * 16;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {  // uniform per CTA
+    const int n0 = tile * 16;
+    const int8_t* pa = q + static_cast<size_t>(min(n0 + g, N - 1)) * K + 16 * c;
+    const int8_t* pb = q + static_cast<size_t>(min(n0 + g + 8, N - 1)) * K + 16 * c;
+    const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(32 * c);
     float acc_a = 0.f, acc_b = 0.f;  // rows g and g + 8
-    for (int ci = 0; ci < mine; ++ci, ++j) {
-      if (j + kW8Stages - 1 < items) issue(j + kW8Stages - 1);
-      cp_async_commit();
-      cp_async_wait<kW8Stages - 1>();  // item j has landed (this lane's own copies)
-      const int ch = warp + ci * kW8Warps;
-      const uint32_t st = ring + static_cast<uint32_t>(j % kW8Stages) * kW8StageBytes;
-      const uint4 wa = lds128(st + 16u * lane), wb = lds128(st + 512u + 16u * lane);
-      const uint4 x0 = lds128(xlane + 128u * ch), x1 = lds128(xlane + 128u * ch + 16u);
-      const uint32_t xa[4][2] = {{x0.x, x0.y}, {x0.z, x0.w}, {x1.x, x1.y}, {x1.z, x1.w}};
-      const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w};
-      const uint32_t rb[4] = {wb.x, wb.y, wb.z, wb.w};
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t a0, a2, a1, a3;
-        int8_pairs_f16(ra[i], a0, a2);  // row g: k-slots (2c, 2c + 1), (2c + 8, 2c + 9)
-        int8_pairs_f16(rb[i], a1, a3);  // row g + 8
-        mma_f16_16816(d, a0, a1, a2, a3, xa[i][0], xa[i][1]);
+    for (int ch0 = warp; ch0 < chunks; ch0 += kW8Warps * kW8Unroll) {
+      uint4 wa[kW8Unroll], wb[kW8Unroll];
+  #pragma unroll
+      for (int u = 0; u < kW8Unroll; ++u) {
+        const int ch = ch0 + u * kW8Warps;
+        if (ch < chunks) {
+          wa[u] = ldg_stream128(pa + 64 * static_cast<size_t>(ch));
+          wb[u] = ldg_stream128(pb + 64 * static_cast<size_t>(ch));
+        }
       }
-      // every B column holds x, so d[0] (row g) and d[2] (row g + 8) are the chunk's sums
-      const float2 cc = cst[ch];
-      acc_a = fmaf(cc.y, d[0] - cc.x, acc_a);
-      acc_b = fmaf(cc.y, d[2] - cc.x, acc_b);
+  #pragma unroll
+      for (int u = 0; u < kW8Unroll; ++u) {
+        const int ch = ch0 + u * kW8Warps;
+        if (ch >= chunks) break;  // warp-uniform
+        const uint4 x0 = lds128(xlane + 128u * ch), x1 = lds128(xlane + 128u * ch + 16u);
+        const uint32_t xa[4][2] = {{x0.x, x0.y}, {x0.z, x0.w}, {x1.x, x1.y}, {x1.z, x1.w}};
+        const uint32_t ra[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t rb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t a0, a2, a1, a3;
+          int8_pairs_f16(ra[i], a0, a2);  // row g: k-slots (2c, 2c + 1), (2c + 8, 2c + 9)
+          int8_pairs_f16(rb[i], a1, a3);  // row g + 8
+          mma_f16_16816(d, a0, a1, a2, a3, xa[i][0], xa[i][1]);
+        }
+        // every B column holds x, so d[0] (row g) and d[2] (row g + 8) are the chunk's sums
+        const float2 cc = cst[ch];
+        acc_a = fmaf(cc.y, d[0] - cc.x, acc_a);
+        acc_b = fmaf(cc.y, d[2] - cc.x, acc_b);
+      }
     }
     if (c == 0) {
       red[warp * 16 + g] = acc_a;
@@ -175,7 +169,7 @@ __global__ void __launch_bounds__(kW8Threads, kW8MinBlocks)
     __syncthreads();
     if (tid < 16 && n0 + tid < N) {
       float v = 0.f;
-#pragma unroll
+  #pragma unroll
       for (int w = 0; w < kW8Warps; ++w) v += red[w * 16 + tid];
       y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * s[n0 + tid]));
     }
@@ -256,12 +250,8 @@ cudaError_t launch_w8a16_gemv(const uint16_t* x, const int8_t* q, const float* s
   }
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  // resident CTAs per SM: the register bound, and what shared memory allows
-  int per_sm = kW8MinBlocks;
-  const int by_smem = static_cast<int>((228u * 1024u) / (smem + 1024u));
-  if (by_smem < per_sm) per_sm = by_smem < 1 ? 1 : by_smem;
   const int tiles = (N + 15) / 16;
-  const int grid = tiles < sms * per_sm ? tiles : sms * per_sm;
+  const int grid = tiles < sms * kW8MinBlocks ? tiles : sms * kW8MinBlocks;
   w8a16_gemv_kernel<<<static_cast<unsigned>(grid), kW8Threads, smem, stream>>>(x, q, s, y, N, K);
   return cudaGetLastError();
 }

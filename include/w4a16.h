@@ -215,9 +215,9 @@ w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scal
 /*
  * w8a16_gemv -- y[n] = s[n] * sum_k q[n, k] x[k] (the scale once per row, after the sum).
  *   x bf16 [K]; q int8 [N, K]; scales fp32 [N]; y bf16 [N] (fp32 accumulation, rounded to
- *   nearest even). The tolerance of w4a16_matmul applies. x is held in shared memory
- *   beside the weight staging: K up to 78,272 (W4A16_ERR_UNSUPPORTED beyond). Requires
- *   N > 0, K > 0, K % 64 == 0.
+ *   nearest even). The tolerance of w4a16_matmul applies. x is held in shared memory:
+ *   K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0,
+ *   K % 64 == 0.
  */
 w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
                         int N, int K, w4a16_stream_t stream);
@@ -244,8 +244,8 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
  * nvfp4_gemv -- y[n] = S * sum_b e4m3(s[n, b]) * sum_j e2m1(q[n, 16 b + j]) x[16 b + j]:
  *   x bf16 [K]; codes, scales, tensor_scale as above (device memory); y bf16 [N] (fp32
  *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. x is held
- *   in shared memory beside the weight staging: K up to 83,840 (W4A16_ERR_UNSUPPORTED
- *   beyond). Requires N > 0, K > 0, K % 128 == 0.
+ *   in shared memory: K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0,
+ *   K > 0, K % 128 == 0.
  */
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, uint16_t* y, int N, int K,
