@@ -119,7 +119,10 @@ w4a16_status w4a16_quantize(const float* w, int N, int K, int group, uint8_t* co
   if (group != 128) return W4A16_ERR_UNSUPPORTED;
   if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(mins))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(w4k::launch_w4a16_quantize(w, N, K, codes, scales, mins,
+  uint32_t* status = status_word_ptr();
+  if (status == nullptr) return W4A16_ERR_CUDA;
+  return from_cuda(w4k::launch_w4a16_quantize(w, N, K, codes, scales, mins, status,
+                                              g_wait_limit_ns,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -243,7 +246,10 @@ w4a16_status w4a16zp_quantize(const float* w, int N, int K, int group, uint32_t*
   if (group != 128) return W4A16_ERR_UNSUPPORTED;
   if (!aligned16(w) || !aligned16(qw_rows) || !aligned16(scales) || !aligned16(zeros))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(w4k::launch_w4a16zp_quantize(w, N, K, qw_rows, scales, zeros,
+  uint32_t* status = status_word_ptr();
+  if (status == nullptr) return W4A16_ERR_CUDA;
+  return from_cuda(w4k::launch_w4a16zp_quantize(w, N, K, qw_rows, scales, zeros, status,
+                                                g_wait_limit_ns,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 

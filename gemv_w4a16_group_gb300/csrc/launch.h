@@ -26,8 +26,11 @@ constexpr uint32_t kStatusLayout = 2u;  // a kernel found its shared memory misa
 // Default limit of a bounded wait (nanoseconds of %globaltimer).
 constexpr uint64_t kDefaultWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
+// Group-128 quantizers: a CTA per piece of up to 8192 floats of a row, staged by one bulk
+// copy (bounded wait; an expiry is latched in `status`).
 cudaError_t launch_w4a16_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
-                                  uint16_t* mins, cudaStream_t stream);
+                                  uint16_t* mins, uint32_t* status, uint64_t wait_limit_ns,
+                                  cudaStream_t stream);
 cudaError_t launch_w4a16_pack(const uint8_t* codes, int N, int K, uint32_t* qw,
                               cudaStream_t stream);
 cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
@@ -35,7 +38,8 @@ cudaError_t launch_q4b32_quantize(const float* w, int N, int K, uint8_t* codes, 
 // Zero-point format: quantize into [N, K/8] words and [N, K/128] FP16 scales and zeros, and
 // transpose those into the matmul's [K/8, N] and [K/128, N].
 cudaError_t launch_w4a16zp_quantize(const float* w, int N, int K, uint32_t* qw_rows,
-                                    uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
+                                    uint16_t* scales, uint16_t* zeros, uint32_t* status,
+                                    uint64_t wait_limit_ns, cudaStream_t stream);
 cudaError_t launch_w4a16zp_prepare(const uint32_t* qw_rows, const uint16_t* scales,
                                    const uint16_t* zeros, int N, int K, uint32_t* qw,
                                    uint16_t* scales_t, uint16_t* zeros_t, cudaStream_t stream);
