@@ -344,29 +344,27 @@ def read_traffic(kernel: str, algorithmic: int):
 
 
 def e2e_ours(copies, x_dev, y_dev, M, N, K, device, stream, steps=2000):
-    """Same metric through the public API with host buffers: each step copies x from
-    pinned host memory, runs w4a16_matmul and reads y back to pinned host memory."""
+    """Same metric through the C-ABI call with host buffers (w4a16_matmul_host): each step
+    copies x from pinned host memory, runs the matmul and copies y back to pinned host
+    memory (one library call), then waits for the result on the host."""
     import gemv_w4a16_group_gb300 as w4
 
     ws = workspace_for(M, N, K, device)
     x_host = x_dev.cpu().pin_memory()
     y_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
     bytes_w = weight_bytes(N, K)
-    with torch.cuda.stream(stream):
-        for i in range(20):
-            x_dev.copy_(x_host, non_blocking=True)
-            c = copies[i % ROTATE]
-            w4.w4a16_matmul(x_dev, c[0], c[1], c[2], y=y_dev, workspace=ws)
-            y_host.copy_(y_dev, non_blocking=True)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(steps):
-            x_dev.copy_(x_host, non_blocking=True)
-            c = copies[i % ROTATE]
-            w4.w4a16_matmul(x_dev, c[0], c[1], c[2], y=y_dev, workspace=ws)
-            y_host.copy_(y_dev, non_blocking=True)
-            stream.synchronize()  # the step's result is on the host
-        t1 = time.perf_counter()
+    for i in range(20):
+        c = copies[i % ROTATE]
+        w4.w4a16_matmul_host(x_host, c[0], c[1], c[2], y_host=y_host, x_dev=x_dev, y_dev=y_dev,
+                             workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        c = copies[i % ROTATE]
+        w4.w4a16_matmul_host(x_host, c[0], c[1], c[2], y_host=y_host, x_dev=x_dev, y_dev=y_dev,
+                             workspace=ws, stream=stream)
+        stream.synchronize()  # the step's result is on the host
+    t1 = time.perf_counter()
     return {"value": round(bytes_w * steps / (t1 - t0) / 1e9, 1), "unit": "GB/s",
             "us_per_step": round((t1 - t0) / steps * 1e6, 2),
             "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2}

@@ -35,7 +35,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "W4A16Error", "library_path", "w4a16_quantize", "w4a16_pack", "w4a16_matmul",
-    "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
+    "w4a16_matmul_workspace_bytes", "w4a16_matmul_noalloc", "w4a16_matmul_host",
+    "q4b32_quantize", "q4b32_gemv", "w4a16_device_status",
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
     "testing_set_q4_variant", "testing_set_skinny_range", "w4a16zp_quantize",
     "w4a16zp_prepare", "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
@@ -69,6 +70,7 @@ def _load():
         "w4a16_pack": [P, I, I, P, P],
         "w4a16_matmul": [P, P, P, P, P, I, I, I, I, P, S, P],
         "w4a16_matmul_noalloc": [P, P, P, P, P, I, I, I, I, P],
+        "w4a16_matmul_host": [P, P, P, P, P, I, I, I, I, P, P, P, S, P],
         "q4b32_quantize": [P, I, I, P, P, P],
         "q4b32_gemv": [P, P, P, P, I, I, P],
         "w4a16_device_status": [P],
@@ -178,6 +180,49 @@ def w4a16_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, mins: 
         _dev(mins, "mins", torch.bfloat16, (K // group, N)),
         _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
     return y
+
+
+def w4a16_matmul_host(x_host: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor,
+                      mins: torch.Tensor, y_host=None, x_dev=None, y_dev=None, group: int = 128,
+                      workspace=None, stream=None) -> torch.Tensor:
+    """y_host [M, N] (bf16, host) = x_host [M, K] (bf16, host) . w_hat^T: one library call that
+    enqueues the copy of x, the matmul and the copy of y on the stream and returns; synchronize
+    the stream before reading y_host, and keep x_host alive until then. Pass page-locked host
+    tensors (``pin_memory()``) and the device staging buffers x_dev, y_dev to avoid any
+    allocation per call; with a raw stream handle, pass the staging buffers too."""
+    if not isinstance(x_host, torch.Tensor) or x_host.is_cuda:
+        raise ValueError("x_host must be a host (CPU) tensor")
+    if x_host.dtype != torch.bfloat16 or not x_host.is_contiguous():
+        raise TypeError("x_host must be a contiguous bfloat16 tensor")
+    M, K = x_host.shape
+    N = qw.shape[1]
+    dev = qw.device
+    if y_host is None:
+        y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    if y_host.is_cuda or y_host.dtype != torch.bfloat16 or tuple(y_host.shape) != (M, N) \
+            or not y_host.is_contiguous():
+        raise ValueError("y_host must be a contiguous host bfloat16 tensor of shape (M, N)")
+    if x_dev is None or y_dev is None:
+        # staging allocated on the stream the copies run on (the caching allocator reuses a
+        # freed block only in that stream's order)
+        on = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(dev)
+        with torch.cuda.stream(on):
+            if x_dev is None:
+                x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            if y_dev is None:
+                y_dev = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("w4a16_matmul_host", _lib.w4a16_matmul_host(
+        x_host.data_ptr(), _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)), y_host.data_ptr(), M, N, K, group,
+        _dev(x_dev, "x_dev", torch.bfloat16, (M, K)), _dev(y_dev, "y_dev", torch.bfloat16, (M, N)),
+        ws_ptr, ws_bytes, _stream(stream)))
+    return y_host
 
 
 def w4a16_matmul_noalloc(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor,

@@ -238,6 +238,30 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
                      false);
 }
 
+w4a16_status w4a16_matmul_host(const uint16_t* x_host, const int32_t* qw, const uint16_t* scales,
+                               const uint16_t* mins, uint16_t* y_host, int M, int N, int K,
+                               int group, uint16_t* x_dev, uint16_t* y_dev, void* workspace,
+                               size_t workspace_bytes, w4a16_stream_t stream) {
+  if (!x_host || !y_host || !x_dev || !y_dev) return W4A16_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // argument checks of the product first, so that an invalid call copies nothing
+  if (!qw || !scales || !mins) return W4A16_ERR_INVALID_ARG;
+  if (group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 128 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x_dev) || !aligned16(y_dev) || !aligned16(qw) || !aligned16(scales) ||
+      !aligned16(mins))
+    return W4A16_ERR_MISALIGNED;
+  if ((workspace == nullptr) != (workspace_bytes == 0)) return W4A16_ERR_WORKSPACE;
+  const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  const w4a16_status st = matmul_impl(x_dev, qw, scales, mins, y_dev, M, N, K, group, workspace,
+                                      workspace_bytes, stream, false);
+  if (st != W4A16_OK) return st;
+  return from_cuda(cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, s));
+}
+
 w4a16_status w4a16zp_quantize(const float* w, int N, int K, int group, uint32_t* qw_rows,
                               uint16_t* scales, uint16_t* zeros, w4a16_stream_t stream) {
   if (!w || !qw_rows || !scales || !zeros) return W4A16_ERR_INVALID_ARG;

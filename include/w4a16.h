@@ -110,6 +110,20 @@ w4a16_status w4a16_matmul(const uint16_t* x, const int32_t* qw, const uint16_t* 
                           const uint16_t* mins, uint16_t* y, int M, int N, int K, int group,
                           void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
 
+/*
+ * w4a16_matmul_host -- the same product with x and y in HOST memory: enqueues on `stream` the
+ * copy of x_host (bf16 [M, K]) into x_dev, w4a16_matmul into y_dev, and the copy of y_dev
+ * (bf16 [M, N]) back into y_host, then returns; synchronize the stream before reading
+ * y_host. x_dev and y_dev are caller-owned device buffers of M*K and M*N bf16 (16-byte
+ * aligned); host buffers should be page-locked for the copies to be asynchronous. Weights,
+ * workspace, kernel choice, tolerance and errors as for w4a16_matmul; an argument error is
+ * returned before anything is enqueued.
+ */
+w4a16_status w4a16_matmul_host(const uint16_t* x_host, const int32_t* qw, const uint16_t* scales,
+                               const uint16_t* mins, uint16_t* y_host, int M, int N, int K,
+                               int group, uint16_t* x_dev, uint16_t* y_dev, void* workspace,
+                               size_t workspace_bytes, w4a16_stream_t stream);
+
 /* Bytes of workspace that let w4a16_matmul split K for this shape, or run the skinny
  * kernel for 9 <= M <= 32 (0 = no benefit). */
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);

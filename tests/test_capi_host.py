@@ -44,6 +44,7 @@ def lib(cuda_lib):
     lib.w8a16_gemv.argtypes = [P, P, P, P, I, I, P]
     lib.nvfp4_quantize.argtypes = [P, I, I, P, P, P, P]
     lib.nvfp4_gemv.argtypes = [P, P, P, P, P, I, I, P]
+    lib.w4a16_matmul_host.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, S, P]
     return lib
 
 
@@ -53,7 +54,7 @@ def test_header_declares_the_boundary():
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
                      "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
                      "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
-                     "nvfp4_gemv"):
+                     "nvfp4_gemv", "w4a16_matmul_host"):
         assert required in names
 
 
@@ -143,6 +144,18 @@ def test_nvfp4_rejects_bad_arguments_on_host(lib):
     assert g(A, A, A, A, B, 4, 64, None) == INVALID        # K % 128
     assert g(A, A, A, A, B, 4, 128 * 2048, None) == UNSUPPORTED
     assert g(A, A, A + 1, A, B, 4, 256, None) == MISALIGNED
+
+
+def test_matmul_host_rejects_bad_arguments_before_copying(lib):
+    h = lib.w4a16_matmul_host
+    good = (A, A, A, A, B)
+    assert h(None, A, A, A, B, 1, 256, 512, 128, A, B, None, 0, None) == INVALID
+    assert h(*good, 1, 256, 512, 128, None, B, None, 0, None) == INVALID     # no x_dev
+    assert h(*good, 0, 256, 512, 128, A, B, None, 0, None) == INVALID
+    assert h(*good, 1, 256, 500, 128, A, B, None, 0, None) == INVALID
+    assert h(*good, 1, 260, 512, 128, A, B, None, 0, None) == UNSUPPORTED
+    assert h(*good, 1, 256, 512, 128, A + 2, B, None, 0, None) == MISALIGNED
+    assert h(*good, 1, 256, 512, 128, A, B, A, 0, None) == WORKSPACE
 
 
 def test_workspace_query_is_host_only(lib):

@@ -367,3 +367,29 @@ def test_q4_quantize_exact_ties(w4):
     torch.cuda.synchronize()
     assert np.array_equal(gc.cpu().numpy(), codes)
     assert np.array_equal(bits(gs), sc)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 14336, 4096), (3, 1536, 1536), (40, 4096, 1024)])
+def test_matmul_host_buffers(w4, M, N, K):
+    """w4a16_matmul_host (x and y in pinned host memory, one call) gives the device call's
+    bits, with and without the caller's staging buffers."""
+    _, codes, s_np, m_np, qw_np = quantized(N, K, seed=M)
+    qw, s, m = to_dev_params(codes, s_np, m_np, qw_np)
+    x = workloads.activations_bf16(M, K, seed=M)
+    need = w4.w4a16_matmul_workspace_bytes(M, N, K)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda") if need else None
+    y_dev = w4.w4a16_matmul(x.cuda(), qw, s, m, workspace=ws)
+    stream = torch.cuda.current_stream()
+    xh = x.pin_memory()  # alive until the stream has copied it
+    y_host = w4.w4a16_matmul_host(xh, qw, s, m, workspace=ws)
+    stream.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+    xd = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    yd = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    w4.w4a16_matmul_host(xh, qw, s, m, y_host=y2, x_dev=xd, y_dev=yd, workspace=ws)
+    stream.synchronize()
+    assert torch.equal(y2.view(torch.int16), y_dev.cpu().view(torch.int16))
+    with pytest.raises(ValueError, match="host"):
+        w4.w4a16_matmul_host(x.cuda(), qw, s, m)
+    assert w4.w4a16_device_status() == 0
