@@ -19,6 +19,7 @@ Array conventions (all numpy, C-contiguous):
     w_hat = q s.
   * NVFP4A16: ``codes`` uint8 [N, K/2] (E2M1, low nibble = even k); ``scales`` uint8
     E4M3 [N, K/16]; ``S`` one fp32; ``x`` bf16 bits [K]; w_hat = e2m1 e4m3 S.
+  * MXFP4A16: ``codes`` as NVFP4; ``scales`` uint8 E8M0 [N, K/32]; w_hat = e2m1 2^(s - 127).
 """
 from __future__ import annotations
 
@@ -98,13 +99,19 @@ def _bind(lib):
     lib.oracle_nvfp4_quantize.argtypes = [P, I, I, P, P, P]
     lib.oracle_nvfp4_dequant.argtypes = [P, P, F, I, I, P]
     lib.oracle_nvfp4_gemv.argtypes = [P, P, P, F, I, I, P, I, P, P]
+    lib.oracle_e8m0_value.argtypes = [I]
+    lib.oracle_e8m0_value.restype = ctypes.c_double
+    lib.oracle_mxfp4_quantize.argtypes = [P, I, I, P, P]
+    lib.oracle_mxfp4_dequant.argtypes = [P, P, I, I, P]
+    lib.oracle_mxfp4_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
     for name in ("oracle_bf16_rne_array", "oracle_fp16_rne_array", "oracle_fp16_to_float_array",
                  "oracle_w4a16_quantize", "oracle_w4a16_pack", "oracle_w4a16_dequant",
                  "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_q4b32_quantize",
                  "oracle_q4b32_dequant", "oracle_q4b32_gemv", "oracle_w4a16zp_quantize",
                  "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul", "oracle_w8a16_quantize",
                  "oracle_w8a16_gemv", "oracle_nvfp4_quantize", "oracle_nvfp4_dequant",
-                 "oracle_nvfp4_gemv"):
+                 "oracle_nvfp4_gemv", "oracle_mxfp4_quantize", "oracle_mxfp4_dequant",
+                 "oracle_mxfp4_gemv"):
         getattr(lib, name).restype = None
     return lib
 
@@ -401,6 +408,49 @@ def nvfp4_gemv(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, S: flo
     a = np.empty(n_out, dtype=np.float64)
     _load().oracle_nvfp4_gemv(_ptr(x_bits), _ptr(codes), _ptr(scales), float(S), N, K, rows_p,
                               n_out, _ptr(y), _ptr(a))
+    return y, a
+
+
+def e8m0_value(code: int) -> float:
+    return float(_load().oracle_e8m0_value(int(code)))
+
+
+def mxfp4_quantize(w: np.ndarray):
+    """fp32 [N, K] -> (codes u8 [N, K/2], scales u8 E8M0 [N, K/32])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    assert K % 32 == 0
+    codes = np.empty((N, K // 2), dtype=np.uint8)
+    scales = np.empty((N, K // 32), dtype=np.uint8)
+    _load().oracle_mxfp4_quantize(_ptr(w), N, K, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def mxfp4_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((N, K), dtype=np.float64)
+    _load().oracle_mxfp4_dequant(_ptr(codes), _ptr(scales), N, K, _ptr(out))
+    return out
+
+
+def mxfp4_gemv(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, rows=None):
+    """y_ref, abs_ref (fp64 [N] or [len(rows)]) for y = W_hat . x."""
+    x_bits = _c(x_bits, np.uint16).ravel()
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    assert x_bits.shape[0] == K and scales.shape == (N, K // 32)
+    if rows is None:
+        n_out, rows_p = N, None
+    else:
+        rows = _c(rows, np.int32)
+        n_out, rows_p = len(rows), _ptr(rows)
+    y = np.empty(n_out, dtype=np.float64)
+    a = np.empty(n_out, dtype=np.float64)
+    _load().oracle_mxfp4_gemv(_ptr(x_bits), _ptr(codes), _ptr(scales), N, K, rows_p, n_out,
+                              _ptr(y), _ptr(a))
     return y, a
 
 

@@ -23,7 +23,8 @@
  *   [P4] "Hardware-invariant NVFP4 progress report 1", "The NVFP4 layout"
  *        (E2M1 weights, largest value 6, an E4M3 scale per 16 weights and an
  *        FP32 scale per tensor; NVFP4A16 decodes to 16-bit floats) and [P1]
- *        Step 6 (4.5 bits per value).
+ *        Step 6 (4.5 bits per value; MX blocks of 32 with an E8M0 scale, the
+ *        scale rule, 4.25 bits per value for MXFP4).
  *   [P3] "Quantization and GEMV", exercise 1 (W8A16 GEMV: symmetric per-row
  *        INT8, s = max|w| / 127, one 16-byte load of 16 codes per lane, the
  *        row's scale applied after the sum) and section "W4A16: dequantizing in registers"
@@ -59,6 +60,12 @@
  *     the nearest E2M1 value, ties to the even code, saturating at 6; a block
  *     of zeros stores scale 0 and codes 0. Codes [N, K/2] (low nibble = even
  *     k), scales [N, K/16].
+ *   - MXFP4 [P1 Step 6]: E2M1 codes, one E8M0 scale (2^(code - 127)) per 32
+ *     weights along K. The block scale is the largest power of two <= max|w|
+ *     divided by 4 (the largest power of two E2M1 holds): 2^(floor(log2 amax) - 2),
+ *     exponent kept in [-127, 127]; codes round w / scale (exact) to the nearest
+ *     E2M1 value, ties to the even code, values past 6 clamped to 6; a block of
+ *     zeros stores scale code 0 and codes 0. Codes [N, K/2], scales [N, K/32].
  *   - W8A16 [P3 exercise 1]: per row s = fp32(max|w| / 127), kept in fp32 (no
  *     storage type is given); q = clamp(round(fl(w / s)), -127, 127) with the
  *     same half-away rounding; a row of zeros stores s = 0 and q = 0. x and y
@@ -625,6 +632,73 @@ void oracle_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* s
     double acc = 0.0, acc_abs = 0.0;
     for (int k = 0; k < K; ++k) {
       double t = (double)oracle_bf16_to_float(x[k]) * nvfp4_w_hat(codes, scales, S, K, n, k);
+      acc += t;
+      acc_abs += fabs(t);
+    }
+    y_ref[i] = acc;
+    if (abs_ref) abs_ref[i] = acc_abs;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP4 weights, 16-bit activations ([P1] Step 6, the OCP MX blocks).      */
+/* ------------------------------------------------------------------------ */
+
+/* E8M0: an unsigned biased exponent, 2^(code - 127); 255 is NaN. */
+double oracle_e8m0_value(int code) { return code == 255 ? NAN : ldexp(1.0, code - 127); }
+
+/* w: fp32 [N, K] (K % 32 == 0); codes: uint8 [N, K/2] (byte j: k = 2j low nibble,
+ * 2j + 1 high nibble); scales: E8M0 [N, K/32]. */
+void oracle_mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales) {
+  for (int n = 0; n < N; ++n) {
+    for (int b = 0; b < K / 32; ++b) {
+      const float* wb = w + (size_t)n * K + (size_t)b * 32;
+      double amax = 0.0;
+      for (int j = 0; j < 32; ++j)
+        if (fabs((double)wb[j]) > amax) amax = fabs((double)wb[j]);
+      int sc = 0;
+      int q[32] = {0};
+      if (amax > 0.0) {
+        int e;
+        frexp(amax, &e);   /* amax = m 2^e, m in [0.5, 1): floor(log2 amax) = e - 1 */
+        int X = (e - 1) - 2;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+        sc = X + 127;
+        for (int j = 0; j < 32; ++j) {
+          double t = ldexp((double)wb[j], -X); /* exact */
+          q[j] = oracle_e2m1_rne((float)t);     /* exact for |t| < 8 */
+        }
+      }
+      scales[(size_t)n * (K / 32) + b] = (uint8_t)sc;
+      for (int j = 0; j < 16; ++j)
+        codes[(size_t)n * (K / 2) + (size_t)b * 16 + j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+    }
+  }
+}
+
+static double mxfp4_w_hat(const uint8_t* codes, const uint8_t* scales, int K, int n, int k) {
+  uint8_t byte = codes[(size_t)n * (K / 2) + k / 2];
+  int q = (k & 1) ? (byte >> 4) : (byte & 15);
+  return oracle_e2m1_value(q) * oracle_e8m0_value(scales[(size_t)n * (K / 32) + k / 32]);
+}
+
+void oracle_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int N, int K,
+                          double* w_hat) {
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) w_hat[(size_t)n * K + k] = mxfp4_w_hat(codes, scales, K, n, k);
+}
+
+/* y_ref[i] = sum_k x[k] * w_hat[n, k] for n = rows[i] (every row when rows is
+ * NULL), fp64; abs_ref the sum of the magnitudes. x: bf16 bit patterns [K]. */
+void oracle_mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales, int N,
+                       int K, const int32_t* rows, int nrows, double* y_ref, double* abs_ref) {
+  if (!rows) nrows = N;
+  for (int i = 0; i < nrows; ++i) {
+    int n = rows ? rows[i] : i;
+    double acc = 0.0, acc_abs = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double t = (double)oracle_bf16_to_float(x[k]) * mxfp4_w_hat(codes, scales, K, n, k);
       acc += t;
       acc_abs += fabs(t);
     }

@@ -716,4 +716,98 @@ def pin_nvfp4_gemv_exact_and_error():
     assert 0.07 < e_nv < e_i4 < 0.15, (e_nv, e_i4)
 
 
+# --------------------------------------------------------------------------- #
+# MXFP4 weights: E2M1 codes, one E8M0 (power-of-two) scale per 32
+# --------------------------------------------------------------------------- #
+
+def pin_mxfp4_hand_worked_blocks_and_scale_format():
+    """Hand-worked blocks (tests/golden/mxfp4_blocks.txt); E8M0 values against PyTorch's
+    float8_e8m0fnu; 4.25 bits per value (the page's figure) from the array sizes."""
+    for tag, rec in _records("mxfp4_blocks.txt"):
+        w = _weights_from(rec).reshape(1, -1)
+        codes, scales = oracle.mxfp4_quantize(w)
+        assert int(scales[0, 0]) == int(rec["scale"][0], 16), (tag, hex(scales[0, 0]))
+        assert [int(v) for v in codes[0]] == [int(v, 16) for v in rec["bytes"]], tag
+    if hasattr(torch, "float8_e8m0fnu"):
+        t = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu)
+        ref = t.float().double().numpy()
+        for c in range(255):
+            assert oracle.e8m0_value(c) == ref[c], c
+    else:  # the format's definition: a biased exponent
+        for c in range(255):
+            assert oracle.e8m0_value(c) == 2.0 ** (c - 127), c
+    assert np.isnan(oracle.e8m0_value(255))
+    codes, scales = oracle.mxfp4_quantize(np.ones((3, 64), dtype=np.float32))
+    assert (codes.nbytes + scales.nbytes) * 8 / (3 * 64) == 4.25
+
+
+def pin_mxfp4_scale_rule_and_round_trip():
+    """On random blocks the scale is 2^(floor(log2 max|w|) - 2) and every code is a nearest
+    E2M1 value of w / scale (ties to the even code, clamped at 6); weights on the grid (a
+    block maximum of 4 or 6 times a power of two) come back exactly."""
+    rng = np.random.default_rng(51)
+    w = (rng.standard_normal((8, 256)) * 10.0 ** rng.uniform(-4, 2, size=(8, 1))).astype(np.float32)
+    codes, scales = oracle.mxfp4_quantize(w)
+    grid = [Fraction(int(2 * oracle.e2m1_value(c)), 2) for c in range(8)]
+    qn = _nv_codes(codes)
+    for n in range(8):
+        for b in range(8):
+            blk = w[n, 32 * b:32 * (b + 1)]
+            amax = Fraction(float(np.abs(blk).max()))
+            X = int(scales[n, b]) - 127
+            assert 2 ** (X + 2) <= amax < 2 ** (X + 3), (n, b, X, float(amax))
+            for j, wv in enumerate(blk):
+                t = abs(Fraction(float(wv)) / Fraction(2) ** X)
+                c = int(qn[n, 32 * b + j]) & 7
+                if t >= 6:
+                    assert c == 7
+                else:
+                    d = [abs(t - g) for g in grid]
+                    assert c == min(range(8), key=lambda i: (d[i], i & 1)), (n, b, j, float(t))
+    X = rng.integers(-20, 10, size=(4, 4))
+    q = rng.integers(0, 16, size=(4, 128))
+    q[:, ::32] = 7  # +6: the block maximum
+    e2 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6])
+    w = (e2[q] * np.repeat(np.exp2(X), 32, axis=1)).astype(np.float32)
+    codes, scales = oracle.mxfp4_quantize(w)
+    np.testing.assert_array_equal(scales.astype(int) - 127, X)
+    np.testing.assert_array_equal(_nv_codes(codes), q)
+    np.testing.assert_array_equal(oracle.mxfp4_dequant(codes, scales), w.astype(np.float64))
+
+
+def pin_mxfp4_gemv_exact_and_error():
+    """Small GEMVs equal the exact rational sum; torch.matmul (fp64) agrees on a larger one;
+    the row subset matches; on weights with 0.1 % outliers MXFP4's weight error lies above
+    NVFP4's (the pages: 11.8 % against 9.4 % on a real layer) and within 8-16 %."""
+    rng = np.random.default_rng(53)
+    for (N, K) in ((2, 32), (3, 96)):
+        w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        codes, scales = oracle.mxfp4_quantize(w)
+        x = workloads.bits16(workloads.activations_bf16(1, K, seed=N))[0]
+        y, a = oracle.mxfp4_gemv(x, codes, scales)
+        qn = _nv_codes(codes)
+        for n in range(N):
+            exact = sum(Fraction(_bf16(x[k])) * Fraction(oracle.e2m1_value(int(qn[n, k]))) *
+                        Fraction(2) ** (int(scales[n, k // 32]) - 127) for k in range(K))
+            assert abs(Fraction(y[n]) - exact) <= Fraction(a[n]) / 2**45, (N, K, n)
+    N, K = 48, 1024
+    w = workloads.weights(N, K, seed=54, outlier_frac=0.001).numpy()
+    codes, scales = oracle.mxfp4_quantize(w)
+    w_hat = oracle.mxfp4_dequant(codes, scales)
+    x = workloads.bits16(workloads.activations_bf16(1, K, seed=54))[0]
+    y, a = oracle.mxfp4_gemv(x, codes, scales)
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double()
+    ref = (torch.from_numpy(w_hat) @ xv).numpy()
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    rows = np.array([N - 1, 2], dtype=np.int32)
+    y2, _ = oracle.mxfp4_gemv(x, codes, scales, rows=rows)
+    np.testing.assert_array_equal(y2, y[rows])
+    w = workloads.weights(256, 2048, seed=0, outlier_frac=0.001).numpy()
+    c, s = oracle.mxfp4_quantize(w)
+    e_mx = np.linalg.norm(oracle.mxfp4_dequant(c, s) - w) / np.linalg.norm(w)
+    c4, s4, S4 = oracle.nvfp4_quantize(w)
+    e_nv = np.linalg.norm(oracle.nvfp4_dequant(c4, s4, S4) - w) / np.linalg.norm(w)
+    assert e_nv < e_mx and 0.08 < e_mx < 0.16, (e_nv, e_mx)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -90,6 +90,12 @@ MUTANTS = [
      "return oracle_e2m1_value(q) * oracle_e4m3_value(scales[(size_t)n * (K / 16) + k / 16]) *\n         (double)S;",
      "return oracle_e2m1_value(q) * oracle_e4m3_value(scales[(size_t)n * (K / 16) + k / 16]);",
      None),
+    ("mx_scale_exponent_minus_1", "int X = (e - 1) - 2;", "int X = (e - 1) - 1;", None),
+    ("mx_scale_from_ceil", "int X = (e - 1) - 2;", "int X = e - 2;", None),
+    ("mx_e8m0_bias_128", "ldexp(1.0, code - 127); }", "ldexp(1.0, code - 128); }", None),
+    ("mx_codes_unscaled", "double t = ldexp((double)wb[j], -X); /* exact */",
+     "double t = (double)wb[j];", None),
+    ("mx_scale_code_off_by_one", "sc = X + 127;", "sc = X + 128;", None),
     ("zp_nibble_order_reversed", "(uint32_t)q << (4 * (k % 8));", "(uint32_t)q << (4 * (7 - k % 8));",
      None),
 ]
