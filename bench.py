@@ -11,7 +11,7 @@ around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than t
 The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
 the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
 quantize and GEMV (16384 x 16384), the zero-point format (quantize, layout move, matmul at
-M = 1, 16, 4096), the W8A16 per-row INT8 and the NVFP4A16 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
+M = 1, 16, 4096), the W8A16 per-row INT8, NVFP4A16 and MXFP4A16 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
 each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -499,7 +499,23 @@ def rows_ours(peaks, device, stream):
     nv["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
                   "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
     rows["nvfp4a16"] = nv
-    del cps4, c4, s4, S4, x8, y8
+    del cps4, c4, s4, S4
+
+    # MXFP4A16 on the up-projection: quantize and the M = 1 GEMV
+    w = workloads.weights(N, K, seed=0).to(device)
+    cm, sm_ = w4.mxfp4_quantize(w)
+    us = graph_time_us(lambda i: w4.mxfp4_quantize(w, codes=cm, scales=sm_), 4, 5, stream)
+    b = N * K * 4 + N * K // 2 + N * K // 32
+    mx = {"shape": [N, K], "quantize": {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                                         "frac_hbm": round(b / us / 1e3 / hbm, 3)}}
+    del w
+    cpsm = [(cm.clone(), sm_.clone()) for _ in range(ROTATE)]
+    us = graph_time_us(lambda i: w4.mxfp4_gemv(x8, *cpsm[i % ROTATE], y=y8), 2 * ROTATE, 10, stream)
+    b = N * K // 2 + N * K // 32
+    mx["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                  "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
+    rows["mxfp4a16"] = mx
+    del cpsm, cm, sm_, x8, y8
 
     # Q4 block-32, 16384 x 16384
     qc_cfg = workloads.Q4_SQUARE

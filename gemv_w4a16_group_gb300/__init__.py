@@ -23,6 +23,8 @@ Formats ("Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 2;
   * NVFP4A16 ("Hardware-invariant NVFP4 progress report 1"): codes uint8 [N, K/2] (E2M1,
     low nibble = even k); scales uint8 [N, K/16] (E4M3 bits); tensor_scale float32 [1];
     x bfloat16 [K]; y bfloat16 [N]; w_hat = e2m1(q) * e4m3(scale) * tensor_scale.
+  * MXFP4A16 ("Low-Precision Kernels ...", Step 6): codes as NVFP4; scales uint8 [N, K/32]
+    (E8M0 bits); w_hat = e2m1(q) * 2^(scale - 127).
 """
 from __future__ import annotations
 
@@ -40,7 +42,7 @@ __all__ = [
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
     "testing_set_q4_variant", "testing_set_skinny_range", "w4a16zp_quantize",
     "w4a16zp_prepare", "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
-    "nvfp4_gemv",
+    "nvfp4_gemv", "mxfp4_quantize", "mxfp4_gemv",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -82,6 +84,8 @@ def _load():
         "w8a16_gemv": [P, P, P, P, I, I, P],
         "nvfp4_quantize": [P, I, I, P, P, P, P],
         "nvfp4_gemv": [P, P, P, P, P, I, I, P],
+        "mxfp4_quantize": [P, I, I, P, P, P],
+        "mxfp4_gemv": [P, P, P, P, I, I, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -359,6 +363,32 @@ def nvfp4_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
         _dev(scales, "scales", torch.uint8, (N, K // 16)),
         _dev(tensor_scale, "tensor_scale", torch.float32, (1,)),
         _dev(y, "y", torch.bfloat16, (N,)), N, K, _stream(stream)))
+    return y
+
+
+def mxfp4_quantize(w: torch.Tensor, codes=None, scales=None, stream=None):
+    """fp32 [N, K] -> (codes uint8 [N, K/2], scales uint8 E8M0 [N, K/32])."""
+    N, K = w.shape
+    if codes is None:
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, K // 32), dtype=torch.uint8, device=w.device)
+    _check("mxfp4_quantize", _lib.mxfp4_quantize(
+        _dev(w, "w", torch.float32), N, K, _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.uint8, (N, K // 32)), _stream(stream)))
+    return codes, scales
+
+
+def mxfp4_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y=None,
+               stream=None) -> torch.Tensor:
+    """y [N] (bf16) = W_hat . x, x bf16 [K]."""
+    N, K = codes.shape[0], codes.shape[1] * 2
+    if y is None:
+        y = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
+    _check("mxfp4_gemv", _lib.mxfp4_gemv(
+        _dev(x, "x", torch.bfloat16, (K,)), _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.uint8, (N, K // 32)), _dev(y, "y", torch.bfloat16, (N,)),
+        N, K, _stream(stream)))
     return y
 
 

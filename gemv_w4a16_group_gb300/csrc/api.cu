@@ -342,6 +342,26 @@ w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+w4a16_status mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                            w4a16_stream_t stream) {
+  if (!w || !codes || !scales) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales)) return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_mxfp4_quantize(w, N, K, codes, scales,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                        uint16_t* y, int N, int K, w4a16_stream_t stream) {
+  if (!x || !codes || !scales || !y) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 128 != 0) return W4A16_ERR_INVALID_ARG;
+  if (w4k::nvfp4_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(
+      w4k::launch_mxfp4_gemv(x, codes, scales, y, N, K, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                             w4a16_stream_t stream) {
   if (!w || !codes || !scales) return W4A16_ERR_INVALID_ARG;

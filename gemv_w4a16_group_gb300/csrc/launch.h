@@ -146,6 +146,13 @@ cudaError_t launch_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uin
                               const float* tensor_scale, uint16_t* y, int N, int K,
                               cudaStream_t stream);
 
+// MXFP4 weights (E2M1 codes [N, K/2], E8M0 block scales [N, K/32]): quantize (K % 32 == 0)
+// and the M = 1 GEMV (K % 128 == 0, shared memory as the NVFP4 GEMV).
+cudaError_t launch_mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream);
+cudaError_t launch_mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                              uint16_t* y, int N, int K, cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

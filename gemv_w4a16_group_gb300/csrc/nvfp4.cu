@@ -91,6 +91,19 @@ struct NvLayout {
   }
 };
 
+// FP16 pair (2^d, 2^d) for -254 <= d <= 0; 0 below 2^-24 (FP16's smallest subnormal).
+__device__ __forceinline__ uint32_t f16x2_pow2(int d) {
+  const uint32_t h = d >= -14 ? static_cast<uint32_t>(d + 15) << 10
+                              : (d >= -24 ? 1u << (d + 24) : 0u);
+  return h | (h << 16);
+}
+
+// MX: MXFP4 (E8M0 scale per 32 codes, no tensor scale) instead of NVFP4 (E4M3 scale per 16
+// codes and a tensor scale). A lane's 32 codes of a row are one MX block; its scale 2^X
+// enters the FP16 codes as 2^(X - R), R the largest X of the row's four blocks in the chunk
+// (exact down to FP16's smallest subnormal: a block 2^24 below its neighbours adds nothing
+// the tolerance sees), and 2^R multiplies the chunk's fp32 sum.
+template <bool MX>
 __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
     nvfp4_gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
                       const uint8_t* __restrict__ scales, const float* __restrict__ tensor_scale,
@@ -154,8 +167,8 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
     const size_t rb = static_cast<size_t>(min(n0 + g + 8, N - 1));
     const uint8_t* pa = codes + ra * (K / 2) + 16 * c;
     const uint8_t* pb = codes + rb * (K / 2) + 16 * c;
-    const uint8_t* qa = scales + ra * (K / 16) + 2 * c;
-    const uint8_t* qb = scales + rb * (K / 16) + 2 * c;
+    const uint8_t* qa = MX ? scales + ra * (K / 32) + c : scales + ra * (K / 16) + 2 * c;
+    const uint8_t* qb = MX ? scales + rb * (K / 32) + c : scales + rb * (K / 16) + 2 * c;
     const uint32_t xlane = smem_addr(xs) + static_cast<uint32_t>(64 * c);
     float acc_a = 0.f, acc_b = 0.f;
     for (int ch0 = warp; ch0 < chunks; ch0 += kNvWarps * kNvUnroll) {
@@ -167,18 +180,39 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
         if (ch < chunks) {
           wa[u] = ldg_stream128_nv(pa + 64 * static_cast<size_t>(ch));
           wb[u] = ldg_stream128_nv(pb + 64 * static_cast<size_t>(ch));
-          sa[u] = __ldg(reinterpret_cast<const unsigned short*>(qa + 8 * static_cast<size_t>(ch)));
-          sb[u] = __ldg(reinterpret_cast<const unsigned short*>(qb + 8 * static_cast<size_t>(ch)));
+          if constexpr (MX) {
+            sa[u] = __ldg(qa + 4 * static_cast<size_t>(ch));
+            sb[u] = __ldg(qb + 4 * static_cast<size_t>(ch));
+          } else {
+            sa[u] = __ldg(reinterpret_cast<const unsigned short*>(qa + 8 * static_cast<size_t>(ch)));
+            sb[u] = __ldg(reinterpret_cast<const unsigned short*>(qb + 8 * static_cast<size_t>(ch)));
+          }
         }
       }
   #pragma unroll
       for (int u = 0; u < kNvUnroll; ++u) {
         const int ch = ch0 + u * kNvWarps;
         if (ch >= chunks) break;  // warp-uniform
-        // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
-        const uint32_t s2a = e4m3x2_f16(sa[u]), s2b = e4m3x2_f16(sb[u]);
-        const uint32_t sa_lo = __byte_perm(s2a, 0u, 0x1010), sa_hi = __byte_perm(s2a, 0u, 0x3232);
-        const uint32_t sb_lo = __byte_perm(s2b, 0u, 0x1010), sb_hi = __byte_perm(s2b, 0u, 0x3232);
+        uint32_t sa_lo, sa_hi, sb_lo, sb_hi;
+        int Ra = 0, Rb = 0;
+        if constexpr (MX) {
+          // largest exponent of the row's four blocks (lanes c = 0..3) in this chunk
+          Ra = static_cast<int>(sa[u]);
+          Rb = static_cast<int>(sb[u]);
+          Ra = max(Ra, __shfl_xor_sync(0xffffffffu, Ra, 1));
+          Rb = max(Rb, __shfl_xor_sync(0xffffffffu, Rb, 1));
+          Ra = max(Ra, __shfl_xor_sync(0xffffffffu, Ra, 2));
+          Rb = max(Rb, __shfl_xor_sync(0xffffffffu, Rb, 2));
+          sa_lo = sa_hi = f16x2_pow2(static_cast<int>(sa[u]) - Ra);
+          sb_lo = sb_hi = f16x2_pow2(static_cast<int>(sb[u]) - Rb);
+        } else {
+          // block scales 2c, 2c + 1 of this lane's 32 k, each duplicated into an FP16 pair
+          const uint32_t s2a = e4m3x2_f16(sa[u]), s2b = e4m3x2_f16(sb[u]);
+          sa_lo = __byte_perm(s2a, 0u, 0x1010);
+          sa_hi = __byte_perm(s2a, 0u, 0x3232);
+          sb_lo = __byte_perm(s2b, 0u, 0x1010);
+          sb_hi = __byte_perm(s2b, 0u, 0x3232);
+        }
         const uint32_t ra4[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
         const uint32_t rb4[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
         float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -197,8 +231,13 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
           }
         }
         const float u2 = cst[ch];
-        acc_a = fmaf(u2, d[0], acc_a);
-        acc_b = fmaf(u2, d[2], acc_b);
+        if constexpr (MX) {
+          acc_a = fmaf(ldexpf(u2, Ra - 127), d[0], acc_a);
+          acc_b = fmaf(ldexpf(u2, Rb - 127), d[2], acc_b);
+        } else {
+          acc_a = fmaf(u2, d[0], acc_a);
+          acc_b = fmaf(u2, d[2], acc_b);
+        }
       }
     }
     if (c == 0) {
@@ -210,7 +249,8 @@ __global__ void __launch_bounds__(kNvThreads, kNvMinBlocks)
       float v = 0.f;
   #pragma unroll
       for (int w = 0; w < kNvWarps; ++w) v += red[w * 16 + tid];
-      y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v * __ldg(tensor_scale)));
+      if constexpr (!MX) v *= __ldg(tensor_scale);
+      y[n0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
     __syncthreads();  // red is rewritten by the next tile
   }
@@ -280,6 +320,39 @@ __global__ void __launch_bounds__(kNvThreads)
   if ((lane & 3) == 0) scales[e0 / 16] = static_cast<uint8_t>(sc);
 }
 
+// MXFP4 ("Low-Precision Kernels ...", Step 6): per block of 32, scale 2^X with
+// X = floor(log2 max|w|) - 2 (the largest power of two not above max|w|, over 4, the largest
+// power of two E2M1 holds), kept in [-127, 127]; codes round w 2^-X (exact) to nearest even
+// E2M1, clamped at 6; a block of zeros stores scale code 0 and codes 0. A warp takes 128
+// consecutive weights (K % 32 == 0: blocks never straddle rows), 8 lanes per block.
+__global__ void __launch_bounds__(kNvThreads)
+    mxfp4_quantize_kernel(const float* __restrict__ w, long long total, uint8_t* __restrict__ codes,
+                          uint8_t* __restrict__ scales) {
+  const long long wi = static_cast<long long>(blockIdx.x) * kNvWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long e0 = wi * 128 + lane * 4;
+  if (wi * 128 >= total) return;  // warp-uniform
+  const bool valid = e0 < total;  // total is a multiple of 32: a block is valid or not
+  const float4 v = valid ? __ldcs(reinterpret_cast<const float4*>(w + e0)) : make_float4(0, 0, 0, 0);
+  float bmax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+  uint32_t sc = 0u, packed = 0u;
+  if (bmax > 0.f) {
+    int e;
+    frexpf(bmax, &e);  // bmax = m 2^e, m in [0.5, 1)
+    const int X = min(127, max(-127, e - 3));
+    sc = static_cast<uint32_t>(X + 127);
+    const float inv = pow2f(-X);  // -125 <= -X <= 127: a normal float
+    const uint32_t b0 = e2m1x2_rn(__fmul_rn(v.y, inv), __fmul_rn(v.x, inv));
+    const uint32_t b1 = e2m1x2_rn(__fmul_rn(v.w, inv), __fmul_rn(v.z, inv));
+    packed = (b0 & 0xFFu) | ((b1 & 0xFFu) << 8);
+  }
+  if (!valid) return;
+  *reinterpret_cast<uint16_t*>(codes + e0 / 2) = static_cast<uint16_t>(packed);
+  if ((lane & 7) == 0) scales[e0 / 32] = static_cast<uint8_t>(sc);
+}
+
 __global__ void nvfp4_finalize_kernel(float* tensor_scale) {
   *tensor_scale = tensor_scale_of(*tensor_scale);  // the word holds amax until now
 }
@@ -315,16 +388,43 @@ cudaError_t launch_nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uin
                               cudaStream_t stream) {
   const uint32_t smem = NvLayout(K).total;
   if (smem > 48u * 1024u) {
-    const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemv_kernel),
-                                               static_cast<int>(smem));
+    const cudaError_t e = set_max_dynamic_smem(
+        reinterpret_cast<const void*>(nvfp4_gemv_kernel<false>), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int tiles = (N + 15) / 16;
   const int grid = tiles < sms * kNvMinBlocks ? tiles : sms * kNvMinBlocks;
-  nvfp4_gemv_kernel<<<static_cast<unsigned>(grid), kNvThreads, smem, stream>>>(
+  nvfp4_gemv_kernel<false><<<static_cast<unsigned>(grid), kNvThreads, smem, stream>>>(
       x, codes, scales, tensor_scale, y, N, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream) {
+  const long long total = static_cast<long long>(N) * K;
+  const long long blocks = (total + 128LL * kNvWarps - 1) / (128LL * kNvWarps);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  mxfp4_quantize_kernel<<<static_cast<unsigned>(blocks), kNvThreads, 0, stream>>>(w, total, codes,
+                                                                                  scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                              uint16_t* y, int N, int K, cudaStream_t stream) {
+  const uint32_t smem = NvLayout(K).total;
+  if (smem > 48u * 1024u) {
+    const cudaError_t e = set_max_dynamic_smem(
+        reinterpret_cast<const void*>(nvfp4_gemv_kernel<true>), static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int tiles = (N + 15) / 16;
+  const int grid = tiles < sms * kNvMinBlocks ? tiles : sms * kNvMinBlocks;
+  nvfp4_gemv_kernel<true><<<static_cast<unsigned>(grid), kNvThreads, smem, stream>>>(
+      x, codes, scales, nullptr, y, N, K);
   return cudaGetLastError();
 }
 

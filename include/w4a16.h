@@ -12,7 +12,8 @@
  *   form w_hat = (q - z) * s with FP16 scale and zero point per group of 128
  *   ("Quantization and GEMV", "The quantization formulas"), and the page's W8A16
  *   exercise adds symmetric per-row INT8 weights, w_hat = q * s; NVFP4 weights (E2M1
- *   codes with E4M3 block scales and an fp32 tensor scale) run weight-only as well.
+ *   codes with E4M3 block scales and an fp32 tensor scale) and MXFP4 weights (E2M1 codes
+ *   with power-of-two E8M0 block scales) run weight-only as well.
  *
  * Conventions shared by every entry point
  *   - Every array pointer is DEVICE memory owned by the caller. The library keeps no
@@ -264,6 +265,31 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, uint16_t* y, int N, int K,
                         w4a16_stream_t stream);
+
+/*
+ * MXFP4 weights with 16-bit activations ("Low-Precision Kernels ...", Step 6, the OCP MX
+ * blocks): E2M1 codes, one E8M0 scale (2^(code - 127)) per 32 weights along K; w_hat =
+ * e2m1(q) * 2^(s_b - 127) (4.25 bits per weight).
+ *
+ * mxfp4_quantize -- w fp32 [N, K] -> codes uint8 [N, K/2] (as NVFP4), scales E8M0 bytes
+ *   [N, K/32]: the scale is the largest power of two <= max|w| of the block, divided by 4
+ *   (the largest power of two E2M1 holds), exponent in [-127, 127]; codes are w / scale
+ *   rounded to the nearest E2M1 value, ties to the even code, values past 6 clamped to 6; a
+ *   block of zeros stores scale code 0 and codes 0. Requires N > 0, K > 0, K % 32 == 0.
+ */
+w4a16_status mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
+                            w4a16_stream_t stream);
+
+/*
+ * mxfp4_gemv -- y[n] = sum_b 2^(s[n, b] - 127) * sum_j e2m1(q[n, 32 b + j]) x[32 b + j]:
+ *   x bf16 [K]; codes, scales as above; y bf16 [N] (fp32 accumulation, rounded to nearest
+ *   even). Within a 128-k chunk of a row, a block more than 2^24 below the chunk's largest
+ *   block scale adds nothing (its terms are below the tolerance). The tolerance of
+ *   w4a16_matmul applies. K up to 83,840 as for nvfp4_gemv. Requires N > 0, K > 0,
+ *   K % 128 == 0.
+ */
+w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                        uint16_t* y, int N, int K, w4a16_stream_t stream);
 
 /*
  * w4a16_device_status -- synchronizes `stream`, then reads and clears the current

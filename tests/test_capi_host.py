@@ -45,6 +45,8 @@ def lib(cuda_lib):
     lib.nvfp4_quantize.argtypes = [P, I, I, P, P, P, P]
     lib.nvfp4_gemv.argtypes = [P, P, P, P, P, I, I, P]
     lib.w4a16_matmul_host.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, S, P]
+    lib.mxfp4_quantize.argtypes = [P, I, I, P, P, P]
+    lib.mxfp4_gemv.argtypes = [P, P, P, P, I, I, P]
     return lib
 
 
@@ -54,7 +56,7 @@ def test_header_declares_the_boundary():
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
                      "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
                      "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
-                     "nvfp4_gemv", "w4a16_matmul_host"):
+                     "nvfp4_gemv", "w4a16_matmul_host", "mxfp4_quantize", "mxfp4_gemv"):
         assert required in names
 
 
@@ -156,6 +158,17 @@ def test_matmul_host_rejects_bad_arguments_before_copying(lib):
     assert h(*good, 1, 260, 512, 128, A, B, None, 0, None) == UNSUPPORTED
     assert h(*good, 1, 256, 512, 128, A + 2, B, None, 0, None) == MISALIGNED
     assert h(*good, 1, 256, 512, 128, A, B, A, 0, None) == WORKSPACE
+
+
+def test_mxfp4_rejects_bad_arguments_on_host(lib):
+    q, g = lib.mxfp4_quantize, lib.mxfp4_gemv
+    assert q(A, 4, 256, None, A, None) == INVALID
+    assert q(A, 4, 48, A, A, None) == INVALID             # K % 32
+    assert q(A, 4, 256, A, A + 4, None) == MISALIGNED
+    assert g(A, A, A, None, 4, 256, None) == INVALID
+    assert g(A, A, A, B, 4, 96, None) == INVALID          # K % 128
+    assert g(A, A, A, B, 4, 128 * 2048, None) == UNSUPPORTED
+    assert g(A + 2, A, A, B, 4, 256, None) == MISALIGNED
 
 
 def test_workspace_query_is_host_only(lib):

@@ -105,3 +105,64 @@ def test_nvfp4_gemv_special_activations(w4):
     torch.cuda.synchronize()
     y_ref, a_ref = oracle.nvfp4_gemv(bits(x), c_np, s_np, S)
     assert oracle.within_tolerance(y.float().cpu().numpy(), y_ref, a_ref).all()
+
+
+# --------------------------------------------------------------------------- #
+# MXFP4 (E2M1 codes, E8M0 power-of-two scale per 32)
+# --------------------------------------------------------------------------- #
+
+def mx_special_weights(N, K, seed):
+    """Seeded weights with 0.1 % outliers, a zero block, blocks on the grid with exact ties,
+    a block needing the clamp at 6, and rows whose blocks differ by large powers of two."""
+    w = workloads.weights(N, K, seed=seed, outlier_frac=0.001).numpy().copy()
+    if N >= 4 and K >= 128:
+        w[0, :32] = 0.0
+        grid = np.array([6, 2.5, 5, 0.25, 0.75, 1.25, 1.75, 3.5, -2.5, -5, -0.25, -6, 0, 1, 4,
+                         -1.5] * 2)
+        w[1, :32] = grid * 2.0 ** -9
+        w[2, :32] = np.linspace(-0.9, 0.9, 32) * 2.0 ** -5  # 0.9 scaled past 6: clamped
+        w[3, :128] *= np.repeat(2.0 ** np.array([-30, 0, -12, 10]), 32)
+    return np.ascontiguousarray(w, dtype=np.float32)
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (100, 512), (1000, 4096), (7, 8224)])
+def test_mxfp4_quantize_bit_exact(w4, N, K):
+    w = mx_special_weights(N, K, seed=N + K)
+    c_ref, s_ref = oracle.mxfp4_quantize(w)
+    c, s = w4.mxfp4_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(s.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(c.cpu().numpy(), c_ref)
+
+
+def test_mxfp4_quantize_hand_worked_blocks(w4):
+    """The blocks of tests/golden/mxfp4_blocks.txt, one row each."""
+    import pins
+
+    recs = pins._records("mxfp4_blocks.txt")
+    w = np.stack([pins._weights_from(rec) for _, rec in recs]).astype(np.float32)
+    c, s = w4.mxfp4_quantize(torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    for i, (tag, rec) in enumerate(recs):
+        assert int(s.cpu().numpy()[i, 0]) == int(rec["scale"][0], 16), tag
+        assert [int(v) for v in c.cpu().numpy()[i]] == [int(v, 16) for v in rec["bytes"]], tag
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (333, 1024), (1000, 4224), (14336, 4096),
+                                 (40, 65536)])
+def test_mxfp4_gemv_every_output(w4, N, K):
+    w = mx_special_weights(N, K, seed=N * 7 + K)
+    c_np, s_np = oracle.mxfp4_quantize(w)
+    x = workloads.activations_bf16(1, K, seed=N)[0]
+    c, s = torch.from_numpy(c_np).cuda(), torch.from_numpy(s_np).cuda()
+    y = w4.mxfp4_gemv(x.cuda(), c, s)
+    y2 = w4.mxfp4_gemv(x.cuda(), c, s)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    y_ref, a_ref = oracle.mxfp4_gemv(bits(x), c_np, s_np)
+    yv = y.float().cpu().numpy()
+    ok = oracle.within_tolerance(yv, y_ref, a_ref)
+    if not ok.all():
+        bad = np.flatnonzero(~ok)[:5]
+        raise AssertionError(f"{int((~ok).sum())}/{ok.size} out of tolerance: "
+                             f"{[(int(n), float(yv[n]), float(y_ref[n])) for n in bad]}")
