@@ -1,8 +1,9 @@
-// NVFP4 weights with 16-bit activations (NVFP4A16): E2M1 codes, one E4M3 scale per 16
-// weights along K and one fp32 scale per tensor ("Hardware-invariant NVFP4 progress report
-// 1", "The NVFP4 layout"; "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured",
-// Step 6). The weight-only path decodes the codes to 16-bit floats and multiplies on the
-// half-precision tensor path:
+// 4-bit float weights with 16-bit activations: NVFP4A16 (E2M1 codes, one E4M3 scale per 16
+// weights along K and one fp32 scale per tensor: "Hardware-invariant NVFP4 progress report
+// 1", "The NVFP4 layout") and MXFP4A16 (E2M1 codes, one E8M0 power-of-two scale per 32:
+// "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured", Step 6). The weight-only
+// path decodes the codes to 16-bit floats and multiplies on the half-precision tensor path
+// (NVFP4 shown; MXFP4 has 2^(s - 127) per 32 and no S):
 //
 //   y[n] = S * sum_b e4m3(s[n, b]) * sum_{j < 16} e2m1(q[n, 16 b + j]) x[16 b + j]
 //
