@@ -11,8 +11,9 @@ around CUDA-graph replays that rotate over 12 weight copies (374 MB, more than t
 The same line carries the other steps of the hot path as "rows": GPU quantize and pack,
 the batch sweep M = 1..4096 against a BF16 cuBLAS matmul at the same M, the Q4 block-32
 quantize and GEMV (16384 x 16384), the zero-point format (quantize, layout move, matmul at
-M = 1, 16, 4096), the W8A16 per-row INT8, NVFP4A16 and MXFP4A16 quantize and GEMV, and the 196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph;
-each with its roofline fraction.
+M = 1, 16, 4096), the W8A16 per-row INT8, NVFP4A16 and MXFP4A16 quantize and GEMV, and the
+196-matmul Qwen2.5-1.5B-shaped decode stack in one CUDA graph (also with q/k/v and gate/up
+concatenated: 112 matmuls); each with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
   python bench.py --case gemv_m1 --launches 6     # a few untimed launches, for ncu
@@ -563,7 +564,35 @@ def rows_ours(peaks, device, stream):
                           "frac": round(tot_bytes / hbm / 1e3 / us_tok, 3),
                           "note": "weights (698 MB) > L2; one graph of 196 launches per token",
                           "pages": "3.68 ms for 197 matmuls (tinygemm, RTX 4060 Laptop)"}
+
+    # The same weights with the projections that share an input concatenated along N (q, k, v
+    # and gate, up: the quantization is per output column, so the fused matmul computes the
+    # same numbers): 4 launches per layer instead of 7.
+    per = len(workloads.QWEN_STACK["block"])
+    fused = []
+    for layer in range(workloads.QWEN_STACK["layers"]):
+        blk = stack[layer * per:(layer + 1) * per]
+        for group in ((0, 1, 2), (3,), (4, 5), (6,)):
+            parts = [blk[j] for j in group]
+            ql = torch.cat([p[1] for p in parts], dim=1).contiguous()
+            sl = torch.cat([p[2] for p in parts], dim=1).contiguous()
+            ml = torch.cat([p[3] for p in parts], dim=1).contiguous()
+            Kl, Nl = ql.shape[0] * 8, ql.shape[1]
+            yl = torch.empty(1, Nl, dtype=torch.bfloat16, device=device)
+            fused.append((parts[0][0], ql, sl, ml, yl, workspace_for(1, Nl, Kl, device)))
     del stack
+
+    def token_fused(i):
+        for (xl, ql, sl, ml, yl, wsl) in fused:
+            w4.w4a16_matmul(xl, ql, sl, ml, y=yl, workspace=wsl)
+
+    us_f = graph_time_us(token_fused, 1, 50, stream)
+    rows["qwen_stack_fused_qkv_gateup"] = {
+        "matmuls": len(fused), "us_per_token": round(us_f, 2), "bytes": tot_bytes,
+        "roofline_us": round(tot_bytes / hbm / 1e3, 2),
+        "frac": round(tot_bytes / hbm / 1e3 / us_f, 3),
+        "note": "same weights, q/k/v and gate/up concatenated along N: 112 launches per token"}
+    del fused
     return rows
 
 
