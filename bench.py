@@ -667,8 +667,9 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
-PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
-                 "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1", "nvfp4_gemv")
+PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
+                 "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
+                 "nvfp4_gemv")
 
 
 def profile_case(args):
@@ -704,8 +705,8 @@ def profile_case(args):
             cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(6)]
             for i in range(n):
                 w4.w4a16zp_matmul(x, *cps[i % 6])
-    elif case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m4096",
-                  "quantize", "pack"):
+    elif case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
+                  "tc_m4096", "quantize", "pack"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
         if case == "quantize":
@@ -717,7 +718,7 @@ def profile_case(args):
         else:
             del w, codes
             M = {"gemv_m1": 1, "gemv_m8": 8, "skinny_m16": 16, "skinny_m32": 32, "tc_m16": 16,
-                 "tc_m4096": 4096}[case]
+                 "tc_m64": 64, "tc_m4096": 4096}[case]
             if case == "tc_m16":  # the tensor-core kernel, not the skinny one the size picks
                 w4.testing_force_kernel(2)
             cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
