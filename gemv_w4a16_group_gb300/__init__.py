@@ -201,6 +201,9 @@ def w4a16_matmul_host(x_host: torch.Tensor, qw: torch.Tensor, scales: torch.Tens
     M, K = x_host.shape
     N = qw.shape[1]
     dev = qw.device
+    p_qw = _dev(qw, "qw", torch.int32, (K // 8, N))
+    p_s = _dev(scales, "scales", torch.bfloat16, (K // group, N))
+    p_m = _dev(mins, "mins", torch.bfloat16, (K // group, N))
     if y_host is None:
         y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     if y_host.is_cuda or y_host.dtype != torch.bfloat16 or tuple(y_host.shape) != (M, N) \
@@ -221,9 +224,7 @@ def w4a16_matmul_host(x_host: torch.Tensor, qw: torch.Tensor, scales: torch.Tens
             raise ValueError("workspace must be a contiguous CUDA tensor")
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check("w4a16_matmul_host", _lib.w4a16_matmul_host(
-        x_host.data_ptr(), _dev(qw, "qw", torch.int32, (K // 8, N)),
-        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
-        _dev(mins, "mins", torch.bfloat16, (K // group, N)), y_host.data_ptr(), M, N, K, group,
+        x_host.data_ptr(), p_qw, p_s, p_m, y_host.data_ptr(), M, N, K, group,
         _dev(x_dev, "x_dev", torch.bfloat16, (M, K)), _dev(y_dev, "y_dev", torch.bfloat16, (M, N)),
         ws_ptr, ws_bytes, _stream(stream)))
     return y_host

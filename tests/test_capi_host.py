@@ -185,3 +185,38 @@ def test_python_binding_refuses_cpu_tensors():
     s = torch.zeros(2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         w4.w4a16_matmul(x, qw, s, s)
+
+
+def test_every_binding_refuses_cpu_tensors():
+    """No entry point has a CPU path: each binding rejects host tensors before any call
+    (w4a16_matmul_host takes host x and y by design, but its weights must be on the GPU)."""
+    import torch
+
+    import gemv_w4a16_group_gb300 as w4
+
+    f32 = torch.zeros(16, 256)
+    bf = torch.zeros(256, dtype=torch.bfloat16)
+    u8 = torch.zeros(16, 128, dtype=torch.uint8)
+    calls = [
+        lambda: w4.w4a16zp_quantize(f32),
+        lambda: w4.w4a16zp_prepare(torch.zeros(16, 32, dtype=torch.int32),
+                                   torch.zeros(16, 2, dtype=torch.float16),
+                                   torch.zeros(16, 2, dtype=torch.float16)),
+        lambda: w4.w4a16zp_matmul(bf.reshape(1, -1), torch.zeros(32, 16, dtype=torch.int32),
+                                  torch.zeros(2, 16, dtype=torch.float16),
+                                  torch.zeros(2, 16, dtype=torch.float16)),
+        lambda: w4.w8a16_quantize(f32),
+        lambda: w4.w8a16_gemv(bf, torch.zeros(16, 256, dtype=torch.int8), torch.zeros(16)),
+        lambda: w4.nvfp4_quantize(f32),
+        lambda: w4.nvfp4_gemv(bf, u8, torch.zeros(16, 16, dtype=torch.uint8), torch.ones(1)),
+        lambda: w4.mxfp4_quantize(f32),
+        lambda: w4.mxfp4_gemv(bf, u8, torch.zeros(16, 8, dtype=torch.uint8)),
+        lambda: w4.w4a16_matmul_host(bf.reshape(1, -1), torch.zeros(32, 16, dtype=torch.int32),
+                                     torch.zeros(2, 16, dtype=torch.bfloat16),
+                                     torch.zeros(2, 16, dtype=torch.bfloat16),
+                                     x_dev=bf.reshape(1, -1),
+                                     y_dev=torch.zeros(1, 16, dtype=torch.bfloat16)),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
