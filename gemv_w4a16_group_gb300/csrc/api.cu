@@ -39,7 +39,7 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 // Kernel choice for w4a16_matmul: 0 = by M (default), 1 = small-M GEMV kernel,
 // 2 = TMA + tcgen05 tensor-core kernel.
 int g_force_kernel = 0;
-// M at or below which the CUDA-core GEMV runs when the choice is by M.
+// M at or below which the GEMV kernel (mma.sync inner products) runs when the choice is by M.
 int g_gemv_max_m = 8;
 int g_skinny_min_m = 9;
 int g_skinny_max_m = 32;

@@ -29,6 +29,10 @@
  *     that expired) are latched in a per-device status word that
  *     w4a16_device_status() reads and clears.
  *   - Weights must be finite.
+ *   - The library caches per-device addresses of its own device variables (the status word
+ *     and the scratch array of w4a16_matmul_noalloc) on first use. Resetting a device
+ *     (cudaDeviceReset) after the library has been used on it is not supported: the
+ *     cached addresses would no longer be valid.
  */
 #ifndef W4A16_GB300_H
 #define W4A16_GB300_H
@@ -184,8 +188,9 @@ w4a16_status w4a16zp_matmul(const uint16_t* x, const int32_t* qw, const uint16_t
  *   than 16 MiB of scratch.
  *   All calls on a device share that array: calls whose kernels may overlap on the GPU
  *   race, so order them (one stream, or events). Each call clears the counters it uses
- *   first. The first call on a device looks up the array's device address; make it
- *   before any stream capture.
+ *   first. The first call on a device looks up the array's device address and caches it
+ *   for the life of the process; make it before any stream capture, and do not reset the
+ *   device afterwards.
  */
 w4a16_status w4a16_matmul_noalloc(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
                                   const uint16_t* mins, uint16_t* y, int M, int N, int K,
