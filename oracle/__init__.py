@@ -79,6 +79,9 @@ def _bind(lib):
     lib.oracle_w4a16_dequant.argtypes = [P, P, P, I, I, I, P]
     lib.oracle_w4a16_matmul.argtypes = [P, P, P, P, I, I, I, I, P, P]
     lib.oracle_w4a16_matmul_cols.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
+    lib.oracle_w4a16_prepared_words.argtypes = [I, I, I]
+    lib.oracle_w4a16_prepared_words.restype = ctypes.c_long
+    lib.oracle_w4a16_prepare.argtypes = [P, P, P, I, I, I, P]
     lib.oracle_q4b32_quantize.argtypes = [P, I, I, P, P]
     lib.oracle_q4b32_dequant.argtypes = [P, P, I, I, P]
     lib.oracle_q4b32_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
@@ -106,7 +109,8 @@ def _bind(lib):
     lib.oracle_mxfp4_gemv.argtypes = [P, P, P, I, I, P, I, P, P]
     for name in ("oracle_bf16_rne_array", "oracle_fp16_rne_array", "oracle_fp16_to_float_array",
                  "oracle_w4a16_quantize", "oracle_w4a16_pack", "oracle_w4a16_dequant",
-                 "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_q4b32_quantize",
+                 "oracle_w4a16_matmul", "oracle_w4a16_matmul_cols", "oracle_w4a16_prepare",
+                 "oracle_q4b32_quantize",
                  "oracle_q4b32_dequant", "oracle_q4b32_gemv", "oracle_w4a16zp_quantize",
                  "oracle_w4a16zp_dequant", "oracle_w4a16zp_matmul", "oracle_w8a16_quantize",
                  "oracle_w8a16_gemv", "oracle_nvfp4_quantize", "oracle_nvfp4_dequant",
@@ -253,6 +257,26 @@ def w4a16_matmul(x_bits: np.ndarray, qw: np.ndarray, scales: np.ndarray, mins: n
         lib.oracle_w4a16_matmul_cols(_ptr(x_bits), _ptr(qw), _ptr(scales), _ptr(mins), M, N, K,
                                      group, _ptr(cols), len(cols), _ptr(y), _ptr(a))
     return y, a
+
+
+def w4a16_prepared_words(N: int, K: int, group: int = 128) -> int:
+    """uint32 words of the prepared layout: one 2176-word record per (128-column tile,
+    group of 128)."""
+    return int(_load().oracle_w4a16_prepared_words(N, K, group))
+
+
+def w4a16_prepare(qw: np.ndarray, scales: np.ndarray, mins: np.ndarray, group: int = 128) -> np.ndarray:
+    """Canonical (qw [K/8, N], BF16 scales and minimums [K/G, N]) -> the prepared layout,
+    uint32 [prepared_words] (see oracle_w4a16_prepare in w4a16_oracle.c)."""
+    qw = _c(qw, np.int32)
+    scales = _c(scales, np.uint16)
+    mins = _c(mins, np.uint16)
+    N = qw.shape[1]
+    K = qw.shape[0] * 8
+    assert K % group == 0
+    out = np.empty(w4a16_prepared_words(N, K, group), dtype=np.uint32)
+    _load().oracle_w4a16_prepare(_ptr(qw), _ptr(scales), _ptr(mins), N, K, group, _ptr(out))
+    return out
 
 
 # --------------------------------------------------------------------------- #

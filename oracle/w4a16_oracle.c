@@ -312,6 +312,73 @@ void oracle_w4a16_matmul_cols(const uint16_t* x, const int32_t* qw, const uint16
 }
 
 /* ------------------------------------------------------------------------ */
+/* Prepared (reordered) W4A16 layout ([P3] "What production kernels do": the  */
+/* weights are rearranged offline so that one wide read feeds the tensor-core */
+/* operand; [P1] "In the real world": reordered tiles whose nibbles convert   */
+/* with one mask-and-or; [P4] "Is it faster?": a handle that owns prepared    */
+/* weights). The same codes, scales and minimums, in another order:           */
+/*                                                                            */
+/*   Columns are cut into tiles of 128 (the last one padded with code 0,      */
+/*   scale 0, minimum 0) and K into groups of 128. Tile t, group g is one      */
+/*   record of 2176 uint32 words (8704 bytes, so 4.25 bits per weight), at    */
+/*   word offset (t * K/128 + g) * 2176:                                       */
+/*     word b*1024 + h*512 + n*4 + j   (b, h in {0,1}; n < 128; j < 4):        */
+/*       the 8 codes of column 128t + n at k = 128g + 64b + 8(4h + j) + 0..7, */
+/*       code of k0 + 2i in bits 4i..4i+3 and code of k0 + 2i + 1 in bits     */
+/*       16 + 4i..16 + 4i + 3 (i < 4): the even weights in the low half, the   */
+/*       odd ones in the high half;                                            */
+/*     word 2048 + n: BF16 scale of (g, column 128t + n) in bits 0..15, BF16   */
+/*       minimum in bits 16..31.                                               */
+/* ------------------------------------------------------------------------ */
+
+#define PREP_TILE 128
+#define PREP_RECORD_WORDS 2176
+
+long oracle_w4a16_prepared_words(int N, int K, int G) {
+  long tiles = (N + PREP_TILE - 1) / PREP_TILE;
+  return tiles * (long)(K / G) * PREP_RECORD_WORDS;
+}
+
+/* qw [K/8, N], scales / mins [K/G, N] (G = 128) -> prep (prepared_words words). */
+void oracle_w4a16_prepare(const int32_t* qw, const uint16_t* scales, const uint16_t* mins,
+                          int N, int K, int G, uint32_t* prep) {
+  int tiles = (N + PREP_TILE - 1) / PREP_TILE;
+  int groups = K / G;
+  for (int t = 0; t < tiles; ++t) {
+    for (int g = 0; g < groups; ++g) {
+      uint32_t* rec = prep + ((size_t)t * groups + g) * PREP_RECORD_WORDS;
+      for (int n = 0; n < PREP_TILE; ++n) {
+        int col = t * PREP_TILE + n;
+        for (int b = 0; b < 2; ++b) {
+          for (int h = 0; h < 2; ++h) {
+            for (int j = 0; j < 4; ++j) {
+              int k0 = g * G + 64 * b + 8 * (4 * h + j);
+              uint32_t word = 0;
+              for (int i = 0; i < 4; ++i) {
+                uint32_t even = 0, odd = 0;
+                if (col < N) {
+                  even = (uint32_t)unpack_code(qw, N, col, k0 + 2 * i);
+                  odd = (uint32_t)unpack_code(qw, N, col, k0 + 2 * i + 1);
+                }
+                word |= even << (4 * i);
+                word |= odd << (16 + 4 * i);
+              }
+              rec[b * 1024 + h * 512 + n * 4 + j] = word;
+            }
+          }
+        }
+        uint32_t s = 0, m = 0;
+        if (col < N) {
+          s = scales[(size_t)g * N + col];
+          m = mins[(size_t)g * N + col];
+        }
+        rec[2048 + n] = s | (m << 16);
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Q4 block-32 ([P2]): 32 codes + one FP16 scale, w_hat = (q - 8) * s.       */
 /* ------------------------------------------------------------------------ */
 

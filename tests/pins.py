@@ -129,6 +129,79 @@ def pin_pack_hand_worked_words():
     assert qw[0].tolist() == [0x11111111, 0x22222222, 0x33333333]
 
 
+def _prepared_golden():
+    """(total words, [(record, index, word)]) from tests/golden/w4a16_prepared_words.txt."""
+    total, words = None, []
+    with open(os.path.join(GOLDEN, "w4a16_prepared_words.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key == "words_total":
+                total = int(vals[0])
+            elif key == "word":
+                words.append((int(vals[0]), int(vals[1]), int(vals[2], 16)))
+    return total, words
+
+
+def pin_prepared_layout_golden_words():
+    """The prepared layout against hand-worked words (tests/golden/w4a16_prepared_words.txt):
+    nibble interleave, word order within a record, record order, the fused scale|minimum
+    words and the zero padding of a partial tile."""
+    N, K = 8, 256
+    codes = np.empty((N, K), dtype=np.uint8)
+    for n in range(N):
+        for k in range(K):
+            codes[n, k] = (n + k + k // 8) % 16
+    qw = oracle.w4a16_pack(codes)
+    g_idx = np.arange(K // 128).reshape(-1, 1)
+    n_idx = np.arange(N).reshape(1, -1)
+    s = (0x3C00 + n_idx + 16 * g_idx).astype(np.uint16)
+    m = (0xBC00 + n_idx + 16 * g_idx).astype(np.uint16)
+    prep = oracle.w4a16_prepare(qw, s, m)
+    total, words = _prepared_golden()
+    assert prep.size == total
+    for rec, idx, want in words:
+        got = int(prep[rec * 2176 + idx])
+        assert got == want, (rec, idx, hex(got), hex(want))
+
+
+def pin_prepared_layout_keeps_4_25_bits_and_every_weight():
+    """The prepared copy is 4.25 bits per weight ("Low-Precision Kernels ...", Step 2) when N
+    fills whole tiles, and it holds every code, scale and minimum exactly once: decoding
+    each weight from it gives the canonical layout's w_hat bit for bit (ragged N too)."""
+    for N, K in ((256, 256), (136, 384)):
+        w = workloads.weights(N, K, seed=N + K).numpy()
+        codes, s, m = oracle.w4a16_quantize(w)
+        qw = oracle.w4a16_pack(codes)
+        prep = oracle.w4a16_prepare(qw, s, m)
+        if N % 128 == 0:
+            assert prep.nbytes * 8 / (N * K) == 4.25
+        rec = prep.reshape(-1, K // 128, 2176)            # [tile][group][word]
+        cw = rec[:, :, :2048].reshape(-1, K // 128, 2, 2, 128, 4)  # [t][g][b][h][n][j]
+        got = np.empty((N, K), dtype=np.int64)
+        for t in range(rec.shape[0]):
+            for n in range(128):
+                col = 128 * t + n
+                if col >= N:
+                    assert not cw[t, :, :, :, n, :].any() and not rec[t, :, 2048 + n].any()
+                    continue
+                for g in range(K // 128):
+                    for b in range(2):
+                        for h in range(2):
+                            for j in range(4):
+                                word = int(cw[t, g, b, h, n, j])
+                                k0 = 128 * g + 64 * b + 8 * (4 * h + j)
+                                for i in range(4):
+                                    got[col, k0 + 2 * i] = (word >> (4 * i)) & 15
+                                    got[col, k0 + 2 * i + 1] = (word >> (16 + 4 * i)) & 15
+        assert np.array_equal(got, codes.astype(np.int64))
+        sm = rec[:, :, 2048:].transpose(1, 0, 2).reshape(K // 128, -1)[:, :N]
+        assert np.array_equal((sm & 0xFFFF).astype(np.uint16), s)
+        assert np.array_equal((sm >> 16).astype(np.uint16), m)
+
+
 def pin_sizes_printed_on_pages():
     """4.25 bits/weight, 3.76x, 31.2 MB, the 4 KB vs 16 KB tile, 18-byte Q4 blocks,
     3.56x and 144 MiB, all computed from the array sizes the oracle produces."""

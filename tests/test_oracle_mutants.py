@@ -98,6 +98,19 @@ MUTANTS = [
     ("mx_scale_code_off_by_one", "sc = X + 127;", "sc = X + 128;", None),
     ("zp_nibble_order_reversed", "(uint32_t)q << (4 * (k % 8));", "(uint32_t)q << (4 * (7 - k % 8));",
      None),
+    ("prep_even_odd_halves_swapped",
+     "word |= even << (4 * i);\n                word |= odd << (16 + 4 * i);",
+     "word |= odd << (4 * i);\n                word |= even << (16 + 4 * i);", None),
+    ("prep_words_reversed_in_quad", "int k0 = g * G + 64 * b + 8 * (4 * h + j);",
+     "int k0 = g * G + 64 * b + 8 * (4 * h + (3 - j));", None),
+    ("prep_halves_of_kblock_swapped", "int k0 = g * G + 64 * b + 8 * (4 * h + j);",
+     "int k0 = g * G + 64 * b + 8 * (4 * (1 - h) + j);", None),
+    ("prep_kblocks_swapped", "int k0 = g * G + 64 * b + 8 * (4 * h + j);",
+     "int k0 = g * G + 64 * (1 - b) + 8 * (4 * h + j);", None),
+    ("prep_scale_min_swapped", "rec[2048 + n] = s | (m << 16);", "rec[2048 + n] = m | (s << 16);",
+     None),
+    ("prep_pairs_adjacent_nibbles", "word |= even << (4 * i);\n                word |= odd << (16 + 4 * i);",
+     "word |= even << (8 * i);\n                word |= odd << (8 * i + 4);", None),
 ]
 
 
