@@ -217,6 +217,14 @@ def workspace_for(M, N, K, device):
     return torch.zeros(need, dtype=torch.uint8, device=device) if need else None
 
 
+def prepared_workspace_for(M, N, K, device):
+    """The workspace w4a16_matmul_prepared asks for at this shape (zero-filled), or None."""
+    import gemv_w4a16_group_gb300 as w4
+
+    need = w4.w4a16_matmul_prepared_workspace_bytes(M, N, K)
+    return torch.zeros(need, dtype=torch.uint8, device=device) if need else None
+
+
 def quantized_on_device(N, K, seed, device, outlier_frac=0.0):
     import gemv_w4a16_group_gb300 as w4
 
@@ -401,7 +409,13 @@ def rows_ours(peaks, device, stream):
     b = N * K + N * K // 2
     rows["w4a16_pack"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
                           "frac_hbm": round(b / us / 1e3 / hbm, 3)}
-    del w, codes, qw, s, m
+    # prepared (reordered) copy of the same packed weights
+    prep = w4.w4a16_prepare(qw, s, m)
+    us = graph_time_us(lambda i: w4.w4a16_prepare(qw, s, m, prepared=prep), 4, 5, stream)
+    b = 2 * weight_bytes(N, K)  # canonical bytes read, the same bytes written reordered
+    rows["w4a16_prepare"] = {"shape": [N, K], "us": round(us, 2), "GBps": round(b / us / 1e3, 1),
+                             "frac_hbm": round(b / us / 1e3 / hbm, 3)}
+    del w, codes, qw, s, m, prep
 
     # batch sweep with outliers, against BF16 cuBLAS at the same M
     cfg = workloads.BATCH_SWEEP
@@ -410,6 +424,7 @@ def rows_ours(peaks, device, stream):
     w_bf16 = w.to(torch.bfloat16)
     del w, codes
     cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(ROTATE)]
+    preps = [w4.w4a16_prepare(*c) for c in cps]
     bf_cps = [w_bf16.clone() for _ in range(3)]  # 3 x 117 MB > 2 x L2
     sweep = []
     for M in cfg["Ms"]:
@@ -423,17 +438,31 @@ def rows_ours(peaks, device, stream):
                               6 if big else 12, 2 if big else 10, stream)
         bts, fl = w4a16_bytes(M, N, K), 2 * M * N * K
         roof = roofline_us(bts, fl, peaks)
+        prepared = None
+        if w4.w4a16_matmul_prepared_uses_prepared(M):
+            wsp = prepared_workspace_for(M, N, K, device)
+            us_p = graph_time_us(
+                lambda i: w4.w4a16_matmul_prepared(x, *cps[i % ROTATE], preps[i % ROTATE], y=y,
+                                                   workspace=wsp),
+                ROTATE if big else 4 * ROTATE, 2 if big else 10, stream)
+            prepared = {"us": round(us_p, 2), "frac": round(roof / us_p, 3),
+                        "speedup_vs_bf16": round(us_bf / us_p, 2) if us_bf else None}
         sweep.append({"M": M, "us": round(us, 2), "TFLOPS": round(fl / us / 1e6, 1),
                       "GBps": round(bts / us / 1e3, 1), "roofline_us": round(roof, 2),
                       "frac": round(roof / us, 3),
                       "bound": "hbm" if bts / (peaks["hbm_gbs"] * 1e3) >= fl / (peaks["bf16_tflops"] * 1e6) else "tensor",
                       "bf16_cublas_us": round(us_bf, 2),
                       "bf16_cublas_TFLOPS": round(fl / us_bf / 1e6, 1),
-                      "speedup_vs_bf16": round(us_bf / us, 2)})
+                      "speedup_vs_bf16": round(us_bf / us, 2),
+                      "prepared_layout": prepared})
         del x, y
-    del cps, bf_cps, w_bf16
+    del cps, preps, bf_cps, w_bf16
     rows["batch_sweep"] = sweep
-    even = [r["M"] for r in sweep if r["speedup_vs_bf16"] <= 1.0]
+    def best_us(r):
+        p = r.get("prepared_layout")
+        return min(r["us"], p["us"]) if p else r["us"]
+
+    even = [r["M"] for r in sweep if r["bf16_cublas_us"] <= best_us(r)]
     bpw = 4.25 / 8
     rows["crossover"] = {
         "predicted_4bit_ridge_M": round(peaks["bf16_tflops"] * 1e12 * bpw / (2 * peaks["hbm_gbs"] * 1e9), 1),

@@ -42,7 +42,10 @@ __all__ = [
     "w4a16_selftest_bounded_wait", "testing_force_kernel", "testing_set_gemv_max_m",
     "testing_set_q4_variant", "testing_set_skinny_range", "w4a16zp_quantize",
     "w4a16zp_prepare", "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
-    "nvfp4_gemv", "mxfp4_quantize", "mxfp4_gemv",
+    "nvfp4_gemv", "mxfp4_quantize", "mxfp4_gemv", "w4a16_prepared_bytes", "w4a16_prepare",
+    "w4a16_matmul_prepared", "w4a16_matmul_prepared_workspace_bytes",
+    "testing_set_prepared_min_m", "testing_set_prepared_max_m",
+    "w4a16_matmul_prepared_uses_prepared",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -86,17 +89,23 @@ def _load():
         "nvfp4_gemv": [P, P, P, P, P, I, I, P],
         "mxfp4_quantize": [P, I, I, P, P, P],
         "mxfp4_gemv": [P, P, P, P, I, I, P],
+        "w4a16_prepare": [P, P, P, I, I, I, P, S, P],
+        "w4a16_matmul_prepared": [P, P, P, P, P, P, I, I, I, I, P, S, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
-    lib.w4a16_matmul_workspace_bytes.argtypes = [I, I, I, I]
-    lib.w4a16_matmul_workspace_bytes.restype = S
+    for name in ("w4a16_matmul_workspace_bytes", "w4a16_matmul_prepared_workspace_bytes"):
+        getattr(lib, name).argtypes = [I, I, I, I]
+        getattr(lib, name).restype = S
+    lib.w4a16_prepared_bytes.argtypes = [I, I, I]
+    lib.w4a16_prepared_bytes.restype = S
     lib.w4a16_status_string.argtypes = [I]
     lib.w4a16_status_string.restype = ctypes.c_char_p
     for name in ("w4a16_testing_force_kernel", "w4a16_testing_set_gemv_max_m",
-                 "w4a16_testing_set_q4_variant"):
+                 "w4a16_testing_set_q4_variant", "w4a16_testing_set_prepared_min_m",
+                 "w4a16_testing_set_prepared_max_m"):
         getattr(lib, name).argtypes = [I]
         getattr(lib, name).restype = I
     lib.w4a16_testing_set_skinny_range.argtypes = [I, I]
@@ -184,6 +193,89 @@ def w4a16_matmul(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor, mins: 
         _dev(mins, "mins", torch.bfloat16, (K // group, N)),
         _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
     return y
+
+
+def _workspace(workspace):
+    if workspace is None:
+        return None, 0
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def w4a16_prepared_bytes(N: int, K: int, group: int = 128) -> int:
+    """Bytes of the prepared (reordered) copy of an N x K weight matrix."""
+    return int(_lib.w4a16_prepared_bytes(N, K, group))
+
+
+def w4a16_prepare(qw: torch.Tensor, scales: torch.Tensor, mins: torch.Tensor, group: int = 128,
+                  prepared=None, stream=None) -> torch.Tensor:
+    """Packed weights (qw int32 [K/8, N], scales / mins bf16 [K/group, N]) -> the prepared
+    copy, uint8 [w4a16_prepared_bytes(N, K)] (records of 128 columns x 128 k; see
+    include/w4a16.h)."""
+    N = qw.shape[1]
+    K = qw.shape[0] * 8
+    nbytes = w4a16_prepared_bytes(N, K, group)
+    if prepared is None:
+        prepared = torch.empty(nbytes, dtype=torch.uint8, device=qw.device)
+    if not (isinstance(prepared, torch.Tensor) and prepared.is_cuda and prepared.is_contiguous()):
+        raise ValueError("prepared must be a contiguous CUDA tensor")
+    _check("w4a16_prepare", _lib.w4a16_prepare(
+        _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)), N, K, group, prepared.data_ptr(),
+        prepared.numel() * prepared.element_size(), _stream(stream)))
+    return prepared
+
+
+def w4a16_matmul_prepared_workspace_bytes(M: int, N: int, K: int, group: int = 128) -> int:
+    return int(_lib.w4a16_matmul_prepared_workspace_bytes(M, N, K, group))
+
+
+def w4a16_matmul_prepared(x: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor,
+                          mins: torch.Tensor, prepared, group: int = 128, y=None,
+                          workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] (bf16) = x [M, K] (bf16) . w_hat^T, reading the prepared copy of the weights
+    (from w4a16_prepare) at the batch sizes where the prepared-layout kernel runs, and
+    (qw, scales, mins) below them."""
+    M, K = x.shape
+    N = qw.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    p_prep = None
+    if prepared is not None:
+        if not (isinstance(prepared, torch.Tensor) and prepared.is_cuda and prepared.is_contiguous()):
+            raise ValueError("prepared must be a contiguous CUDA tensor")
+        if prepared.numel() * prepared.element_size() < w4a16_prepared_bytes(N, K, group):
+            raise ValueError("prepared is smaller than w4a16_prepared_bytes(N, K)")
+        p_prep = prepared.data_ptr()
+    ws_ptr, ws_bytes = _workspace(workspace)
+    _check("w4a16_matmul_prepared", _lib.w4a16_matmul_prepared(
+        _dev(x, "x", torch.bfloat16), _dev(qw, "qw", torch.int32, (K // 8, N)),
+        _dev(scales, "scales", torch.bfloat16, (K // group, N)),
+        _dev(mins, "mins", torch.bfloat16, (K // group, N)), p_prep,
+        _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, group, ws_ptr, ws_bytes, _stream(stream)))
+    return y
+
+
+def w4a16_matmul_prepared_uses_prepared(M: int) -> bool:
+    """Whether w4a16_matmul_prepared runs the prepared-layout kernel at this M (else it is
+    w4a16_matmul on the canonical arrays)."""
+    lo = int(_lib.w4a16_testing_set_prepared_min_m(0))
+    hi = int(_lib.w4a16_testing_set_prepared_max_m(0))
+    return lo <= M <= hi
+
+
+def testing_set_prepared_min_m(m: int) -> int:
+    """Smallest M that w4a16_matmul_prepared sends to the prepared-layout kernel; returns the
+    previous value (m < 1 only queries)."""
+    return int(_lib.w4a16_testing_set_prepared_min_m(m))
+
+
+def testing_set_prepared_max_m(m: int) -> int:
+    """Largest M that w4a16_matmul_prepared sends to the prepared-layout kernel; returns the
+    previous value (m < 1 only queries)."""
+    return int(_lib.w4a16_testing_set_prepared_max_m(m))
 
 
 def w4a16_matmul_host(x_host: torch.Tensor, qw: torch.Tensor, scales: torch.Tensor,

@@ -43,6 +43,12 @@ int g_force_kernel = 0;
 int g_gemv_max_m = 8;
 int g_skinny_min_m = 9;
 int g_skinny_max_m = 32;
+// Range of M for which w4a16_matmul_prepared runs the prepared-layout tensor-core kernel
+// (measured on the 14336 x 4096 layer: 1.6-1.7x the canonical path at M = 48..128, even at
+// 32, the skinny kernel ahead at 16 and below, a tie from 192).
+int g_prep_min_m = 32;
+int g_prep_max_m = 128;
+bool prep_by_m(int M) { return M >= g_prep_min_m && M <= g_prep_max_m; }
 
 // The skinny kernel keeps its converted activations in the workspace past a reserve it
 // never writes: the split-K kernels keep their arrival counters (which must stay zero
@@ -262,6 +268,61 @@ w4a16_status w4a16_matmul_host(const uint16_t* x_host, const int32_t* qw, const 
   return from_cuda(cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, s));
 }
 
+size_t w4a16_prepared_bytes(int N, int K, int group) {
+  if (group != 128 || N <= 0 || K <= 0 || K % group != 0) return 0;
+  return w4k::w4a16_prepared_bytes(N, K);
+}
+
+w4a16_status w4a16_prepare(const int32_t* qw, const uint16_t* scales, const uint16_t* mins,
+                           int N, int K, int group, void* prepared, size_t prepared_bytes,
+                           w4a16_stream_t stream) {
+  if (!qw || !scales || !mins || !prepared) return W4A16_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 128) return W4A16_ERR_UNSUPPORTED;
+  if (prepared_bytes < w4k::w4a16_prepared_bytes(N, K)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(qw) || !aligned16(scales) || !aligned16(mins) || !aligned16(prepared))
+    return W4A16_ERR_MISALIGNED;
+  return from_cuda(w4k::launch_w4a16_prepare(reinterpret_cast<const uint32_t*>(qw), scales, mins,
+                                             N, K, static_cast<uint32_t*>(prepared),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_matmul_prepared_workspace_bytes(int M, int N, int K, int group) {
+  if (M <= 0 || N <= 0 || K <= 0 || group != 128 || K % group != 0) return 0;
+  if (!prep_by_m(M)) return w4a16_matmul_workspace_bytes(M, N, K, group);
+  w4k::TcpPlan plan;
+  if (!w4k::tcp_plan(M, N, K, w4k::device_sm_count(), true, &plan)) return 0;
+  return plan.ws_bytes;
+}
+
+w4a16_status w4a16_matmul_prepared(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                                   const uint16_t* mins, const void* prepared, uint16_t* y, int M,
+                                   int N, int K, int group, void* workspace,
+                                   size_t workspace_bytes, w4a16_stream_t stream) {
+  if (prepared == nullptr || !prep_by_m(M))
+    return matmul_impl(x, qw, scales, mins, y, M, N, K, group, workspace, workspace_bytes, stream,
+                       false);
+  if (!x || !qw || !scales || !mins || !y) return W4A16_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || group <= 0 || K % group != 0) return W4A16_ERR_INVALID_ARG;
+  if (group != 128 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(mins) ||
+      !aligned16(y) || !aligned16(prepared))
+    return W4A16_ERR_MISALIGNED;
+  if ((workspace == nullptr) != (workspace_bytes == 0)) return W4A16_ERR_WORKSPACE;
+  if (workspace != nullptr && !aligned16(workspace)) return W4A16_ERR_MISALIGNED;
+  uint32_t* status = status_word_ptr();
+  if (status == nullptr) return W4A16_ERR_CUDA;
+  const int sms = w4k::device_sm_count();
+  w4k::TcpPlan plan;
+  if (!w4k::tcp_plan(M, N, K, sms, workspace != nullptr, &plan)) return W4A16_ERR_UNSUPPORTED;
+  if (plan.stream_k && workspace_bytes < plan.ws_bytes &&
+      !w4k::tcp_plan(M, N, K, sms, false, &plan))
+    return W4A16_ERR_UNSUPPORTED;
+  return from_cuda(w4k::launch_w4a16_tcp(x, static_cast<const uint32_t*>(prepared), y, M, N, K,
+                                         plan, workspace, status, g_wait_limit_ns,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status w4a16zp_quantize(const float* w, int N, int K, int group, uint32_t* qw_rows,
                               uint16_t* scales, uint16_t* zeros, w4a16_stream_t stream) {
   if (!w || !qw_rows || !scales || !zeros) return W4A16_ERR_INVALID_ARG;
@@ -437,6 +498,18 @@ int w4a16_testing_set_skinny_range(int lo, int hi) {
     g_skinny_min_m = lo;
     g_skinny_max_m = hi;
   }
+  return prev;
+}
+
+int w4a16_testing_set_prepared_min_m(int m) {
+  const int prev = g_prep_min_m;
+  if (m >= 1) g_prep_min_m = m;
+  return prev;
+}
+
+int w4a16_testing_set_prepared_max_m(int m) {
+  const int prev = g_prep_max_m;
+  if (m >= 1) g_prep_max_m = m;
   return prev;
 }
 

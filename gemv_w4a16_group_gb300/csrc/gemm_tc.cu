@@ -203,9 +203,13 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % kStages, sa = kb % kAStages;
-      if (!mbar_wait_bounded(&full[s], (kb / kStages) & 1u, abort_flag, status, limit_ns) ||
-          (kb >= kAStages && !mbar_wait_bounded(&aempty[sa], ((kb / kAStages) - 1) & 1u,
-                                                abort_flag, status, limit_ns))) {
+      bool got = mbar_wait_bounded(&full[s], (kb / kStages) & 1u, abort_flag, status, limit_ns) &&
+                 (kb < kAStages || mbar_wait_bounded(&aempty[sa], ((kb / kAStages) - 1) & 1u,
+                                                     abort_flag, status, limit_ns));
+      // Lanes leave the waits at different times; the TMEM store below is .sync.aligned and
+      // must be executed by the whole warp together.
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
         ok = false;
         break;
       }
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
           }
         }
       }
+      __syncwarp();
       if constexpr (kParts == 1)
         tmem_st_32cols(lane_base + L::a_col0 + sa * 32, out);
       else
@@ -254,7 +259,8 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
       if (lane == 0) mbar_arrive(&afull[sa]);
     }
     // Epilogue: accumulator lane `row` holds y[m0 + j, n0 + row] in column j.
-    const bool have_acc = ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns);
+    const bool have_acc =
+        __all_sync(0xffffffffu, ok && mbar_wait_bounded(accfull, 0u, abort_flag, status, limit_ns));
     const int n = n0 + row;
     constexpr int kChunks = BM >= 32 ? BM / 32 : 1;
     if (have_acc) tc_fence_after_sync();
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
 #pragma unroll 1
         for (int c = part; c < kChunks; c += kParts) {
           uint32_t v[32];
+          __syncwarp();
           tmem_ld_32cols(lane_base + c * 32, v);  // BM < 32: columns >= BM are never stored
           tmem_ld_wait();
           if (n < N) {
@@ -285,6 +292,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
 #pragma unroll 1
         for (int c = part; c < kChunks; c += kParts) {
           uint32_t v[32];
+          __syncwarp();
           tmem_ld_32cols(lane_base + c * 32, v);
           tmem_ld_wait();
           if (n < N) {
@@ -297,6 +305,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
         }
       }
       __threadfence();
+      __syncwarp();
       asm volatile("bar.sync 2, %0;" ::"n"(kDequantWarps * 32) : "memory");
       uint32_t* tile_count = ws_counter + blockIdx.y * gridDim.x + blockIdx.x;
       // Low 16 bits count arrivals; a CTA without a valid partial also sets bit 16.
@@ -304,6 +313,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
         const uint32_t inc = have_acc ? 1u : 0x10001u;
         *reinterpret_cast<volatile uint32_t*>(tmem_holder + 2) = atomicAdd(tile_count, inc) + inc;
       }
+      __syncwarp();
       asm volatile("bar.sync 2, %0;" ::"n"(kDequantWarps * 32) : "memory");
       const uint32_t after = *reinterpret_cast<volatile uint32_t*>(tmem_holder + 2);
       const bool last = (after & 0xFFFFu) == static_cast<uint32_t>(splits);
@@ -350,6 +360,7 @@ __global__ void __launch_bounds__(Roles<BM>::kThreads, Roles<BM>::kMinBlocks)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) {
+    __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::tmem_cols);
   }

@@ -35,9 +35,9 @@ EncodeTiledFn encode_fn() {
 
 struct MapKey {
   const void* base;
-  uint64_t inner, outer, row_bytes;
-  uint32_t box_inner, box_outer;
-  int dtype, swizzle;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  int rank, dtype, swizzle;
 };
 
 struct MapKeyEq {
@@ -71,17 +71,23 @@ std::mutex g_smem_mu;
 
 }  // namespace
 
-cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
-                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+namespace {
+
+// Tiled descriptor of a rank-2 or rank-3 tensor (dims innermost first, byte strides of the
+// outer dims), unit element strides, out-of-bounds elements read as zero; cached by its
+// arguments.
+cudaError_t encode_cached(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int rank,
+                          const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                          CUtensorMapSwizzle swizzle) {
   MapKey key;
   std::memset(&key, 0, sizeof(key));  // padding bytes take part in the comparison
   key.base = base;
-  key.inner = inner;
-  key.outer = outer;
-  key.row_bytes = row_bytes;
-  key.box_inner = box_inner;
-  key.box_outer = box_outer;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides[i];
   key.dtype = static_cast<int>(dt);
   key.swizzle = static_cast<int>(swizzle);
   {
@@ -94,11 +100,15 @@ cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const vo
   }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3];
+  const cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+  CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -106,6 +116,23 @@ cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const vo
   if (g_maps.size() >= kMaxMaps) g_maps.clear();
   g_maps[key] = *map;
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {row_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_cached(map, dt, base, 2, dims, strides, box, swizzle);
+}
+
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                                 const uint64_t dims[3], const uint64_t strides[2],
+                                 const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  return encode_cached(map, dt, base, 3, dims, strides, box, swizzle);
 }
 
 cudaError_t set_max_dynamic_smem(const void* func, int bytes) {

@@ -16,6 +16,11 @@ namespace w4k {
 cudaError_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
                               uint64_t inner, uint64_t outer, uint64_t row_bytes,
                               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// The same for a rank-3 tensor: dims innermost first, byte strides of dims 1 and 2 (any
+// order), box per dim.
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                                 const uint64_t dims[3], const uint64_t strides[2],
+                                 const uint32_t box[3], CUtensorMapSwizzle swizzle);
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device, size).
 cudaError_t set_max_dynamic_smem(const void* func, int bytes);
 
@@ -115,6 +120,30 @@ cudaError_t launch_w4a16_skinny(const uint16_t* x, const uint32_t* qw, const uin
                                 void* workspace, const SkinnyPlan& plan, uint32_t* status,
                                 uint64_t wait_limit_ns, cudaStream_t stream,
                                 bool zero_point = false);
+
+// Prepared (reordered) W4A16 layout: 128-column x 128-k records of 8704 bytes (codes with
+// the even weights in the low half of each word, then one scale|minimum word per column),
+// and the persistent tensor-core matmul that reads it (prepared.cu). The plan fixes the
+// batch tile (BN rows, the MMA's N), the unit grid and, with a workspace, the stream-K
+// split: arrival counters (zero before the launch; the kernel leaves them zero) and two
+// fp32 partial tiles per CTA.
+struct TcpPlan {
+  int bn = 0;        // batch rows per tile
+  int P = 0;         // row tiles
+  int T = 0;         // 128-column tiles
+  int ctas = 0;
+  bool stream_k = false;
+  size_t counter_bytes = 0;
+  size_t ws_bytes = 0;  // 0 without stream-K
+};
+size_t w4a16_prepared_bytes(int N, int K);
+int tcp_block_n(int M);
+bool tcp_plan(int M, int N, int K, int sms, bool want_stream, TcpPlan* plan);
+cudaError_t launch_w4a16_prepare(const uint32_t* qw, const uint16_t* scales, const uint16_t* mins,
+                                 int N, int K, uint32_t* prep, cudaStream_t stream);
+cudaError_t launch_w4a16_tcp(const uint16_t* x, const uint32_t* prep, uint16_t* y, int M, int N,
+                             int K, const TcpPlan& plan, void* workspace, uint32_t* status,
+                             uint64_t wait_limit_ns, cudaStream_t stream);
 
 // Q4 block-32 GEMV.
 cudaError_t launch_q4b32_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,

@@ -134,6 +134,62 @@ w4a16_status w4a16_matmul_host(const uint16_t* x_host, const int32_t* qw, const 
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);
 
 /*
+ * Prepared (reordered) weights ("Quantization and GEMV", "What production kernels do": the
+ * weights are rearranged once, offline, so that the kernel's wide reads feed the tensor-core
+ * operand; "Low-Precision Kernels ...", "In the real world": reordered tiles whose nibbles
+ * convert with one mask-and-or; "Hardware-invariant NVFP4 progress report 1", "Is it
+ * faster?": a handle that owns prepared weights). The same codes, scales and minimums as
+ * (qw, scales, mins), 4.25 bits per weight, in records of 128 columns x 128 k:
+ *   record (t, g), at byte (t * K/128 + g) * 8704, is 2176 uint32 words:
+ *     word b*1024 + h*512 + n*4 + j (b, h < 2, n < 128, j < 4) holds the 8 codes of column
+ *       128 t + n at k = 128 g + 64 b + 8 (4 h + j) + 0..7: the code of k0 + 2i in bits
+ *       4i..4i+3, the code of k0 + 2i + 1 in bits 16 + 4i..16 + 4i + 3;
+ *     word 2048 + n: the BF16 scale of (g, column 128 t + n) in bits 0..15 and its BF16
+ *       minimum in bits 16..31.
+ *   Columns past N (in the last tile) hold code 0, scale 0 and minimum 0.
+ *
+ * w4a16_prepared_bytes -- bytes of the prepared copy: ceil(N / 128) * (K / 128) * 8704
+ *   (0 for unsupported arguments: group != 128, K % 128 != 0).
+ */
+size_t w4a16_prepared_bytes(int N, int K, int group);
+
+/*
+ * w4a16_prepare -- writes the prepared copy of packed weights (one kernel, asynchronous).
+ *   qw int32 [K/8, N], scales / mins bf16 [K/group, N] (as for w4a16_matmul)
+ *   prepared: caller-owned device buffer of at least w4a16_prepared_bytes(N, K, group)
+ *   bytes, 16-byte aligned, not overlapping the inputs.
+ * Returns W4A16_ERR_INVALID_ARG if prepared_bytes is too small. Requires N > 0, K > 0,
+ * group == 128, K % group == 0.
+ */
+w4a16_status w4a16_prepare(const int32_t* qw, const uint16_t* scales, const uint16_t* mins,
+                           int N, int K, int group, void* prepared, size_t prepared_bytes,
+                           w4a16_stream_t stream);
+
+/*
+ * w4a16_matmul_prepared -- y = x . W_hat^T as w4a16_matmul, with the prepared copy of the
+ * same weights at hand. For 32 <= M <= 128 (by default) it runs the persistent tensor-core
+ * kernel that reads `prepared` (TMA + tcgen05, rebuilt weights in tensor memory, fp32
+ * sums); for other M, or with prepared == NULL, it is exactly w4a16_matmul on (qw, scales,
+ * mins). Same tolerance and determinism as w4a16_matmul.
+ *   x bf16 [M, K]; qw, scales, mins as for w4a16_matmul; prepared from w4a16_prepare on the
+ *   same weights; y bf16 [M, N].
+ *   workspace / workspace_bytes: optional caller-owned device scratch sized with
+ *   w4a16_matmul_prepared_workspace_bytes(); for shapes with fewer 128-column tiles than half
+ *   the SMs it lets the kernel split K evenly over the SMs (per-tile arrival counters and fp32
+ *   partial tiles). Zero-fill it before its first use and do not share it with calls that may
+ *   run concurrently or with other entry points. NULL (with 0 bytes) is accepted: the kernel
+ *   then gives each CTA whole tiles.
+ * Requires M > 0, N > 0, K > 0, group == 128, K % group == 0, N % 8 == 0.
+ */
+w4a16_status w4a16_matmul_prepared(const uint16_t* x, const int32_t* qw, const uint16_t* scales,
+                                   const uint16_t* mins, const void* prepared, uint16_t* y,
+                                   int M, int N, int K, int group, void* workspace,
+                                   size_t workspace_bytes, w4a16_stream_t stream);
+
+/* Bytes of workspace that let w4a16_matmul_prepared balance this shape (0 = none needed). */
+size_t w4a16_matmul_prepared_workspace_bytes(int M, int N, int K, int group);
+
+/*
  * Zero-point format ("Quantization and GEMV", "The quantization formulas" and "W4A16:
  * dequantizing in registers"): w_hat = (q - z) * s with one FP16 scale s and one FP16
  * zero point z per group of 128 weights along K (4.25 bits per weight).

@@ -30,6 +30,12 @@ int w4a16_testing_set_gemv_max_m(int m);
  * Returns the previous range as (lo << 8) | hi. */
 int w4a16_testing_set_skinny_range(int lo, int hi);
 
+/* Range of M for which w4a16_matmul_prepared runs the prepared-layout kernel (default
+ * 32..128): smallest and largest M; values below 1 only query. Each returns the previous
+ * value. */
+int w4a16_testing_set_prepared_min_m(int m);
+int w4a16_testing_set_prepared_max_m(int m);
+
 /* Kernel of q4b32_gemv: 2 = TMA-staged tensor-pipe kernel (default; shapes it does not
  * take fall back to 1), 1 = CUDA-core kernel with mixed FP16 FMAs, 0 = CUDA-core kernel
  * with packed fp32 FMAs. Other values only query. Returns the previous value. */

@@ -47,6 +47,12 @@ def lib(cuda_lib):
     lib.w4a16_matmul_host.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, S, P]
     lib.mxfp4_quantize.argtypes = [P, I, I, P, P, P]
     lib.mxfp4_gemv.argtypes = [P, P, P, P, I, I, P]
+    lib.w4a16_prepare.argtypes = [P, P, P, I, I, I, P, S, P]
+    lib.w4a16_matmul_prepared.argtypes = [P, P, P, P, P, P, I, I, I, I, P, S, P]
+    lib.w4a16_prepared_bytes.argtypes = [I, I, I]
+    lib.w4a16_prepared_bytes.restype = S
+    lib.w4a16_matmul_prepared_workspace_bytes.argtypes = [I, I, I, I]
+    lib.w4a16_matmul_prepared_workspace_bytes.restype = S
     return lib
 
 
@@ -56,7 +62,9 @@ def test_header_declares_the_boundary():
                      "q4b32_quantize", "w4a16_matmul_workspace_bytes", "w4a16_device_status",
                      "w4a16_status_string", "w4a16zp_quantize", "w4a16zp_prepare",
                      "w4a16zp_matmul", "w8a16_quantize", "w8a16_gemv", "nvfp4_quantize",
-                     "nvfp4_gemv", "w4a16_matmul_host", "mxfp4_quantize", "mxfp4_gemv"):
+                     "nvfp4_gemv", "w4a16_matmul_host", "mxfp4_quantize", "mxfp4_gemv",
+                     "w4a16_prepared_bytes", "w4a16_prepare", "w4a16_matmul_prepared",
+                     "w4a16_matmul_prepared_workspace_bytes"):
         assert required in names
 
 
@@ -169,6 +177,34 @@ def test_mxfp4_rejects_bad_arguments_on_host(lib):
     assert g(A, A, A, B, 4, 96, None) == INVALID          # K % 128
     assert g(A, A, A, B, 4, 128 * 2048, None) == UNSUPPORTED
     assert g(A + 2, A, A, B, 4, 256, None) == MISALIGNED
+
+
+def test_prepared_entry_points_reject_bad_arguments_on_host(lib):
+    """The prepared layout's size rule (4.25 bits per weight in 128 x 128 records) and the
+    host-side checks of w4a16_prepare and w4a16_matmul_prepared."""
+    nb = lib.w4a16_prepared_bytes
+    assert nb(14336, 4096, 128) == 31_195_136           # the canonical bytes, reordered
+    assert nb(136, 256, 128) == 2 * 2 * 8704            # a partial last tile is padded
+    assert nb(256, 200, 128) == 0 and nb(256, 256, 64) == 0 and nb(0, 256, 128) == 0
+    p = lib.w4a16_prepare
+    need = nb(256, 512, 128)
+    assert p(A, A, A, 256, 512, 128, None, need, None) == INVALID
+    assert p(A, A, A, 256, 500, 128, B, need, None) == INVALID          # K % group
+    assert p(A, A, A, 256, 512, 64, B, need, None) == UNSUPPORTED
+    assert p(A, A, A, 256, 512, 128, B, need - 16, None) == INVALID     # buffer too small
+    assert p(A, A + 4, A, 256, 512, 128, B, need, None) == MISALIGNED
+    assert p(A, A, A, 256, 512, 128, B + 8, need, None) == MISALIGNED
+    m = lib.w4a16_matmul_prepared
+    good = (A, A, A, A, A, B)
+    assert m(None, A, A, A, A, B, 64, 256, 512, 128, None, 0, None) == INVALID
+    assert m(*good, 64, 256, 500, 128, None, 0, None) == INVALID
+    assert m(*good, 64, 260, 512, 128, None, 0, None) == UNSUPPORTED
+    assert m(*good, 64, 256, 512, 64, None, 0, None) == UNSUPPORTED
+    assert m(A, A, A, A, A + 8, B, 64, 256, 512, 128, None, 0, None) == MISALIGNED
+    assert m(*good, 64, 256, 512, 128, A, 0, None) == WORKSPACE
+    assert m(*good, 64, 256, 512, 128, A + 4, 64, None) == MISALIGNED
+    # below the threshold (and with no prepared copy) it is w4a16_matmul's checks
+    assert m(A, A, A, A, None, B, 1, 260, 512, 128, None, 0, None) == UNSUPPORTED
 
 
 def test_workspace_query_is_host_only(lib):
