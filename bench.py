@@ -741,7 +741,7 @@ def run_reference(args, world, rank):
 
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
                  "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
-                 "nvfp4_gemv")
+                 "nvfp4_gemv", "prep_m64", "prep_m128", "tc_m128", "prepare")
 
 
 def profile_case(args):
@@ -777,8 +777,25 @@ def profile_case(args):
             cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(6)]
             for i in range(n):
                 w4.w4a16zp_matmul(x, *cps[i % 6])
+    elif case in ("prep_m64", "prep_m128", "prepare"):
+        N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+        w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
+        del w, codes
+        if case == "prepare":
+            prep = w4.w4a16_prepare(qw, s, m)
+            for _ in range(n):
+                w4.w4a16_prepare(qw, s, m, prepared=prep)
+        else:
+            M = 64 if case == "prep_m64" else 128
+            cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
+            preps = [w4.w4a16_prepare(*c) for c in cps]
+            x = workloads.activations_bf16(M, K, seed=M).to(device)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            ws = prepared_workspace_for(M, N, K, device)
+            for i in range(n):
+                w4.w4a16_matmul_prepared(x, *cps[i % 6], preps[i % 6], y=y, workspace=ws)
     elif case in ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
-                  "tc_m4096", "quantize", "pack"):
+                  "tc_m128", "tc_m4096", "quantize", "pack"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
         if case == "quantize":
@@ -790,7 +807,7 @@ def profile_case(args):
         else:
             del w, codes
             M = {"gemv_m1": 1, "gemv_m8": 8, "skinny_m16": 16, "skinny_m32": 32, "tc_m16": 16,
-                 "tc_m64": 64, "tc_m4096": 4096}[case]
+                 "tc_m64": 64, "tc_m128": 128, "tc_m4096": 4096}[case]
             if case == "tc_m16":  # the tensor-core kernel, not the skinny one the size picks
                 w4.testing_force_kernel(2)
             cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
