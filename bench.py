@@ -741,21 +741,21 @@ def run_reference(args, world, rank):
 
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
                  "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
-                 "nvfp4_gemv", "prep_m64", "prep_m128", "tc_m128", "prepare")
+                 "nvfp4_gemv", "mxfp4_gemv", "prep_m64", "prep_m128", "tc_m128", "prepare")
 
 
 def profile_case(args):
     """A few launches of one workload, untimed, for a profiler (ncu -k ... -c ...): the
     Llama-3-8B up-projection (14336 x 4096) at M = 1, 8, 16 or 32 (skinny kernel), 16
     (tensor-core kernel) or 4096 with 6 rotating weight copies (174 MB > L2), the Q4
-    block-32 GEMV (16384 x 16384), quantize / pack, the W8A16 GEMV or the zero-point
+    block-32 GEMV (16384 x 16384), quantize / pack, the W8A16, NVFP4 or MXFP4 GEMV or the zero-point
     matmul at M = 1 on the same layer."""
     import gemv_w4a16_group_gb300 as w4
 
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     case, n = args.case, args.launches
-    if case in ("w8a16_gemv", "zp_m1", "nvfp4_gemv"):
+    if case in ("w8a16_gemv", "zp_m1", "nvfp4_gemv", "mxfp4_gemv"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w = workloads.weights(N, K, seed=0).to(device)
         x = workloads.activations_bf16(1, K, seed=1).to(device)
@@ -765,6 +765,12 @@ def profile_case(args):
             cps = [(c4.clone(), s4.clone(), S4.clone()) for _ in range(6)]
             for i in range(n):
                 w4.nvfp4_gemv(x[0], *cps[i % 6])
+        elif case == "mxfp4_gemv":
+            cm, sm_ = w4.mxfp4_quantize(w)
+            del w
+            cps = [(cm.clone(), sm_.clone()) for _ in range(6)]
+            for i in range(n):
+                w4.mxfp4_gemv(x[0], *cps[i % 6])
         elif case == "w8a16_gemv":
             q8, s8 = w4.w8a16_quantize(w)
             del w

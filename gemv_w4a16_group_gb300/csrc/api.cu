@@ -390,17 +390,26 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int g_fp4_variant = 1;
+
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, uint16_t* y, int N, int K,
                         w4a16_stream_t stream) {
   if (!x || !codes || !scales || !tensor_scale || !y) return W4A16_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0 || K % 128 != 0) return W4A16_ERR_INVALID_ARG;
-  if (w4k::nvfp4_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(tensor_scale) ||
       !aligned16(y))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(w4k::launch_nvfp4_gemv(x, codes, scales, tensor_scale, y, N, K,
-                                          reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g_fp4_variant == 1 && w4k::fp4_tc_supports(N, K, false)) {
+    uint32_t* status = status_word_ptr();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(w4k::launch_fp4_gemv_tc(x, codes, scales, tensor_scale, y, N, K, false,
+                                             status, g_wait_limit_ns, s));
+  }
+  // K % 512 != 0 or x too long for the ring beside it: the plain-load kernel.
+  if (w4k::nvfp4_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
+  return from_cuda(w4k::launch_nvfp4_gemv(x, codes, scales, tensor_scale, y, N, K, s));
 }
 
 w4a16_status mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
@@ -416,11 +425,17 @@ w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* 
                         uint16_t* y, int N, int K, w4a16_stream_t stream) {
   if (!x || !codes || !scales || !y) return W4A16_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0 || K % 128 != 0) return W4A16_ERR_INVALID_ARG;
-  if (w4k::nvfp4_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(
-      w4k::launch_mxfp4_gemv(x, codes, scales, y, N, K, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g_fp4_variant == 1 && w4k::fp4_tc_supports(N, K, true)) {
+    uint32_t* status = status_word_ptr();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(w4k::launch_fp4_gemv_tc(x, codes, scales, nullptr, y, N, K, true, status,
+                                             g_wait_limit_ns, s));
+  }
+  if (w4k::nvfp4_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
+  return from_cuda(w4k::launch_mxfp4_gemv(x, codes, scales, y, N, K, s));
 }
 
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
@@ -516,6 +531,12 @@ int w4a16_testing_set_prepared_max_m(int m) {
 int w4a16_testing_set_q4_variant(int v) {
   const int prev = g_q4_variant;
   if (v >= 0 && v <= 2) g_q4_variant = v;
+  return prev;
+}
+
+int w4a16_testing_set_fp4_variant(int v) {
+  const int prev = g_fp4_variant;
+  if (v >= 0 && v <= 1) g_fp4_variant = v;
   return prev;
 }
 

@@ -1,0 +1,531 @@
+// NVFP4A16 / MXFP4A16 GEMV on a TMA ring: y[n] = S sum_b e4m3(s[n,b]) sum_{j<16} e2m1(q) x
+// (NVFP4, "Hardware-invariant NVFP4 progress report 1", "The NVFP4 layout") or
+// y[n] = sum_b 2^(s[n,b] - 127) sum_{j<32} e2m1(q) x (MXFP4, "Low-Precision Kernels: INT4,
+// INT8 and FP8 Matmuls, Measured", Step 6).
+//
+// The codes are laid out like the Q4 block-32 format ([N, K/2], byte j of a row holding k = 2j
+// in its low nibble), so this kernel streams them the way the Q4 tensor-pipe GEMV does: work
+// units of T tiles of 16 rows and all of K, a producer warp copying 512-k chunks by TMA (two
+// 128-byte-wide code boxes with the 128-byte swizzle, one box of block scales) into a ring,
+// consumer lanes (gq, c) reading word c of a 32-k block of rows gq and gq + 8 of a tile, two
+// m16n8k16 MMAs per block (FP16 x FP16 -> fp32; x fills the n8 columns).
+//
+//   * Warps: T x P consumer warps, warp (t, p) taking tile t and the 32-k blocks p, p + P, ...
+//     of every chunk, with (T, P) picked per shape from (1, 16), (2, 8), (3, 8), (4, 4),
+//     (6, 4), (8, 2), (12, 2) so that the units spread over the SMs and 16 or 24 warps
+//     compute (the loop is latency-bound: more warps, not fewer instructions, is what moved
+//     it). Per unit the P partial sums of a row are added in a fixed order; no atomics.
+//   * A byte of two codes becomes an FP16 pair in one cvt.rn.f16x2.e2m1x2 (natural k order,
+//     so x waits in shared memory in natural order, 8 k per 16 bytes).
+//   * NVFP4: the E4M3 scale of the 16-k block a word belongs to (words 0, 1 and 2, 3 of a
+//     32-k block are its two 16-k blocks) multiplies the word's pairs in FP16, exactly (an
+//     E2M1 value has 2 significant bits and an E4M3 scale 4; their product lies between 2^-10
+//     and 2688, inside FP16's normal range), and x is FP16 under one power of two for the
+//     whole vector (largest |x| in [2^14, 2^15)), so the MMAs accumulate a unit's rows over
+//     all of K with no per-block fold (four independent accumulator chains); the tensor scale
+//     and the power of two multiply each output once.
+//   * MXFP4: x is FP16 under a power of two per 32-k block, each 32-k block's MMAs start
+//     from zero, and the block's power-of-two scale times the x scale multiplies its fp32 sum
+//     (lane c folds the c-th block of each group of four, like the Q4 scale).
+//   * The codes carry no offset, so there is no correction term.
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4k {
+namespace {
+
+constexpr int kFMaxWarps = 24;  // consumer warps of the widest configuration
+constexpr int kFBoxK = 256;     // 128 code bytes per row: one 128-byte swizzle row
+constexpr int kFChunkK = 512;   // two code boxes per chunk
+constexpr int kFBlocks = kFChunkK / 32;  // 32-k blocks per chunk
+constexpr int kFMaxStages = 12;
+constexpr uint32_t kFSmem = 227u * 1024u - 1024u;  // the base is aligned up to 1024 B
+
+// Shared-memory layout for T tiles per unit and K; sb = scale bytes per row and chunk (32 for
+// NVFP4's 32 E4M3 scales of 512 k, 16 for MXFP4's E8M0 ones).
+struct FLayout {
+  uint32_t code_bytes, scale_bytes, stage_bytes, red_off, cst_off, xperm_off, bar_off, total;
+  __host__ __device__ FLayout(int T, int K, int stages, int sb) {
+    code_bytes = 4096u * static_cast<uint32_t>(T);  // two boxes of 16 T rows x 128 B
+    scale_bytes = static_cast<uint32_t>(sb) * 16u * static_cast<uint32_t>(T);
+    stage_bytes = (code_bytes + scale_bytes + 1023u) & ~1023u;
+    red_off = static_cast<uint32_t>(stages) * stage_bytes;          // [P][16 T] fp32
+    cst_off = red_off + 16u * kFMaxWarps * 4u;                      // [K/32] 2^-e
+    xperm_off = (cst_off + (static_cast<uint32_t>(K) / 32u) * 4u + 15u) & ~15u;
+    bar_off = (xperm_off + (static_cast<uint32_t>(K) / 8u) * 16u + 7u) & ~7u;
+    total = bar_off + 2u * kFMaxStages * 8u + 16u;
+  }
+};
+
+__device__ __forceinline__ void f_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f_lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 f_lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t f_lds_u8(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t f_lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// FP16 pairs of the four bytes of `w` (byte j -> (code 2j, code 2j + 1)).
+__device__ __forceinline__ void f_e2m1_pairs(uint32_t w, uint32_t (&p)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+      : "r"(w));
+}
+
+// FP16 pair of the two E4M3 bytes in the low 16 bits of `v`.
+__device__ __forceinline__ uint32_t f_e4m3_pair(uint32_t v) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t, u;\n\tmov.b32 {t, u}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f_hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f_pow2(int e) {  // 2^e for -126 <= e <= 127
+  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
+// e with amax 2^e in [2^14, 2^15) (0 for amax = 0), kept where 2^e and 2^-e are normal.
+__device__ __forceinline__ int f_x_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  return max(-100, min(100, 141 - static_cast<int>(__float_as_uint(amax) >> 23)));
+}
+
+// The 8 BF16 values of a 16-byte segment as floats.
+__device__ __forceinline__ void f_bf16x8(uint4 in, float (&v)[8]) {
+  const uint32_t xw[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    v[2 * h] = __uint_as_float(xw[h] << 16);
+    v[2 * h + 1] = __uint_as_float(xw[h] & 0xFFFF0000u);
+  }
+}
+
+// 8 floats times sc, as FP16 (exact for BF16 inputs scaled into FP16's normal range).
+__device__ __forceinline__ uint4 f_f16x8(const float (&v)[8], float sc) {
+  return make_uint4(f_f16x2(v[0] * sc, v[1] * sc), f_f16x2(v[2] * sc, v[3] * sc),
+                    f_f16x2(v[4] * sc, v[5] * sc), f_f16x2(v[6] * sc, v[7] * sc));
+}
+
+// 2^(code - 127) for an E8M0 code (0..254; code 0 is 2^-127, a subnormal float).
+__device__ __forceinline__ float f_e8m0(uint32_t code) {
+  return __uint_as_float(code == 0u ? 0x00400000u : (code << 23));
+}
+
+template <int NT>
+__device__ __forceinline__ void f_consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+struct FMaps {
+  CUtensorMap codes;   // uint8 [N, K/2], box {128, 16 T}, 128-byte swizzle
+  CUtensorMap scales;  // uint8 [N, K/16] (NVFP4) or [N, K/32] (MXFP4), box {32 or 16, 16 T}
+};
+
+template <bool MX, int T, int P>
+__global__ void __launch_bounds__(T * P * 32 + 32, 1)
+    fp4_gemv_tc_kernel(const __grid_constant__ FMaps maps, const uint16_t* __restrict__ x,
+                       const float* __restrict__ tensor_scale, uint16_t* __restrict__ y, int N,
+                       int K, int nunits, int stages, uint32_t* __restrict__ status,
+                       uint64_t limit_ns) {
+  constexpr int W = T * P;            // consumer warps
+  constexpr int NC = W * 32;          // consumer threads
+  constexpr int NB = kFBlocks / P;    // 32-k blocks of a chunk per warp
+  constexpr int SB = MX ? 16 : 32;    // scale bytes per row and chunk
+  constexpr int ROWS = 16 * T;        // rows per unit
+  static_assert(kFBlocks % P == 0 && W <= kFMaxWarps, "bad warp split");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const FLayout L(T, K, stages, SB);
+  float* sRed = reinterpret_cast<float*>(smem + L.red_off);  // [P][ROWS]
+  float* sCst = reinterpret_cast<float*>(smem + L.cst_off);  // [K/32] 2^-e (NVFP4: [0] only)
+  uint4* sX = reinterpret_cast<uint4*>(smem + L.xperm_off);  // [K/8] FP16, natural order
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + kFMaxStages;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kFMaxStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kchunks = K / kFChunkK;
+  const uint32_t tx_bytes = L.code_bytes + L.scale_bytes;
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], W);
+    }
+    *abort_flag = 0u;
+    fence_barrier_init();
+    pdl_launch_dependents();
+  }
+  __syncthreads();
+
+  if (warp == W) {
+    // ---------------- producer: weights only, no wait on the previous kernel -----------
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.codes);
+      tma_prefetch_desc(&maps.scales);
+      int j = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int row0 = u * ROWS;
+        for (int kc = 0; kc < kchunks; ++kc, ++j) {
+          const int s = j % stages;
+          const uint32_t use = static_cast<uint32_t>(j / stages);
+          if (use > 0 &&
+              !mbar_wait_bounded(&empty[s], (use - 1) & 1u, abort_flag, status, limit_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* buf = smem + s * L.stage_bytes;
+          mbar_arrive_expect_tx(&full[s], tx_bytes);
+          tma_load_2d(buf, &maps.codes, &full[s], kc * (kFChunkK / 2), row0);
+          tma_load_2d(buf + L.code_bytes / 2, &maps.codes, &full[s],
+                      kc * (kFChunkK / 2) + kFBoxK / 2, row0);
+          tma_load_2d(buf + L.code_bytes, &maps.scales, &full[s], kc * SB, row0);
+        }
+      }
+      // Stay until this CTA's last copies have landed (bounded).
+      const int issued = j;
+      for (int s = 0; s < stages && s < issued; ++s) {
+        const int last = (issued - 1 - s) / stages;
+        volatile uint32_t no_abort = 0u;
+        mbar_wait_bounded(&full[s], static_cast<uint32_t>(last) & 1u, &no_abort, status,
+                          limit_ns);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  pdl_wait();  // x and y may belong to the previous kernel on the stream
+  const int segs = K / 8;  // segment R = 8 k
+  if constexpr (MX) {
+    // x (BF16) -> FP16 in natural order with a power-of-two scale per 32-k block, the 4
+    // segments of a block on 4 adjacent lanes (segs and the thread count are multiples of
+    // 32, so a warp is either wholly inside x or wholly past it).
+    for (int base = 0; base < segs; base += NC) {
+      const int R = base + tid;
+      if (R >= segs) break;  // warp-uniform
+      float v[8];
+      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+      float amax = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int e = f_x_exponent(amax);
+      sX[R] = f_f16x8(v, f_pow2(e));
+      if ((R & 3) == 0) sCst[R >> 2] = f_pow2(-e);
+    }
+  } else {
+    // x (BF16) -> FP16 in natural order under one power of two for the whole vector (largest
+    // |x| in [2^14, 2^15)). Pass 1 finds the largest |x|, pass 2 converts.
+    float amax = 0.f;
+    for (int R = tid; R < segs; R += NC) {
+      float v[8];
+      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) sRed[warp] = amax;
+    f_consumer_bar<NC>();
+    amax = sRed[0];
+#pragma unroll
+    for (int w = 1; w < W; ++w) amax = fmaxf(amax, sRed[w]);
+    const int e = f_x_exponent(amax);
+    const float sc = f_pow2(e);
+    for (int R = tid; R < segs; R += NC) {
+      float v[8];
+      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+      sX[R] = f_f16x8(v, sc);
+    }
+    if (tid == 0) sCst[0] = f_pow2(-e);
+  }
+  f_consumer_bar<NC>();
+
+  const int gq = lane >> 2, c = lane & 3;
+  const int t = warp % T, p = warp / T;  // tile in the unit, first 32-k block in a chunk
+  const uint32_t rowA = static_cast<uint32_t>(16 * t + gq);  // rowB = rowA + 8
+  // Per block r of this warp (block p + P r of a chunk): the offset of row rowA's word c in
+  // a stage (rows gq and gq + 8 share the 128-byte swizzle phase gq = row mod 8), and of
+  // this lane's 16 bytes of x in a chunk.
+  uint32_t code_off[NB], x_off[NB];
+#pragma unroll
+  for (int r = 0; r < NB; ++r) {
+    const uint32_t j = static_cast<uint32_t>(p + P * r);
+    code_off[r] = (j >> 3) * (L.code_bytes / 2) + rowA * 128u +
+                  (((j & 7u) ^ static_cast<uint32_t>(gq)) << 4) + 4u * static_cast<uint32_t>(c);
+    x_off[r] = (j * 4u + static_cast<uint32_t>(c)) * 16u;
+  }
+  // NVFP4: words c = 0, 1 of a 32-k block hold its first 16-k block, c = 2, 3 its second;
+  // this selector duplicates the lane's byte of a block's two scale bytes.
+  const uint32_t ssel = static_cast<uint32_t>(c >> 1) * 0x11u;
+  const uint32_t ring_base = smem_addr(smem);
+  const uint32_t xbase = smem_addr(sX);
+  const float S = MX ? 1.0f : __ldg(tensor_scale) * sCst[0];
+  int s = 0;
+  uint32_t phase = 0u;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const int row0 = u * ROWS;
+    float accA = 0.f, accB = 0.f;  // MX: rows rowA, rowB, this lane's blocks
+    // NVFP4: the unit's sums (every lane), in four independent MMA chains (block parity x
+    // first / second MMA of a block), added at the end
+    float dacc[4][4] = {};
+    for (int kc = 0; kc < kchunks; ++kc) {
+      // On an expired wait every warp keeps walking without computing, so all consumer
+      // warps still meet at the per-unit barriers below.
+      const bool landed = mbar_wait_bounded(&full[s], phase, abort_flag, status, limit_ns);
+      const uint32_t buf = ring_base + static_cast<uint32_t>(s) * L.stage_bytes;
+      const uint32_t sbox = buf + L.code_bytes;  // [16 T rows][SB bytes]
+      const uint32_t xk = xbase + static_cast<uint32_t>(kc) * (kFBlocks * 64u);
+      if (landed) {
+        if constexpr (!MX) {
+#pragma unroll
+          for (int r = 0; r < NB; ++r) {
+            const uint32_t j = static_cast<uint32_t>(p + P * r);
+            const uint32_t w0 = f_lds32(buf + code_off[r]);
+            const uint32_t w1 = f_lds32(buf + code_off[r] + 1024u);
+            const uint4 e = f_lds128(xk + x_off[r]);
+            const uint32_t qa = f_lds_u16(sbox + rowA * SB + 2u * j);
+            const uint32_t qb = f_lds_u16(sbox + (rowA + 8u) * SB + 2u * j);
+            const uint32_t sA = f_e4m3_pair(__byte_perm(qa, 0u, ssel));
+            const uint32_t sB = f_e4m3_pair(__byte_perm(qb, 0u, ssel));
+            uint32_t p0[4], p1[4];
+            f_e2m1_pairs(w0, p0);
+            f_e2m1_pairs(w1, p1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              p0[i] = f_hmul2(p0[i], sA);
+              p1[i] = f_hmul2(p1[i], sB);
+            }
+            // k-slots (2c, 2c + 1) and (2c + 8, 2c + 9) of an MMA hold k = 8c + 0, 1 and
+            // 8c + 2, 3 (first MMA) or 8c + 4, 5 and 8c + 6, 7 (second): x in natural order.
+            f_mma(dacc[2 * (r & 1)], p0[0], p1[0], p0[1], p1[1], e.x, e.y);
+            f_mma(dacc[2 * (r & 1) + 1], p0[2], p1[2], p0[3], p1[3], e.z, e.w);
+          }
+        } else {
+          constexpr int G = NB < 4 ? NB : 4;  // blocks per fold group
+#pragma unroll
+          for (int i = 0; i < NB / G; ++i) {
+            float d[G][4];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const int r = G * i + g;
+              const uint32_t w0 = f_lds32(buf + code_off[r]);
+              const uint32_t w1 = f_lds32(buf + code_off[r] + 1024u);
+              const uint4 e = f_lds128(xk + x_off[r]);
+              uint32_t p0[4], p1[4];
+              f_e2m1_pairs(w0, p0);
+              f_e2m1_pairs(w1, p1);
+#pragma unroll
+              for (int f = 0; f < 4; ++f) d[g][f] = 0.f;
+              f_mma(d[g], p0[0], p1[0], p0[1], p1[1], e.x, e.y);
+              f_mma(d[g], p0[2], p1[2], p0[3], p1[3], e.z, e.w);
+            }
+            // Lane c folds block G i + c of the group for both rows (its D equals the other
+            // lanes'); with fewer than four blocks in a group the other lanes add nothing.
+            if (c < G) {
+              float dA = d[0][0], dB = d[0][2];
+#pragma unroll
+              for (int g = 1; g < G; ++g) {
+                if (c == g) {
+                  dA = d[g][0];
+                  dB = d[g][2];
+                }
+              }
+              const uint32_t j = static_cast<uint32_t>(p + P * (G * i + c));
+              const float u2 = sCst[kc * kFBlocks + static_cast<int>(j)];
+              const float sA = f_e8m0(f_lds_u8(sbox + rowA * SB + j));
+              const float sB = f_e8m0(f_lds_u8(sbox + (rowA + 8u) * SB + j));
+              accA = fmaf(sA * u2, dA, accA);
+              accB = fmaf(sB * u2, dB, accB);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == stages) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if constexpr (MX) {
+      // Row sums: the 4 lanes of a row group (fixed order).
+      accA += __shfl_xor_sync(0xffffffffu, accA, 1);
+      accA += __shfl_xor_sync(0xffffffffu, accA, 2);
+      accB += __shfl_xor_sync(0xffffffffu, accB, 1);
+      accB += __shfl_xor_sync(0xffffffffu, accB, 2);
+    } else {
+      // column 2c of D; every column holds the same sums
+      accA = (dacc[0][0] + dacc[1][0]) + (dacc[2][0] + dacc[3][0]);
+      accB = (dacc[0][2] + dacc[1][2]) + (dacc[2][2] + dacc[3][2]);
+    }
+    if (c == 0) {
+      sRed[p * ROWS + static_cast<int>(rowA)] = accA;
+      sRed[p * ROWS + static_cast<int>(rowA) + 8] = accB;
+    }
+    f_consumer_bar<NC>();
+    // then the P parts of each row (fixed order)
+    for (int i = tid; i < ROWS; i += NC) {
+      const int n = row0 + i;
+      if (n < N) {
+        float v = sRed[i];
+#pragma unroll
+        for (int q = 1; q < P; ++q) v += sRed[q * ROWS + i];
+        y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(S * v));
+      }
+    }
+    f_consumer_bar<NC>();
+  }
+}
+
+struct FCfg {
+  int T, P;
+};
+// (tiles per unit, k-parts per chunk), by growing T; 16 or 24 consumer warps each.
+constexpr FCfg kFCfgs[] = {{1, 16}, {2, 8}, {3, 8}, {4, 4}, {6, 4}, {8, 2}, {12, 2}};
+constexpr int kFNumCfgs = static_cast<int>(sizeof(kFCfgs) / sizeof(kFCfgs[0]));
+
+struct FPlan {
+  int cfg = -1, nunits = 0, stages = 0;
+};
+
+// The smallest unit (T tiles of 16 rows) that spreads the rows over the SMs in one wave,
+// else the largest; then the largest unit no larger than that whose ring of at least two
+// stages fits beside x; the deepest such ring.
+FPlan f_plan(int N, int K, int sms, int sb) {
+  FPlan p;
+  if (K % kFChunkK != 0 || N <= 0 || sms <= 0) return p;
+  const int tiles = (N + 15) / 16;
+  const int need = (tiles + sms - 1) / sms;
+  int ci = 0;
+  while (ci + 1 < kFNumCfgs && kFCfgs[ci].T < need) ++ci;
+  for (; ci >= 0; --ci) {
+    const int T = kFCfgs[ci].T;
+    const uint32_t fixed = FLayout(T, K, 0, sb).total;
+    const uint32_t stage = FLayout(T, K, 0, sb).stage_bytes;
+    int stages = fixed < kFSmem ? static_cast<int>((kFSmem - fixed) / stage) : 0;
+    if (stages > kFMaxStages) stages = kFMaxStages;
+    if (stages >= 2) {
+      p.cfg = ci;
+      p.nunits = (tiles + T - 1) / T;
+      p.stages = stages;
+      return p;
+    }
+  }
+  return p;
+}
+
+template <bool MX, int T, int P>
+cudaError_t launch_fp4(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                       const float* tensor_scale, uint16_t* y, int N, int K, const FPlan& plan,
+                       int sms, uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  constexpr int SB = MX ? 16 : 32;
+  FMaps maps;
+  cudaError_t e = encode_tensor_map(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes,
+                                    static_cast<uint64_t>(K) / 2, static_cast<uint64_t>(N),
+                                    static_cast<uint64_t>(K) / 2, kFBoxK / 2,
+                                    static_cast<uint32_t>(16 * T), CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const uint64_t srow = MX ? static_cast<uint64_t>(K) / 32 : static_cast<uint64_t>(K) / 16;
+  e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, srow,
+                        static_cast<uint64_t>(N), srow, static_cast<uint32_t>(SB),
+                        static_cast<uint32_t>(16 * T), CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  const uint32_t smem = FLayout(T, K, plan.stages, SB).total + 1024u;
+  auto kern = fp4_gemv_tc_kernel<MX, T, P>;
+  e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = plan.nunits < sms ? plan.nunits : sms;
+  return launch_with_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T * P * 32 + 32), smem,
+                         stream, maps, x, tensor_scale, y, N, K, plan.nunits, plan.stages,
+                         status, limit_ns);
+}
+
+template <bool MX>
+cudaError_t launch_fp4_cfg(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                           const float* tensor_scale, uint16_t* y, int N, int K,
+                           const FPlan& plan, int sms, uint32_t* status, uint64_t limit_ns,
+                           cudaStream_t stream) {
+#define W4K_FP4_CASE(I, T_, P_)                                                       \
+  case I:                                                                             \
+    return launch_fp4<MX, T_, P_>(x, codes, scales, tensor_scale, y, N, K, plan, sms, \
+                                  status, limit_ns, stream);
+  switch (plan.cfg) {
+    W4K_FP4_CASE(0, 1, 16)
+    W4K_FP4_CASE(1, 2, 8)
+    W4K_FP4_CASE(2, 3, 8)
+    W4K_FP4_CASE(3, 4, 4)
+    W4K_FP4_CASE(4, 6, 4)
+    W4K_FP4_CASE(5, 8, 2)
+    W4K_FP4_CASE(6, 12, 2)
+    default:
+      return cudaErrorNotSupported;
+  }
+#undef W4K_FP4_CASE
+}
+
+}  // namespace
+
+bool fp4_tc_supports(int N, int K, bool mx) {
+  return f_plan(N, K, device_sm_count(), mx ? 16 : 32).cfg >= 0;
+}
+
+cudaError_t launch_fp4_gemv_tc(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                               const float* tensor_scale, uint16_t* y, int N, int K, bool mx,
+                               uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  const FPlan plan = f_plan(N, K, sms, mx ? 16 : 32);
+  if (plan.cfg < 0) return cudaErrorNotSupported;
+  if (mx)
+    return launch_fp4_cfg<true>(x, codes, scales, nullptr, y, N, K, plan, sms, status,
+                                wait_limit_ns, stream);
+  return launch_fp4_cfg<false>(x, codes, scales, tensor_scale, y, N, K, plan, sms, status,
+                               wait_limit_ns, stream);
+}
+
+}  // namespace w4k

@@ -182,6 +182,15 @@ cudaError_t launch_mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, 
 cudaError_t launch_mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                               uint16_t* y, int N, int K, cudaStream_t stream);
 
+// NVFP4 (mx = false) / MXFP4 (mx = true) GEMV on the tensor pipe (TMA-staged, mma.sync
+// FP16 -> fp32), M = 1. Needs K % 512 == 0 and x, its per-block constants and a two-stage
+// ring in shared memory; fp4_tc_supports() tells. `tensor_scale` is read for NVFP4 only.
+// Bounded waits report through `status`.
+bool fp4_tc_supports(int N, int K, bool mx);
+cudaError_t launch_fp4_gemv_tc(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                               const float* tensor_scale, uint16_t* y, int N, int K, bool mx,
+                               uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -2,10 +2,10 @@
  * w4a16_testing.h -- test and benchmark hooks of the GB300 W4A16 library.
  *
  * Not part of the stable API (w4a16.h). They change process-global choices that
- * w4a16_matmul and q4b32_gemv read on the host before each launch, so they must not be
- * called while another host thread is issuing those calls. The pages have no
- * counterpart: they exist so that tests can check every kernel at every shape and the
- * benchmark can compare the kernels.
+ * w4a16_matmul, q4b32_gemv, nvfp4_gemv and mxfp4_gemv read on the host before each
+ * launch, so they must not be called while another host thread is issuing those calls.
+ * The pages have no counterpart: they exist so that tests can check every kernel at every
+ * shape and the benchmark can compare the kernels.
  */
 #ifndef W4A16_GB300_TESTING_H
 #define W4A16_GB300_TESTING_H
@@ -40,6 +40,11 @@ int w4a16_testing_set_prepared_max_m(int m);
  * take fall back to 1), 1 = CUDA-core kernel with mixed FP16 FMAs, 0 = CUDA-core kernel
  * with packed fp32 FMAs. Other values only query. Returns the previous value. */
 int w4a16_testing_set_q4_variant(int v);
+
+/* Kernel of nvfp4_gemv and mxfp4_gemv: 1 = TMA-staged tensor-pipe kernel (default; shapes
+ * it does not take, K % 512 != 0 or x too long for its ring, fall back to 0), 0 = the
+ * plain-load kernel. Other values only query. Returns the previous value. */
+int w4a16_testing_set_fp4_variant(int v);
 
 #ifdef __cplusplus
 }

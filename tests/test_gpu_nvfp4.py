@@ -24,6 +24,15 @@ def w4():
     return mod
 
 
+@pytest.fixture(params=[1, 0], ids=["ring", "plain"])
+def fp4_variant(request, w4):
+    """Run the GEMV test through the tensor-pipe ring kernel (shapes it does not take fall
+    back to the plain-load kernel) and through the plain-load kernel."""
+    prev = w4.testing_set_fp4_variant(request.param)
+    yield request.param
+    w4.testing_set_fp4_variant(prev)
+
+
 def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -70,9 +79,13 @@ def test_nvfp4_quantize_hand_worked_tensors(w4):
         assert [int(v) for v in c.cpu().numpy()[0, :16]] == [int(v, 16) for v in rec["bytes"]], tag
 
 
-@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (333, 1024), (1000, 4224), (4096, 4096),
-                                 (14336, 4096), (40, 65536)])
-def test_nvfp4_gemv_every_output(w4, N, K):
+# K % 512 == 0 takes the ring kernel, units of T tiles of 16 rows split over P k-parts:
+# N = 13, 40, 333, 1000 (T = 1, P = 16), 4096 (2, 8), 14336 (6, 4), 12008 (6, 4; the last
+# unit one ragged tile), 28672 (12, 2); x up to 64 k long.
+@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (13, 512), (333, 1024), (1000, 4224),
+                                 (1000, 4608), (4096, 4096), (14336, 4096), (12008, 1536),
+                                 (28672, 1024), (40, 65536)])
+def test_nvfp4_gemv_every_output(w4, fp4_variant, N, K):
     w = special_weights(N, K, seed=N * 5 + K)
     c_np, s_np, S = oracle.nvfp4_quantize(w)
     x = workloads.activations_bf16(1, K, seed=N)[0]
@@ -91,7 +104,7 @@ def test_nvfp4_gemv_every_output(w4, N, K):
                              f"{[(int(n), float(yv[n]), float(y_ref[n])) for n in bad]}")
 
 
-def test_nvfp4_gemv_special_activations(w4):
+def test_nvfp4_gemv_special_activations(w4, fp4_variant):
     """x with a zero chunk, a 2^20 range of magnitudes inside a chunk and a large value."""
     N, K = 96, 1024
     w = special_weights(N, K, seed=9)
@@ -148,9 +161,10 @@ def test_mxfp4_quantize_hand_worked_blocks(w4):
         assert [int(v) for v in c.cpu().numpy()[i]] == [int(v, 16) for v in rec["bytes"]], tag
 
 
-@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (333, 1024), (1000, 4224), (14336, 4096),
+@pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (13, 512), (333, 1024), (1000, 4224),
+                                 (1000, 4608), (14336, 4096), (12008, 1536), (28672, 1024),
                                  (40, 65536)])
-def test_mxfp4_gemv_every_output(w4, N, K):
+def test_mxfp4_gemv_every_output(w4, fp4_variant, N, K):
     w = mx_special_weights(N, K, seed=N * 7 + K)
     c_np, s_np = oracle.mxfp4_quantize(w)
     x = workloads.activations_bf16(1, K, seed=N)[0]
