@@ -46,6 +46,7 @@ __all__ = [
     "w4a16_matmul_prepared", "w4a16_matmul_prepared_workspace_bytes",
     "testing_set_prepared_min_m", "testing_set_prepared_max_m",
     "w4a16_matmul_prepared_uses_prepared", "testing_set_fp4_variant",
+    "fp4_matmul_workspace_bytes", "nvfp4_matmul", "mxfp4_matmul",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -89,6 +90,8 @@ def _load():
         "nvfp4_gemv": [P, P, P, P, P, I, I, P],
         "mxfp4_quantize": [P, I, I, P, P, P],
         "mxfp4_gemv": [P, P, P, P, I, I, P],
+        "nvfp4_matmul": [P, P, P, P, P, I, I, I, P, S, P],
+        "mxfp4_matmul": [P, P, P, P, I, I, I, P, S, P],
         "w4a16_prepare": [P, P, P, I, I, I, P, S, P],
         "w4a16_matmul_prepared": [P, P, P, P, P, P, I, I, I, I, P, S, P],
     }
@@ -101,6 +104,8 @@ def _load():
         getattr(lib, name).restype = S
     lib.w4a16_prepared_bytes.argtypes = [I, I, I]
     lib.w4a16_prepared_bytes.restype = S
+    lib.fp4_matmul_workspace_bytes.argtypes = [I, I]
+    lib.fp4_matmul_workspace_bytes.restype = S
     lib.w4a16_status_string.argtypes = [I]
     lib.w4a16_status_string.restype = ctypes.c_char_p
     for name in ("w4a16_testing_force_kernel", "w4a16_testing_set_gemv_max_m",
@@ -456,6 +461,48 @@ def nvfp4_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
         _dev(scales, "scales", torch.uint8, (N, K // 16)),
         _dev(tensor_scale, "tensor_scale", torch.float32, (1,)),
         _dev(y, "y", torch.bfloat16, (N,)), N, K, _stream(stream)))
+    return y
+
+
+def fp4_matmul_workspace_bytes(M: int, K: int) -> int:
+    """Workspace bytes nvfp4_matmul / mxfp4_matmul need for M rows of x (0 for M = 1)."""
+    return int(_lib.fp4_matmul_workspace_bytes(M, K))
+
+
+def _fp4_matmul_args(name, x, codes, y, workspace):
+    N, K = codes.shape[0], codes.shape[1] * 2
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None and M > 1:
+        workspace = torch.empty(max(fp4_matmul_workspace_bytes(M, K), 16), dtype=torch.uint8,
+                                device=x.device)
+    ws, ws_bytes = _workspace(workspace)
+    return M, N, K, y, ws, ws_bytes
+
+
+def nvfp4_matmul(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                 tensor_scale: torch.Tensor, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] (bf16) = x . W_hat^T, x bf16 [M, K]; a workspace of
+    fp4_matmul_workspace_bytes(M, K) bytes is allocated when none is given."""
+    M, N, K, y, ws, ws_bytes = _fp4_matmul_args("nvfp4_matmul", x, codes, y, workspace)
+    _check("nvfp4_matmul", _lib.nvfp4_matmul(
+        _dev(x, "x", torch.bfloat16, (M, K)), _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.uint8, (N, K // 16)),
+        _dev(tensor_scale, "tensor_scale", torch.float32, (1,)),
+        _dev(y, "y", torch.bfloat16, (M, N)), M, N, K, ws, ws_bytes, _stream(stream)))
+    return y
+
+
+def mxfp4_matmul(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y=None,
+                 workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] (bf16) = x . W_hat^T, x bf16 [M, K]; a workspace of
+    fp4_matmul_workspace_bytes(M, K) bytes is allocated when none is given."""
+    M, N, K, y, ws, ws_bytes = _fp4_matmul_args("mxfp4_matmul", x, codes, y, workspace)
+    _check("mxfp4_matmul", _lib.mxfp4_matmul(
+        _dev(x, "x", torch.bfloat16, (M, K)), _dev(codes, "codes", torch.uint8, (N, K // 2)),
+        _dev(scales, "scales", torch.uint8, (N, K // 32)), _dev(y, "y", torch.bfloat16, (M, N)),
+        M, N, K, ws, ws_bytes, _stream(stream)))
     return y
 
 

@@ -438,6 +438,48 @@ w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* 
   return from_cuda(w4k::launch_mxfp4_gemv(x, codes, scales, y, N, K, s));
 }
 
+size_t fp4_matmul_workspace_bytes(int M, int K) {
+  if (M <= 1 || K <= 0 || K % 512 != 0) return 0;
+  return w4k::fp4_matmul_workspace_bytes(M, K);
+}
+
+static w4a16_status fp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                               const float* tensor_scale, uint16_t* y, int M, int N, int K,
+                               bool mx, void* workspace, size_t workspace_bytes,
+                               w4a16_stream_t stream) {
+  if (M == 1)
+    return mx ? mxfp4_gemv(x, codes, scales, y, N, K, stream)
+              : nvfp4_gemv(x, codes, scales, tensor_scale, y, N, K, stream);
+  if (!x || !codes || !scales || !y || (!mx && !tensor_scale)) return W4A16_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 512 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y) ||
+      (!mx && !aligned16(tensor_scale)))
+    return W4A16_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < w4k::fp4_matmul_workspace_bytes(M, K))
+    return W4A16_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return W4A16_ERR_MISALIGNED;
+  if (!w4k::fp4_matmul_supports(N, K, mx)) return W4A16_ERR_UNSUPPORTED;
+  uint32_t* status = status_word_ptr();
+  if (status == nullptr) return W4A16_ERR_CUDA;
+  return from_cuda(w4k::launch_fp4_matmul(x, codes, scales, tensor_scale, y, M, N, K, mx,
+                                          workspace, status, g_wait_limit_ns,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status nvfp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                          const float* tensor_scale, uint16_t* y, int M, int N, int K,
+                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  return fp4_matmul(x, codes, scales, tensor_scale, y, M, N, K, false, workspace,
+                    workspace_bytes, stream);
+}
+
+w4a16_status mxfp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                          uint16_t* y, int M, int N, int K, void* workspace,
+                          size_t workspace_bytes, w4a16_stream_t stream) {
+  return fp4_matmul(x, codes, scales, nullptr, y, M, N, K, true, workspace, workspace_bytes,
+                    stream);
+}
+
 w4a16_status q4b32_quantize(const float* w, int N, int K, uint8_t* codes, uint16_t* scales,
                             w4a16_stream_t stream) {
   if (!w || !codes || !scales) return W4A16_ERR_INVALID_ARG;

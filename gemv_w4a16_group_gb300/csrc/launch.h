@@ -191,6 +191,16 @@ cudaError_t launch_fp4_gemv_tc(const uint16_t* x, const uint8_t* codes, const ui
                                const float* tensor_scale, uint16_t* y, int N, int K, bool mx,
                                uint32_t* status, uint64_t wait_limit_ns, cudaStream_t stream);
 
+// NVFP4 / MXFP4 matmul for M > 1: x prepared into the workspace (fp4_matmul_workspace_bytes),
+// then one tensor-pipe pass per 32 rows of x. Needs K % 512 == 0; fp4_matmul_supports() tells
+// whether every pass size fits in shared memory.
+size_t fp4_matmul_workspace_bytes(int M, int K);
+bool fp4_matmul_supports(int N, int K, bool mx);
+cudaError_t launch_fp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                              const float* tensor_scale, uint16_t* y, int M, int N, int K,
+                              bool mx, void* workspace, uint32_t* status, uint64_t wait_limit_ns,
+                              cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

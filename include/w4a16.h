@@ -319,9 +319,12 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
 /*
  * nvfp4_gemv -- y[n] = S * sum_b e4m3(s[n, b]) * sum_j e2m1(q[n, 16 b + j]) x[16 b + j]:
  *   x bf16 [K]; codes, scales, tensor_scale as above (device memory); y bf16 [N] (fp32
- *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. x is held
- *   in shared memory: K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0,
- *   K > 0, K % 128 == 0.
+ *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. For
+ *   K % 512 == 0 the tensor-pipe kernel runs: x is held in shared memory in FP16 under one
+ *   power of two (its largest magnitude in [2^14, 2^15)), so elements more than 29 binades
+ *   below the largest lose bits (their terms lie far below the tolerance); K up to about
+ *   100,000. Other K take a kernel with x in FP16 per 128-k chunk: K up to about 110,000
+ *   (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0, K % 128 == 0.
  */
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, uint16_t* y, int N, int K,
@@ -344,13 +347,38 @@ w4a16_status mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
 /*
  * mxfp4_gemv -- y[n] = sum_b 2^(s[n, b] - 127) * sum_j e2m1(q[n, 32 b + j]) x[32 b + j]:
  *   x bf16 [K]; codes, scales as above; y bf16 [N] (fp32 accumulation, rounded to nearest
- *   even). Within a 128-k chunk of a row, a block more than 2^24 below the chunk's largest
- *   block scale adds nothing (its terms are below the tolerance). The tolerance of
- *   w4a16_matmul applies. K up to 83,840 as for nvfp4_gemv. Requires N > 0, K > 0,
- *   K % 128 == 0.
+ *   even). The tolerance of w4a16_matmul applies. For K % 512 == 0 the tensor-pipe kernel
+ *   runs (x in FP16 under a power of two per 32-k block, each block's sum times its scale in
+ *   fp32); other K take a kernel in which, within a 128-k chunk of a row, a block more than
+ *   2^24 below the chunk's largest block scale adds nothing (its terms are below the
+ *   tolerance). K limits as for nvfp4_gemv. Requires N > 0, K > 0, K % 128 == 0.
  */
 w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         uint16_t* y, int N, int K, w4a16_stream_t stream);
+
+/*
+ * nvfp4_matmul / mxfp4_matmul -- Y[m, n] = sum_k x[m, k] w_hat[n, k] for a batch of M rows
+ *   (the formats above; "Low-Precision Kernels ...", Step 6, and "Step 3: measured from 1
+ *   row to 4,096" for the batch). x bf16 [M, K] row-major; codes, scales (and tensor_scale
+ *   for NVFP4) as for the GEMVs; y bf16 [M, N] row-major. M = 1 runs the GEMV and needs no
+ *   workspace. For M > 1, a first kernel writes each row of x into `workspace` in FP16
+ *   under the row's power of two (largest magnitude in [2^14, 2^15)) in the order the MMAs
+ *   read it, and a second kernel streams the weights once per 32 rows of x, decoding each
+ *   weight fragment once for those rows (for M > 32 the weights stream again for every
+ *   further 32 rows). The tolerance of w4a16_matmul applies per output. Workspace: at least
+ *   fp4_matmul_workspace_bytes(M, K) bytes of device memory, 16-byte aligned, owned by the
+ *   caller and not touched by other work while the call runs on `stream`; too small or
+ *   NULL for M > 1 gives W4A16_ERR_WORKSPACE, launching nothing. Requires M > 0, N > 0,
+ *   K > 0, K % 512 == 0 for M > 1 (K % 128 == 0 for M = 1); W4A16_ERR_UNSUPPORTED when the
+ *   shape's ring does not fit in shared memory (K beyond about 100,000 at the widest tiles).
+ */
+size_t fp4_matmul_workspace_bytes(int M, int K);
+w4a16_status nvfp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                          const float* tensor_scale, uint16_t* y, int M, int N, int K,
+                          void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
+w4a16_status mxfp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
+                          uint16_t* y, int M, int N, int K, void* workspace,
+                          size_t workspace_bytes, w4a16_stream_t stream);
 
 /*
  * w4a16_device_status -- synchronizes `stream`, then reads and clears the current

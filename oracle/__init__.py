@@ -20,6 +20,8 @@ Array conventions (all numpy, C-contiguous):
   * NVFP4A16: ``codes`` uint8 [N, K/2] (E2M1, low nibble = even k); ``scales`` uint8
     E4M3 [N, K/16]; ``S`` one fp32; ``x`` bf16 bits [K]; w_hat = e2m1 e4m3 S.
   * MXFP4A16: ``codes`` as NVFP4; ``scales`` uint8 E8M0 [N, K/32]; w_hat = e2m1 2^(s - 127).
+  * The NVFP4A16 / MXFP4A16 matmuls take ``x`` bf16 bits [M, K] and return [M, N] (or
+    [M, len(rows)]): Y[m] = W_hat . x[m], the GEMV of each row.
 """
 from __future__ import annotations
 
@@ -435,6 +437,15 @@ def nvfp4_gemv(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, S: flo
     return y, a
 
 
+def nvfp4_matmul(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, S: float,
+                 rows=None):
+    """y_ref, abs_ref (fp64 [M, N] or [M, len(rows)]) for Y[m] = W_hat . x[m]: the GEMV of
+    each row of x (the matmul's definition, a row at a time)."""
+    x_bits = _c(x_bits, np.uint16)
+    outs = [nvfp4_gemv(x_bits[m], codes, scales, S, rows=rows) for m in range(x_bits.shape[0])]
+    return np.stack([o[0] for o in outs]), np.stack([o[1] for o in outs])
+
+
 def e8m0_value(code: int) -> float:
     return float(_load().oracle_e8m0_value(int(code)))
 
@@ -481,6 +492,14 @@ def mxfp4_gemv(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, rows=N
 # --------------------------------------------------------------------------- #
 # Q4 block-32
 # --------------------------------------------------------------------------- #
+
+def mxfp4_matmul(x_bits: np.ndarray, codes: np.ndarray, scales: np.ndarray, rows=None):
+    """y_ref, abs_ref (fp64 [M, N] or [M, len(rows)]) for Y[m] = W_hat . x[m]: the GEMV of
+    each row of x."""
+    x_bits = _c(x_bits, np.uint16)
+    outs = [mxfp4_gemv(x_bits[m], codes, scales, rows=rows) for m in range(x_bits.shape[0])]
+    return np.stack([o[0] for o in outs]), np.stack([o[1] for o in outs])
+
 
 def q4b32_quantize(w: np.ndarray):
     """fp32 [N, K] -> (codes u8 [N, K/2], scales fp16-bits [N, K/32])."""

@@ -883,4 +883,44 @@ def pin_mxfp4_gemv_exact_and_error():
     assert e_nv < e_mx and 0.08 < e_mx < 0.16, (e_nv, e_mx)
 
 
+def pin_fp4_matmul_exact_and_library():
+    """The NVFP4A16 / MXFP4A16 matmuls: every output of small batches equals the exact
+    rational sum over the rebuilt weights (rows of x of different magnitudes, so a
+    transposed or shared row fails); a larger batch equals torch.matmul (fp64) of x and the
+    dequantized weights; the row subset matches."""
+    rng = np.random.default_rng(61)
+    M, N, K = 3, 4, 64
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x = workloads.bits16(workloads.activations_bf16(M, K, seed=61)
+                         * torch.tensor([[1.0], [-8.0], [0.25]]).to(torch.bfloat16))
+    c4, s4, S4 = oracle.nvfp4_quantize(w)
+    cm, sm = oracle.mxfp4_quantize(w)
+    y4, a4 = oracle.nvfp4_matmul(x, c4, s4, S4)
+    ym, am = oracle.mxfp4_matmul(x, cm, sm)
+    assert y4.shape == (M, N) and ym.shape == (M, N)
+    q4, qm = _nv_codes(c4), _nv_codes(cm)
+    for m in range(M):
+        for n in range(N):
+            e4 = sum(Fraction(_bf16(x[m, k])) * Fraction(oracle.e2m1_value(int(q4[n, k]))) *
+                     Fraction(oracle.e4m3_value(int(s4[n, k // 16]))) * Fraction(S4)
+                     for k in range(K))
+            em = sum(Fraction(_bf16(x[m, k])) * Fraction(oracle.e2m1_value(int(qm[n, k]))) *
+                     Fraction(2) ** (int(sm[n, k // 32]) - 127) for k in range(K))
+            assert abs(Fraction(y4[m, n]) - e4) <= Fraction(a4[m, n]) / 2**45, (m, n)
+            assert abs(Fraction(ym[m, n]) - em) <= Fraction(am[m, n]) / 2**45, (m, n)
+    M, N, K = 5, 40, 512
+    w = workloads.weights(N, K, seed=62, outlier_frac=0.001).numpy()
+    c4, s4, S4 = oracle.nvfp4_quantize(w)
+    cm, sm = oracle.mxfp4_quantize(w)
+    x = workloads.bits16(workloads.activations_bf16(M, K, seed=62))
+    xv = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double()
+    for (y, a), w_hat in ((oracle.nvfp4_matmul(x, c4, s4, S4), oracle.nvfp4_dequant(c4, s4, S4)),
+                          (oracle.mxfp4_matmul(x, cm, sm), oracle.mxfp4_dequant(cm, sm))):
+        ref = (xv @ torch.from_numpy(w_hat).T).numpy()
+        assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    rows = np.array([N - 1, 7], dtype=np.int32)
+    y, _ = oracle.mxfp4_matmul(x, cm, sm)
+    y2, _ = oracle.mxfp4_matmul(x, cm, sm, rows=rows)
+    np.testing.assert_array_equal(y2, y[:, rows])
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

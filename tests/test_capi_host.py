@@ -53,6 +53,10 @@ def lib(cuda_lib):
     lib.w4a16_prepared_bytes.restype = S
     lib.w4a16_matmul_prepared_workspace_bytes.argtypes = [I, I, I, I]
     lib.w4a16_matmul_prepared_workspace_bytes.restype = S
+    lib.nvfp4_matmul.argtypes = [P, P, P, P, P, I, I, I, P, S, P]
+    lib.mxfp4_matmul.argtypes = [P, P, P, P, I, I, I, P, S, P]
+    lib.fp4_matmul_workspace_bytes.argtypes = [I, I]
+    lib.fp4_matmul_workspace_bytes.restype = S
     return lib
 
 
@@ -177,6 +181,28 @@ def test_mxfp4_rejects_bad_arguments_on_host(lib):
     assert g(A, A, A, B, 4, 96, None) == INVALID          # K % 128
     assert g(A, A, A, B, 4, 128 * 2048, None) == UNSUPPORTED
     assert g(A + 2, A, A, B, 4, 256, None) == MISALIGNED
+
+
+def test_fp4_matmul_rejects_bad_arguments_on_host(lib):
+    """The M > 1 NVFP4 / MXFP4 matmuls: the workspace query (x rows padded to the passes' 8,
+    16 or 32, FP16, plus a float per row) and the host-side rejections, before any launch."""
+    wb = lib.fp4_matmul_workspace_bytes
+    assert wb(1, 512) == 0 and wb(2, 500) == 0
+    assert wb(2, 512) == 8 * 512 * 2 + 8 * 4
+    assert wb(16, 512) == 16 * 512 * 2 + 16 * 4
+    assert wb(40, 512) == 64 * 512 * 2 + 64 * 4
+    nv, mx = lib.nvfp4_matmul, lib.mxfp4_matmul
+    need = wb(4, 512)
+    assert nv(A, A, A, A, B, 4, 8, 512, None, 0, None) == WORKSPACE
+    assert nv(A, A, A, A, B, 4, 8, 512, A, need - 16, None) == WORKSPACE
+    assert nv(A, A, A, A, B, 4, 8, 512, A + 8, need, None) == MISALIGNED
+    assert nv(A, A, A, None, B, 4, 8, 512, A, need, None) == INVALID     # no tensor scale
+    assert nv(A, A, A, A, B, 4, 8, 256, A, need, None) == INVALID        # K % 512
+    assert nv(A, A, A, A, B, 0, 8, 512, A, need, None) == INVALID
+    assert nv(A + 2, A, A, A, B, 4, 8, 512, A, need, None) == MISALIGNED
+    assert mx(A, A, A, B, 4, 8, 512, None, 0, None) == WORKSPACE
+    assert mx(A, A, None, B, 4, 8, 512, A, need, None) == INVALID
+    assert mx(A, A, A, B + 4, 4, 8, 512, A, need, None) == MISALIGNED
 
 
 def test_prepared_entry_points_reject_bad_arguments_on_host(lib):

@@ -180,3 +180,106 @@ def test_mxfp4_gemv_every_output(w4, fp4_variant, N, K):
         bad = np.flatnonzero(~ok)[:5]
         raise AssertionError(f"{int((~ok).sum())}/{ok.size} out of tolerance: "
                              f"{[(int(n), float(yv[n]), float(y_ref[n])) for n in bad]}")
+
+
+# --------------------------------------------------------------------------- #
+# M > 1: nvfp4_matmul / mxfp4_matmul (x prepared once, one pass per 32 rows)
+# --------------------------------------------------------------------------- #
+
+def _fp4_case(fmt, N, K, seed):
+    if fmt == "nv":
+        w = special_weights(N, K, seed=seed)
+        c, s, S = oracle.nvfp4_quantize(w)
+        return c, s, S
+    w = mx_special_weights(N, K, seed=seed)
+    c, s = oracle.mxfp4_quantize(w)
+    return c, s, None
+
+
+def _fp4_run(w4, fmt, x, c, s, S, y=None, workspace=None):
+    cd, sd = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    if fmt == "nv":
+        St = torch.tensor([S], dtype=torch.float32, device="cuda")
+        return w4.nvfp4_matmul(x, cd, sd, St, y=y, workspace=workspace)
+    return w4.mxfp4_matmul(x, cd, sd, y=y, workspace=workspace)
+
+
+def _fp4_ref(fmt, x, c, s, S, rows=None):
+    xb = bits(x).reshape(x.shape[0], -1)
+    if fmt == "nv":
+        return oracle.nvfp4_matmul(xb, c, s, S, rows=rows)
+    return oracle.mxfp4_matmul(xb, c, s, rows=rows)
+
+
+def _fp4_check(y, y_ref, a_ref, cols=None):
+    yv = y.float().cpu().numpy()
+    if cols is not None:
+        yv = yv[:, cols]
+    ok = oracle.within_tolerance(yv, y_ref, a_ref)
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{int((~ok).sum())}/{ok.size} out of tolerance: "
+                             f"{[(int(i), int(j), float(yv[i, j]), float(y_ref[i, j])) for i, j in bad]}")
+
+
+# Passes of 8, 16 and 32 rows (M = 2 .. 8, 9 .. 16, 17 .. 32) and several passes (33, 70);
+# units of (2, 8), (6, 4) and (12, 2) tiles x k-parts; ragged N and the last unit.
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+@pytest.mark.parametrize("M,N,K", [(2, 16, 512), (3, 40, 1024), (8, 333, 512), (9, 1000, 1536),
+                                   (16, 256, 512), (17, 136, 1024), (32, 5000, 1024),
+                                   (33, 520, 512), (70, 264, 2048), (5, 28680, 512)])
+def test_fp4_matmul_every_output(w4, fmt, M, N, K):
+    c, s, S = _fp4_case(fmt, N, K, seed=M * 31 + N)
+    x = workloads.activations_bf16(M, K, seed=M + K)
+    x[M // 2] *= 64  # rows of different magnitudes: each row keeps its own power of two
+    xd = x.cuda()
+    y1 = _fp4_run(w4, fmt, xd, c, s, S)
+    y2 = _fp4_run(w4, fmt, xd, c, s, S)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    y_ref, a_ref = _fp4_ref(fmt, x, c, s, S)
+    _fp4_check(y1, y_ref, a_ref)
+    assert w4.w4a16_device_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+@pytest.mark.parametrize("M", [2, 8, 16, 32, 64])
+def test_fp4_matmul_full_size(w4, fmt, M):
+    """The 14336 x 4096 up-projection at batch sizes up to 64: every batch row of one weight
+    row in each 16-row tile (and both tile halves), with the library's own workspace."""
+    N, K = 14336, 4096
+    c, s, S = _fp4_case(fmt, N, K, seed=7)
+    x = workloads.activations_bf16(M, K, seed=M)
+    ws = torch.zeros(w4.fp4_matmul_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    y = _fp4_run(w4, fmt, x.cuda(), c, s, S, workspace=ws)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M)
+    cols = (np.arange(0, N, 16) + rng.integers(0, 16, size=N // 16)).astype(np.int32)
+    y_ref, a_ref = _fp4_ref(fmt, x, c, s, S, rows=cols)
+    _fp4_check(y, y_ref, a_ref, cols)
+    assert w4.w4a16_device_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+def test_fp4_matmul_m1_is_the_gemv_and_guard_bands(w4, fmt):
+    """M = 1 gives the GEMV's bits; for M > 1 exactly y[M, N] is written."""
+    N, K = 200, 1024
+    c, s, S = _fp4_case(fmt, N, K, seed=3)
+    x = workloads.activations_bf16(1, K, seed=3).cuda()
+    y = _fp4_run(w4, fmt, x, c, s, S)
+    cd, sd = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    if fmt == "nv":
+        g = w4.nvfp4_gemv(x[0], cd, sd, torch.tensor([S], dtype=torch.float32, device="cuda"))
+    else:
+        g = w4.mxfp4_gemv(x[0], cd, sd)
+    torch.cuda.synchronize()
+    assert torch.equal(y[0].view(torch.int16), g.view(torch.int16))
+    M, pad = 11, 4096
+    buf = torch.full((pad + M * N + pad,), 12345, dtype=torch.int16, device="cuda")
+    yv = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+    x = workloads.activations_bf16(M, K, seed=4)
+    _fp4_run(w4, fmt, x.cuda(), c, s, S, y=yv)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345)
+    y_ref, a_ref = _fp4_ref(fmt, x, c, s, S)
+    _fp4_check(yv, y_ref, a_ref)

@@ -140,3 +140,27 @@ def test_planted_mistake_is_caught(mid, old, new, occ, tmp_path):
                 caught.append(pin.__name__)
                 break
     assert caught, f"mutant {mid} passed every pin"
+
+
+def _matmul_first_row_only(x_bits, *args, **kw):
+    import numpy as np
+    x = np.asarray(x_bits)
+    return _REAL_NV(np.repeat(x[:1], x.shape[0], axis=0), *args, **kw)
+
+
+def _matmul_rows_reversed(x_bits, *args, **kw):
+    import numpy as np
+    y, a = _REAL_NV(x_bits, *args, **kw)
+    return np.ascontiguousarray(y[::-1]), np.ascontiguousarray(a[::-1])
+
+
+_REAL_NV = oracle.nvfp4_matmul
+
+
+@pytest.mark.parametrize("mistake", [_matmul_first_row_only, _matmul_rows_reversed],
+                         ids=["fp4_matmul_first_row_only", "fp4_matmul_rows_reversed"])
+def test_planted_fp4_matmul_mistake_is_caught(mistake, monkeypatch):
+    """The row loop of the FP4 matmul oracle, with a mistake planted in it, fails its pin."""
+    monkeypatch.setattr(oracle, "nvfp4_matmul", mistake)
+    with pytest.raises(AssertionError):
+        pins.pin_fp4_matmul_exact_and_library()
