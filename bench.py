@@ -541,6 +541,16 @@ def rows_ours(peaks, device, stream):
     b = N * K // 2 + N * K // 16
     nv["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
                   "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
+    for Mb in (8, 32):  # the M > 1 matmul (x prepared once, one pass per 32 rows)
+        xb = workloads.activations_bf16(Mb, K, seed=Mb).to(device)
+        yb = torch.empty(Mb, N, dtype=torch.bfloat16, device=device)
+        wsb = torch.empty(w4.fp4_matmul_workspace_bytes(Mb, K), dtype=torch.uint8, device=device)
+        us = graph_time_us(lambda i: w4.nvfp4_matmul(xb, *cps4[i % ROTATE], y=yb, workspace=wsb),
+                           2 * ROTATE, 10, stream)
+        bb = b + 2 * Mb * K + 2 * Mb * N
+        nv[f"matmul_m{Mb}"] = {"us": round(us, 2), "GBps": round(bb / us / 1e3, 1),
+                               "frac_hbm": round(bb / us / 1e3 / hbm, 3)}
+        del xb, yb, wsb
     rows["nvfp4a16"] = nv
     del cps4, c4, s4, S4
 
@@ -557,6 +567,16 @@ def rows_ours(peaks, device, stream):
     b = N * K // 2 + N * K // 32
     mx["gemv"] = {"us": round(us, 2), "GBps": round(b / us / 1e3, 1),
                   "frac_hbm": round(b / us / 1e3 / hbm, 3), "roofline_us": round(b / hbm / 1e3, 2)}
+    for Mb in (8, 32):
+        xb = workloads.activations_bf16(Mb, K, seed=Mb).to(device)
+        yb = torch.empty(Mb, N, dtype=torch.bfloat16, device=device)
+        wsb = torch.empty(w4.fp4_matmul_workspace_bytes(Mb, K), dtype=torch.uint8, device=device)
+        us = graph_time_us(lambda i: w4.mxfp4_matmul(xb, *cpsm[i % ROTATE], y=yb, workspace=wsb),
+                           2 * ROTATE, 10, stream)
+        bb = b + 2 * Mb * K + 2 * Mb * N
+        mx[f"matmul_m{Mb}"] = {"us": round(us, 2), "GBps": round(bb / us / 1e3, 1),
+                               "frac_hbm": round(bb / us / 1e3 / hbm, 3)}
+        del xb, yb, wsb
     rows["mxfp4a16"] = mx
     del cpsm, cm, sm_, x8, y8
 
@@ -814,7 +834,7 @@ def profile_case(args):
             del w, codes
             M = {"gemv_m1": 1, "gemv_m8": 8, "skinny_m16": 16, "skinny_m32": 32, "tc_m16": 16,
                  "tc_m64": 64, "tc_m128": 128, "tc_m4096": 4096}[case]
-            if case == "tc_m16":  # the tensor-core kernel, not the skinny one the size picks
+            if case.startswith("tc_"):  # the tensor-core kernel whatever the size picks
                 w4.testing_force_kernel(2)
             cps = [(qw.clone(), s.clone(), m.clone()) for _ in range(6)]
             x = workloads.activations_bf16(M, K, seed=M).to(device)

@@ -137,7 +137,8 @@ def run_and_check(w4, M, N, K, seed, cols=None, workspace=True):
 
 @pytest.mark.parametrize("kernel", [GEMV, SKINNY, TCGEN05])
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (3, 136, 1536), (8, 1000, 1280),
-                                   (13, 4872, 640), (32, 4872, 1024), (37, 264, 384)])
+                                   (13, 4872, 640), (32, 4872, 1024), (37, 264, 384),
+                                   (200, 1000, 512)])
 def test_zp_matmul_every_output(w4, restore, kernel, M, N, K):
     if kernel == SKINNY and M > 32:
         pytest.skip("the skinny kernel takes M <= 32")
