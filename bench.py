@@ -761,7 +761,8 @@ def run_reference(args, world, rank):
 
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
                  "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
-                 "nvfp4_gemv", "mxfp4_gemv", "prep_m64", "prep_m128", "tc_m128", "prepare")
+                 "nvfp4_gemv", "nvfp4_gemv_plain", "mxfp4_gemv", "prep_m64", "prep_m128",
+                 "tc_m128", "prepare")
 
 
 def profile_case(args):
@@ -775,11 +776,13 @@ def profile_case(args):
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     case, n = args.case, args.launches
-    if case in ("w8a16_gemv", "zp_m1", "nvfp4_gemv", "mxfp4_gemv"):
+    if case in ("w8a16_gemv", "zp_m1", "nvfp4_gemv", "nvfp4_gemv_plain", "mxfp4_gemv"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w = workloads.weights(N, K, seed=0).to(device)
         x = workloads.activations_bf16(1, K, seed=1).to(device)
-        if case == "nvfp4_gemv":
+        if case == "nvfp4_gemv_plain":  # the plain-load kernel, not the ring the shape picks
+            w4.testing_set_fp4_variant(0)
+        if case in ("nvfp4_gemv", "nvfp4_gemv_plain"):
             c4, s4, S4 = w4.nvfp4_quantize(w)
             del w
             cps = [(c4.clone(), s4.clone(), S4.clone()) for _ in range(6)]
