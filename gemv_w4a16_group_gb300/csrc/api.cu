@@ -41,7 +41,7 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 int g_force_kernel = 0;
 // M at or below which the GEMV kernel (mma.sync inner products) runs when the choice is by M.
 int g_gemv_max_m = 8;
-int g_skinny_min_m = 9;
+int g_skinny_min_m = 5;  // M = 5..8 measured faster on the skinny kernel than on the GEMV
 int g_skinny_max_m = 32;
 // Range of M for which w4a16_matmul_prepared runs the prepared-layout tensor-core kernel
 // (measured on the 14336 x 4096 layer: 1.6-1.7x the canonical path at M = 48..128, even at

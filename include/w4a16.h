@@ -96,13 +96,13 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw,
  *   qw     int32 [K/8, N]  (as written by w4a16_pack)
  *   scales bf16 [K/group, N], mins bf16 [K/group, N]
  *   y      bf16 [M, N]     (fp32 accumulation, rounded to nearest even)
- * Kernel choice is by M: a GEMV for M <= 8, for 9 <= M <= 32 a skinny kernel (FP16
- * mma.sync with the batch in n8 tiles) when the caller's workspace holds its converted
- * activations, a TMA + tcgen05 tensor-core kernel otherwise. Accuracy: |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k|
- * per output, y_ref the exact product on the same 4-bit weights. Results are
+ * Kernel choice is by M: for 5 <= M <= 32 a skinny kernel (FP16 mma.sync with the batch in
+ * n8 tiles) when the caller's workspace holds its converted activations; otherwise a GEMV for
+ * M <= 8 and a TMA + tcgen05 tensor-core kernel above. Accuracy:
+ * |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k| per output, y_ref the exact product on the same 4-bit weights. Results are
  * deterministic (no floating-point atomics).
  *   workspace / workspace_bytes: optional caller-owned device scratch that lets small-N
- *   shapes split K across thread blocks and lets 9 <= M <= 32 use the skinny kernel; size
+ *   shapes split K across thread blocks and lets 5 <= M <= 32 use the skinny kernel; size
  *   it with w4a16_matmul_workspace_bytes(). NULL (with 0 bytes) is always accepted. The
  *   workspace must be zero-filled before its first use and not shared by calls that may
  *   run concurrently. The split-K counters live in its first workspace_bytes / 128 + 256
@@ -130,7 +130,7 @@ w4a16_status w4a16_matmul_host(const uint16_t* x_host, const int32_t* qw, const 
                                size_t workspace_bytes, w4a16_stream_t stream);
 
 /* Bytes of workspace that let w4a16_matmul split K for this shape, or run the skinny
- * kernel for 9 <= M <= 32 (0 = no benefit). */
+ * kernel for 5 <= M <= 32 (0 = no benefit). */
 size_t w4a16_matmul_workspace_bytes(int M, int N, int K, int group);
 
 /*

@@ -26,7 +26,7 @@ int w4a16_testing_force_kernel(int kernel);
 int w4a16_testing_set_gemv_max_m(int m);
 
 /* Range of M that the by-M choice sends to the skinny kernel when the shape fits it and the
- * workspace is large enough (default 9..32; hi at most 32). Negative values only query.
+ * workspace is large enough (default 5..32; hi at most 32). Negative values only query.
  * Returns the previous range as (lo << 8) | hi. */
 int w4a16_testing_set_skinny_range(int lo, int hi);
 

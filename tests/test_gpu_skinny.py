@@ -85,10 +85,10 @@ def test_skinny_matches_oracle(w4, skinny_everywhere, M, N, K):
     assert w4.w4a16_device_status() == 0
 
 
-@pytest.mark.parametrize("M", [9, 16, 32])
+@pytest.mark.parametrize("M", [5, 8, 9, 16, 32])
 def test_skinny_by_m_every_output(w4, M):
-    """Default range: 9 <= M <= 32 on the Llama up-projection picks the skinny kernel when
-    the workspace holds its plan; every output checked."""
+    """Default range: 5 <= M <= 32 on the Llama up-projection picks the skinny kernel when
+    the workspace holds its plan (two n8 tiles up to M = 16); every output checked."""
     N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
     need = w4.w4a16_matmul_workspace_bytes(M, N, K)
     assert need >= (K // 8) * 8 * ((M + 7) // 8) * 16  # at least the converted activations
