@@ -762,7 +762,7 @@ def run_reference(args, world, rank):
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
                  "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
                  "nvfp4_gemv", "nvfp4_gemv_plain", "mxfp4_gemv", "prep_m64", "prep_m128",
-                 "tc_m128", "prepare")
+                 "tc_m128", "prepare", "qwen_layer")
 
 
 def profile_case(args):
@@ -806,6 +806,22 @@ def profile_case(args):
             cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(6)]
             for i in range(n):
                 w4.w4a16zp_matmul(x, *cps[i % 6])
+    elif case == "qwen_layer":
+        # one Qwen2.5-1.5B-shaped layer (7 matmuls, each with its own weights and x, the
+        # workspace the library asks for), the layer repeated n times
+        layer = []
+        for name, Nl, Kl in workloads.QWEN_STACK["block"]:
+            g = torch.Generator(device=device)
+            g.manual_seed(len(layer))
+            wl = torch.randn(Nl, Kl, generator=g, device=device) * workloads.WEIGHT_STD
+            cl, sl, ml = w4.w4a16_quantize(wl)
+            ql = w4.w4a16_pack(cl)
+            xl = torch.randn(1, Kl, generator=g, device=device).to(torch.bfloat16)
+            yl = torch.empty(1, Nl, dtype=torch.bfloat16, device=device)
+            layer.append((xl, ql, sl, ml, yl, workspace_for(1, Nl, Kl, device)))
+        for _ in range(n):
+            for (xl, ql, sl, ml, yl, wsl) in layer:
+                w4.w4a16_matmul(xl, ql, sl, ml, y=yl, workspace=wsl)
     elif case in ("prep_m64", "prep_m128", "prepare"):
         N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
         w, codes, qw, s, m = quantized_on_device(N, K, 0, device)
