@@ -166,13 +166,22 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
     }
   } else {
     // x (BF16) -> FP16 in natural order under one power of two for the whole vector (largest
-    // |x| in [2^14, 2^15)). Pass 1 finds the largest |x|, pass 2 converts.
+    // |x| in [2^14, 2^15)). Pass 1 finds the largest |x|, pass 2 converts; with one segment
+    // per thread (K <= 8 NC) the segment stays in registers between the passes.
     float amax = 0.f;
-    for (int R = tid; R < segs; R += NC) {
-      float v[8];
-      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+    const bool one = segs <= NC;
+    float v1[8] = {};
+    if (one) {
+      if (tid < segs) f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + tid), v1);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v1[q]));
+    } else {
+      for (int R = tid; R < segs; R += NC) {
+        float v[8];
+        f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+      }
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -183,10 +192,14 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
     for (int w = 1; w < W; ++w) amax = fmaxf(amax, sRed[w]);
     const int e = f_x_exponent(amax);
     const float sc = f_pow2(e);
-    for (int R = tid; R < segs; R += NC) {
-      float v[8];
-      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
-      sX[R] = f_f16x8(v, sc);
+    if (one) {
+      if (tid < segs) sX[tid] = f_f16x8(v1, sc);
+    } else {
+      for (int R = tid; R < segs; R += NC) {
+        float v[8];
+        f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+        sX[R] = f_f16x8(v, sc);
+      }
     }
     if (tid == 0) sCst[0] = f_pow2(-e);
   }
