@@ -46,7 +46,7 @@ __all__ = [
     "w4a16_matmul_prepared", "w4a16_matmul_prepared_workspace_bytes",
     "testing_set_prepared_min_m", "testing_set_prepared_max_m",
     "w4a16_matmul_prepared_uses_prepared", "testing_set_fp4_variant",
-    "fp4_matmul_workspace_bytes", "nvfp4_matmul", "mxfp4_matmul",
+    "fp4_matmul_workspace_bytes", "nvfp4_matmul", "mxfp4_matmul", "testing_set_w8_variant",
 ]
 
 STATUS_NAMES = {0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED",
@@ -110,7 +110,8 @@ def _load():
     lib.w4a16_status_string.restype = ctypes.c_char_p
     for name in ("w4a16_testing_force_kernel", "w4a16_testing_set_gemv_max_m",
                  "w4a16_testing_set_q4_variant", "w4a16_testing_set_prepared_min_m",
-                 "w4a16_testing_set_prepared_max_m", "w4a16_testing_set_fp4_variant"):
+                 "w4a16_testing_set_prepared_max_m", "w4a16_testing_set_fp4_variant",
+                 "w4a16_testing_set_w8_variant"):
         getattr(lib, name).argtypes = [I]
         getattr(lib, name).restype = I
     lib.w4a16_testing_set_skinny_range.argtypes = [I, I]
@@ -587,6 +588,12 @@ def testing_set_skinny_range(lo: int, hi: int):
 
 def testing_set_q4_variant(v: int) -> int:
     return int(_lib.w4a16_testing_set_q4_variant(v))
+
+
+def testing_set_w8_variant(v: int) -> int:
+    """Kernel of w8a16_gemv: 1 = tensor-pipe ring (default), 0 = plain loads; other values
+    only query. Returns the previous value."""
+    return int(_lib.w4a16_testing_set_w8_variant(v))
 
 
 def testing_set_fp4_variant(v: int) -> int:

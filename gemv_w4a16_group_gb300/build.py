@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libw4a16_gb300.so")
 
 SOURCES = ["api.cu", "quant_pack.cu", "gemv.cu", "q4b32.cu", "q4b32_mma.cu", "gemm_tc.cu",
            "no_alloc.cu", "host_cache.cu", "skinny.cu", "w8a16.cu",
-           "nvfp4.cu", "fp4_mma.cu", "fp4_matmul.cu", "prepared.cu"]
+           "nvfp4.cu", "fp4_mma.cu", "fp4_matmul.cu", "prepared.cu", "w8a16_mma.cu"]
 HEADERS = ["common.cuh", "fp4_common.cuh", "launch.h"]
 PUBLIC_HEADERS = ["w4a16.h", "w4a16_testing.h"]
 

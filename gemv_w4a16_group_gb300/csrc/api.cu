@@ -369,15 +369,23 @@ w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scal
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int g_w8_variant = 1;
+
 w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
                         int N, int K, w4a16_stream_t stream) {
   if (!x || !q || !scales || !y) return W4A16_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0 || K % 64 != 0) return W4A16_ERR_INVALID_ARG;
-  if (w4k::w8a16_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || !aligned16(y))
     return W4A16_ERR_MISALIGNED;
-  return from_cuda(
-      w4k::launch_w8a16_gemv(x, q, scales, y, N, K, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g_w8_variant == 1 && w4k::w8a16_tc_supports(N, K)) {
+    uint32_t* status = status_word_ptr();
+    if (status == nullptr) return W4A16_ERR_CUDA;
+    return from_cuda(w4k::launch_w8a16_gemv_tc(x, q, scales, y, N, K, status, g_wait_limit_ns, s));
+  }
+  // K % 512 != 0 or x too long for the ring: the plain-load kernel.
+  if (w4k::w8a16_smem_bytes(K) > 227u * 1024u) return W4A16_ERR_UNSUPPORTED;
+  return from_cuda(w4k::launch_w8a16_gemv(x, q, scales, y, N, K, s));
 }
 
 w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_t* scales,
@@ -573,6 +581,12 @@ int w4a16_testing_set_prepared_max_m(int m) {
 int w4a16_testing_set_q4_variant(int v) {
   const int prev = g_q4_variant;
   if (v >= 0 && v <= 2) g_q4_variant = v;
+  return prev;
+}
+
+int w4a16_testing_set_w8_variant(int v) {
+  const int prev = g_w8_variant;
+  if (v >= 0 && v <= 1) g_w8_variant = v;
   return prev;
 }
 

@@ -201,6 +201,14 @@ cudaError_t launch_fp4_matmul(const uint16_t* x, const uint8_t* codes, const uin
                               bool mx, void* workspace, uint32_t* status, uint64_t wait_limit_ns,
                               cudaStream_t stream);
 
+// W8A16 GEMV on the tensor pipe (TMA-staged, mma.sync FP16 -> fp32): K % 512 == 0 and x and
+// a two-stage ring in shared memory; w8a16_tc_supports() tells. Bounded waits report through
+// `status`.
+bool w8a16_tc_supports(int N, int K);
+cudaError_t launch_w8a16_gemv_tc(const uint16_t* x, const int8_t* q, const float* scales,
+                                 uint16_t* y, int N, int K, uint32_t* status,
+                                 uint64_t wait_limit_ns, cudaStream_t stream);
+
 // Bounded-wait self test: waits on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -291,9 +291,10 @@ w4a16_status w8a16_quantize(const float* w, int N, int K, int8_t* q, float* scal
 /*
  * w8a16_gemv -- y[n] = s[n] * sum_k q[n, k] x[k] (the scale once per row, after the sum).
  *   x bf16 [K]; q int8 [N, K]; scales fp32 [N]; y bf16 [N] (fp32 accumulation, rounded to
- *   nearest even). The tolerance of w4a16_matmul applies. x is held in shared memory:
- *   K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0,
- *   K % 64 == 0.
+ *   nearest even). The tolerance of w4a16_matmul applies. x is held in shared memory in
+ *   FP16: for K % 512 == 0 (the tensor-pipe kernel) under one power of two for the vector,
+ *   K up to about 100,000; for other K under a power of two per 64 k, K up to about
+ *   110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0, K % 64 == 0.
  */
 w4a16_status w8a16_gemv(const uint16_t* x, const int8_t* q, const float* scales, uint16_t* y,
                         int N, int K, w4a16_stream_t stream);

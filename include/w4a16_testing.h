@@ -46,6 +46,11 @@ int w4a16_testing_set_q4_variant(int v);
  * plain-load kernel. Other values only query. Returns the previous value. */
 int w4a16_testing_set_fp4_variant(int v);
 
+/* Kernel of w8a16_gemv: 1 = TMA-staged tensor-pipe kernel (default; shapes it does not take,
+ * K % 512 != 0 or x too long for its ring, fall back to 0), 0 = the plain-load kernel. Other
+ * values only query. Returns the previous value. */
+int w4a16_testing_set_w8_variant(int v);
+
 #ifdef __cplusplus
 }
 #endif

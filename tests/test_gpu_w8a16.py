@@ -24,6 +24,15 @@ def w4():
     return mod
 
 
+@pytest.fixture(params=[1, 0], ids=["ring", "plain"])
+def w8_variant(request, w4):
+    """Run the GEMV test through the tensor-pipe ring kernel (shapes it does not take fall
+    back to the plain-load kernel) and through the plain-load kernel."""
+    prev = w4.testing_set_w8_variant(request.param)
+    yield request.param
+    w4.testing_set_w8_variant(prev)
+
+
 def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -66,9 +75,12 @@ def test_w8_quantize_hand_worked_rows(w4):
         assert q[i, :8].tolist() == [int(v) for v in rec["q"]], tag
 
 
-@pytest.mark.parametrize("N,K", [(16, 64), (17, 128), (333, 1024), (1000, 4160), (4096, 4096),
-                                 (14336, 4096), (64, 65536)])
-def test_w8_gemv_every_output(w4, N, K):
+# K % 512 == 0 takes the ring kernel: units of T tiles of 16 rows split over P k-parts
+# (13, 333: T = 1; 4096: 2; 12008: 6 with a ragged last unit; 28672: 12) and x up to 64 k.
+@pytest.mark.parametrize("N,K", [(16, 64), (17, 128), (13, 512), (333, 1024), (1000, 4160),
+                                 (4096, 4096), (14336, 4096), (12008, 1536), (28672, 1024),
+                                 (64, 65536)])
+def test_w8_gemv_every_output(w4, w8_variant, N, K):
     w = special_rows(N, K, seed=N * 3 + K)
     q_np, s_np = oracle.w8a16_quantize(w)
     x = workloads.activations_bf16(1, K, seed=N)[0]
@@ -87,7 +99,7 @@ def test_w8_gemv_every_output(w4, N, K):
     assert yv[0] == 0.0  # the zero row
 
 
-def test_w8_gemv_special_activations(w4):
+def test_w8_gemv_special_activations(w4, w8_variant):
     """x with zeros, a 2^20 range of magnitudes inside a chunk, and an all-zero chunk."""
     N, K = 96, 1024
     w = special_rows(N, K, seed=5)
