@@ -46,6 +46,8 @@ METRIC = "W4A16 µs & effective HBM GB/s at M=1; TFLOPS vs M=1..4096; % of roofl
 PAGES_M1_GBPS = 169.0  # the pages' M=1 effective bandwidth for this shape (RTX 4060 Laptop)
 ROTATE = 12            # weight copies in rotation (12 x 31.2 MB > 2 x L2)
 GRAPH_LEN = 96         # launches per captured graph in the timed loop
+EVENT_GRAPH_MAX = 2048  # up to this many steps a region is one graph with its events inside
+EVENT_GRAPH_PRE = 8     # untimed launches at the head of such a graph
 ROUNDS = 3             # timed regions per run; the median is reported
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -263,10 +265,38 @@ def run_ours(args, world, rank, local):
         for i in range(max(args.warmup, 3)):
             step(i)
     torch.cuda.synchronize()
-    glen = min(GRAPH_LEN, args.steps)
-    g_main = capture(step, glen, stream)
-    tail = args.steps % glen
-    g_tail = capture(step, tail, stream) if tail else None
+    in_graph = args.steps <= EVENT_GRAPH_MAX
+    if in_graph:
+        # One graph per region: EVENT_GRAPH_PRE untimed launches, then exactly --steps timed
+        # ones. The start and end events are recorded inside the graph on a branch forked
+        # from the launch stream after the last untimed and the last timed launch, so the
+        # chain of dependent launches is not broken and the region runs from the completion
+        # of the last untimed launch to that of the last timed one: --steps launches in the
+        # steady state, with no host latency inside.
+        side = torch.cuda.Stream(device)
+        ev0 = torch.cuda.Event(enable_timing=True, external=True)
+        ev1 = torch.cuda.Event(enable_timing=True, external=True)
+        fork0, fork1, join = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        g_main = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_main, stream=stream):
+            for i in range(EVENT_GRAPH_PRE):
+                step(i)
+            fork0.record(stream)
+            side.wait_event(fork0)
+            ev0.record(side)
+            for i in range(args.steps):
+                step(EVENT_GRAPH_PRE + i)
+            fork1.record(stream)
+            side.wait_event(fork1)
+            ev1.record(side)
+            join.record(side)
+            stream.wait_event(join)
+        g_tail = None
+    else:
+        glen = min(GRAPH_LEN, args.steps)
+        g_main = capture(step, glen, stream)
+        tail = args.steps % glen
+        g_tail = capture(step, tail, stream) if tail else None
     with torch.cuda.stream(stream):
         g_main.replay()
     torch.cuda.synchronize()
@@ -274,14 +304,21 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)
-    # ROUNDS timed regions of exactly --steps launches each; the median is reported. Before
-    # each region an untimed replay is already queued on the stream, so that the region's
-    # start event fires when the GPU reaches it rather than when the host gets there (the
-    # host's graph-launch latency would otherwise land inside a short region).
+    # ROUNDS timed regions of exactly --steps launches each; the median is reported. For long
+    # runs (several graphs per region) an untimed replay is already queued before each
+    # region, so that its start event fires when the GPU reaches it rather than when the host
+    # gets there.
     region_s = []
     for _ in range(ROUNDS):
         barrier(world)
         torch.cuda.synchronize()
+        if in_graph:
+            with torch.cuda.stream(stream):
+                g_main.replay()
+            torch.cuda.synchronize()
+            barrier(world)
+            region_s.append(ev0.elapsed_time(ev1) / 1e3)
+            continue
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):  # replay() launches on the current stream
             g_main.replay()  # untimed: keeps the GPU busy while the timed region is queued
@@ -317,8 +354,11 @@ def run_ours(args, world, rank, local):
             "config": {"workload": cfg["name"], "M": M, "N": N, "K": K, "group": cfg["group"]},
             "timing": {"l2": f"rotating {ROTATE} weight copies ({ROTATE * bytes_w / 1e6:.0f} MB "
                              "> 2x L2), CUDA-graph replay",
-                       "statistic": f"median of {ROUNDS} timed regions of {args.steps} launches, "
-                                    "each started behind an untimed replay",
+                       "statistic": (f"median of {ROUNDS} timed regions of {args.steps} launches, "
+                                     + (f"each one graph of {EVENT_GRAPH_PRE} untimed + "
+                                        f"{args.steps} timed launches with its events recorded "
+                                        "inside on a forked branch" if in_graph else
+                                        "each started behind an untimed replay")),
                        "us_per_step": round(us_per_step, 3),
                        "regions_us_per_step": [round(t / args.steps * 1e6, 3) for t in region_s],
                        "parallelism": f"replicas x{world}"},
