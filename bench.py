@@ -802,7 +802,7 @@ def run_reference(args, world, rank):
 PROFILE_CASES = ("gemv_m1", "gemv_m8", "skinny_m16", "skinny_m32", "tc_m16", "tc_m64",
                  "tc_m4096", "q4b32_gemv", "quantize", "pack", "w8a16_gemv", "zp_m1",
                  "nvfp4_gemv", "nvfp4_gemv_plain", "mxfp4_gemv", "prep_m64", "prep_m128",
-                 "tc_m128", "prepare", "qwen_layer")
+                 "tc_m128", "prepare", "qwen_layer", "nvfp4_mm32")
 
 
 def profile_case(args):
@@ -846,6 +846,18 @@ def profile_case(args):
             cps = [(qk.clone(), sk.clone(), zk.clone()) for _ in range(6)]
             for i in range(n):
                 w4.w4a16zp_matmul(x, *cps[i % 6])
+    elif case == "nvfp4_mm32":
+        # the NVFP4 matmul at M = 32 on the up-projection (one pass of 32 rows)
+        N, K = workloads.LLAMA_UP["N"], workloads.LLAMA_UP["K"]
+        w = workloads.weights(N, K, seed=0).to(device)
+        c4, s4, S4 = w4.nvfp4_quantize(w)
+        del w
+        cps = [(c4.clone(), s4.clone(), S4.clone()) for _ in range(6)]
+        x = workloads.activations_bf16(32, K, seed=32).to(device)
+        y = torch.empty(32, N, dtype=torch.bfloat16, device=device)
+        ws = torch.empty(w4.fp4_matmul_workspace_bytes(32, K), dtype=torch.uint8, device=device)
+        for i in range(n):
+            w4.nvfp4_matmul(x, *cps[i % 6], y=y, workspace=ws)
     elif case == "qwen_layer":
         # one Qwen2.5-1.5B-shaped layer (7 matmuls, each with its own weights and x, the
         # workspace the library asks for), the layer repeated n times

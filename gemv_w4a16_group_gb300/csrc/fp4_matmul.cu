@@ -7,8 +7,9 @@
 //   * fp4_xprep_kernel, one CTA per row of x (rows padded with zeros to whole passes):
 //     the row in FP16 under one power of two (largest |x| in [2^14, 2^15); exact for BF16
 //     values within 29 binades of the row's largest), written in the MMA's B-fragment order
-//     (for 8 rows, a 32-k block and k-quarter c: the 8 rows' 16-byte runs of 8 k side by
-//     side, so one 512-byte run feeds a warp's B fragments), and 2^-e per row;
+//     (for 8 rows and a 32-k block: row-major 16-byte runs of 8 k, unit 4 row + quarter, so
+//     lane 4 gq + c of a warp reads unit lane of one 512-byte run, without bank conflicts),
+//     and 2^-e per row;
 //   * fp4_matmul_tc_kernel: the GEMV kernel's structure (units of T tiles of 16 weight rows
 //     and all of K, a producer warp streaming 512-k chunks by TMA into a ring, warp (t, p)
 //     taking tile t and the 32-k blocks p, p + P, ... of every chunk) with each chunk's slice
@@ -42,8 +43,8 @@ struct MLayout {
     scale_bytes = static_cast<uint32_t>(sb) * 16u * static_cast<uint32_t>(T);
     x_off = (code_bytes + scale_bytes + 1023u) & ~1023u;
     stage_bytes = x_off + static_cast<uint32_t>(MB) * kMXSlice;
-    red_off = static_cast<uint32_t>(stages) * stage_bytes;             // [16 T][8 MB] fp32
-    bar_off = red_off + 16u * static_cast<uint32_t>(T) * 8u * static_cast<uint32_t>(MB) * 4u;
+    red_off = static_cast<uint32_t>(stages) * stage_bytes;             // [8 MB][16 T + 1] fp32
+    bar_off = red_off + (16u * static_cast<uint32_t>(T) + 1u) * 8u * static_cast<uint32_t>(MB) * 4u;
     total = bar_off + 2u * kMMaxStages * 8u + 16u;
   }
 };
@@ -55,7 +56,7 @@ __device__ __forceinline__ void m_consumer_bar() {
 
 // x [M, K] BF16 -> xf (FP16, B-fragment order, Mp rows: M rounded up to a whole number of
 // passes, the rows past M zero) and u[m] = 2^-e_m (0 past M).
-// Unit (16 bytes) ((mc * K/32 + b) * 4 + c) * 8 + gq of xf holds x[8 mc + gq, 32 b + 8 c ..
+// Unit (16 bytes) ((mc * K/32 + b) * 8 + gq) * 4 + c of xf holds x[8 mc + gq, 32 b + 8 c ..
 // 32 b + 8 c + 7] 2^e.
 __global__ void __launch_bounds__(kXprepThreads)
     fp4_xprep_kernel(const uint16_t* __restrict__ x, int M, int K, uint4* __restrict__ xf,
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kXprepThreads)
       f_bf16x8(__ldg(src + s), v);
       out = f_f16x8(v, sc);
     }
-    xf[((base + static_cast<size_t>(s >> 2)) * 4 + static_cast<size_t>(s & 3)) * 8 + gq] = out;
+    xf[((base + static_cast<size_t>(s >> 2)) * 8 + gq) * 4 + static_cast<size_t>(s & 3)] = out;
   }
   if (tid == 0) u[m] = m < M ? f_pow2(-e) : 0.f;
 }
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const MLayout L(T, MB, stages, SB);
-  float* sRed = reinterpret_cast<float*>(smem + L.red_off);  // [ROWS][8 MB]
+  float* sRed = reinterpret_cast<float*>(smem + L.red_off);  // [8 MB][ROWS + 1]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kMMaxStages;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kMMaxStages);
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
     const uint32_t j = static_cast<uint32_t>(p + P * r);
     code_off[r] = (j >> 3) * (L.code_bytes / 2) + rowA * 128u +
                   (((j & 7u) ^ static_cast<uint32_t>(gq)) << 4) + 4u * static_cast<uint32_t>(c);
-    x_off[r] = L.x_off + ((j * 4u + static_cast<uint32_t>(c)) * 8u + static_cast<uint32_t>(gq)) * 16u;
+    x_off[r] = L.x_off + (j * 32u + static_cast<uint32_t>(lane)) * 16u;  // unit 32 j + 4 gq + c
   }
   const uint32_t ssel = static_cast<uint32_t>(c >> 1) * 0x11u;
   const uint32_t ring_base = smem_addr(smem);
@@ -284,18 +285,18 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
 #pragma unroll
           for (int f = 0; f < 4; ++f) v[f] = NCH == 2 ? acc[i][0][f] + acc[i][NCH - 1][f] : acc[i][0][f];
           const int mA = 8 * i + 2 * c;
-          float* ra = sRed + rowA * (8 * MB) + mA;
-          float* rb = sRed + (rowA + 8u) * (8 * MB) + mA;
+          float* ra = sRed + mA * (ROWS + 1) + rowA;  // column m of D, rows rowA, rowA + 8
+          float* rb = ra + 8;
           if (q == 0) {
             ra[0] = v[0];
-            ra[1] = v[1];
+            ra[ROWS + 1] = v[1];
             rb[0] = v[2];
-            rb[1] = v[3];
+            rb[ROWS + 1] = v[3];
           } else {
             ra[0] += v[0];
-            ra[1] += v[1];
+            ra[ROWS + 1] += v[1];
             rb[0] += v[2];
-            rb[1] += v[3];
+            rb[ROWS + 1] += v[3];
           }
         }
       }
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
       const int n = row0 + row, mg = m0 + m;
       if (n < N && mg < M)
         y[static_cast<size_t>(mg) * N + n] = __bfloat16_as_ushort(
-            __float2bfloat16_rn(S * __ldg(u + mg) * sRed[row * (8 * MB) + m]));
+            __float2bfloat16_rn(S * __ldg(u + mg) * sRed[m * (ROWS + 1) + row]));
     }
     m_consumer_bar<NC>();
   }
