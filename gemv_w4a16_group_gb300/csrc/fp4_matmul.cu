@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(kXprepThreads)
 
 struct MMaps {
   CUtensorMap codes;   // uint8 [N, K/2], box {128, 16 T}, 128-byte swizzle
-  CUtensorMap scales;  // uint8 [N, K/16] (NVFP4) or [N, K/32] (MXFP4), box {32 or 16, 16 T}
+  // uint8 [N, K/16] (NVFP4, box {32, 16 T}, 32-byte swizzle) or [N, K/32] (MXFP4, box
+  // {16, 16 T}, no swizzle)
+  CUtensorMap scales;
 };
 
 // One pass over rows m0 .. m0 + 8 MB - 1 of x (those below M are written). xf points at the
@@ -205,13 +207,17 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   const int gq = lane >> 2, c = lane & 3;
   const int t = warp % T, p = warp / T;  // tile in the unit, first 32-k block in a chunk
   const uint32_t rowA = static_cast<uint32_t>(16 * t + gq);  // rowB = rowA + 8
-  uint32_t code_off[NB], x_off[NB];
+  // NVFP4 scale box: 32-byte swizzle (16-byte halves of a row swap where bit 2 of the row is
+  // set), so rows gq and gq + 4 read different banks.
+  uint32_t code_off[NB], x_off[NB], s_off[NB];
+  const uint32_t sswz = MX ? 0u : (static_cast<uint32_t>(gq) & 4u) << 2;
 #pragma unroll
   for (int r = 0; r < NB; ++r) {
     const uint32_t j = static_cast<uint32_t>(p + P * r);
     code_off[r] = (j >> 3) * (L.code_bytes / 2) + rowA * 128u +
                   (((j & 7u) ^ static_cast<uint32_t>(gq)) << 4) + 4u * static_cast<uint32_t>(c);
     x_off[r] = L.x_off + (j * 32u + static_cast<uint32_t>(lane)) * 16u;  // unit 32 j + 4 gq + c
+    s_off[r] = rowA * SB + (MX ? j : ((2u * j) ^ sswz));
   }
   const uint32_t ssel = static_cast<uint32_t>(c >> 1) * 0x11u;
   const uint32_t ring_base = smem_addr(smem);
@@ -229,15 +235,14 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
       if (landed) {
 #pragma unroll
         for (int r = 0; r < NB; ++r) {
-          const uint32_t j = static_cast<uint32_t>(p + P * r);
           const uint32_t w0 = f_lds32(buf + code_off[r]);
           const uint32_t w1 = f_lds32(buf + code_off[r] + 1024u);
           uint32_t p0[4], p1[4];
           f_e2m1_pairs(w0, p0);
           f_e2m1_pairs(w1, p1);
           if constexpr (!MX) {
-            const uint32_t qa = f_lds_u16(sbox + rowA * SB + 2u * j);
-            const uint32_t qb = f_lds_u16(sbox + (rowA + 8u) * SB + 2u * j);
+            const uint32_t qa = f_lds_u16(sbox + s_off[r]);
+            const uint32_t qb = f_lds_u16(sbox + s_off[r] + 8u * SB);
             const uint32_t sA = f_e4m3_pair(__byte_perm(qa, 0u, ssel));
             const uint32_t sB = f_e4m3_pair(__byte_perm(qb, 0u, ssel));
 #pragma unroll
@@ -253,8 +258,8 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
               f_mma(d, p0[2], p1[2], p0[3], p1[3], e.z, e.w);
             }
           } else {
-            const float sA = f_e8m0(f_lds_u8(sbox + rowA * SB + j));
-            const float sB = f_e8m0(f_lds_u8(sbox + (rowA + 8u) * SB + j));
+            const float sA = f_e8m0(f_lds_u8(sbox + s_off[r]));
+            const float sB = f_e8m0(f_lds_u8(sbox + s_off[r] + 8u * SB));
 #pragma unroll
             for (int i = 0; i < MB; ++i) {
               const uint4 e = f_lds128(buf + x_off[r] + static_cast<uint32_t>(i) * kMXSlice);
@@ -428,7 +433,8 @@ cudaError_t launch_fp4_matmul(const uint16_t* x, const uint8_t* codes, const uin
     const uint64_t srow = mx ? static_cast<uint64_t>(K) / 32 : static_cast<uint64_t>(K) / 16;
     e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, srow,
                           static_cast<uint64_t>(N), srow, mx ? 16u : 32u,
-                          static_cast<uint32_t>(16 * T), CU_TENSOR_MAP_SWIZZLE_NONE);
+                          static_cast<uint32_t>(16 * T),
+                          mx ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_32B);
     if (e != cudaSuccess) return e;
     const uint8_t* xp = xf + static_cast<size_t>(m0 / 8) * static_cast<size_t>(K) * 16;
     if (mx) {

@@ -17,13 +17,14 @@
 //     it). Per unit the P partial sums of a row are added in a fixed order; no atomics.
 //   * A byte of two codes becomes an FP16 pair in one cvt.rn.f16x2.e2m1x2 (natural k order,
 //     so x waits in shared memory in natural order, 8 k per 16 bytes).
-//   * NVFP4: the E4M3 scale of the 16-k block a word belongs to (words 0, 1 and 2, 3 of a
-//     32-k block are its two 16-k blocks) multiplies the word's pairs in FP16, exactly (an
-//     E2M1 value has 2 significant bits and an E4M3 scale 4; their product lies between 2^-10
-//     and 2688, inside FP16's normal range), and x is FP16 under one power of two for the
-//     whole vector (largest |x| in [2^14, 2^15)), so the MMAs accumulate a unit's rows over
-//     all of K with no per-block fold (four independent accumulator chains); the tensor scale
-//     and the power of two multiply each output once.
+//   * NVFP4: x is FP16 under one power of two for the whole vector (largest |x| in
+//     [2^14, 2^15)). The n8 columns of the MMAs keep the 16-k blocks apart: over a group of
+//     up to four 32-k blocks of a warp, column 2g + h of B is x on the h-th 16-k half of the
+//     group's g-th block and zero elsewhere (a lane whose column is not the block's reads a
+//     zero segment instead of x; the choice is made once, in its per-block x offset). After
+//     the group, column n of D holds the rows' sums over 16-k block n alone, and lane c,
+//     which holds columns 2c and 2c + 1, multiplies the two sums of block c by their E4M3
+//     scales in fp32. The tensor scale and the power of two multiply each output once.
 //   * MXFP4: x is FP16 under a power of two per 32-k block, each 32-k block's MMAs start
 //     from zero, and the block's power-of-two scale times the x scale multiplies its fp32 sum
 //     (lane c folds the c-th block of each group of four, like the Q4 scale).
@@ -44,6 +45,12 @@ constexpr uint32_t kFSmem = 227u * 1024u - 1024u;  // the base is aligned up to 
 
 // Shared-memory layout for T tiles per unit and K; sb = scale bytes per row and chunk (32 for
 // NVFP4's 32 E4M3 scales of 512 k, 16 for MXFP4's E8M0 ones).
+// x in shared memory, per 512-k chunk: MXFP4 its 64 16-byte segments (8 k each); NVFP4 the
+// same 64 segments, then zero segments at 64 and 68 (72 segments = 1152 bytes per chunk), one
+// on each half of the banks.
+constexpr uint32_t kFXChunkMX = 64u * 16u;
+constexpr uint32_t kFXChunkNV = 72u * 16u;
+
 struct FLayout {
   uint32_t code_bytes, scale_bytes, stage_bytes, red_off, cst_off, xperm_off, bar_off, total;
   __host__ __device__ FLayout(int T, int K, int stages, int sb) {
@@ -52,8 +59,9 @@ struct FLayout {
     stage_bytes = (code_bytes + scale_bytes + 1023u) & ~1023u;
     red_off = static_cast<uint32_t>(stages) * stage_bytes;          // [P][16 T] fp32
     cst_off = red_off + 16u * kFMaxWarps * 4u;                      // [K/32] 2^-e
-    xperm_off = (cst_off + (static_cast<uint32_t>(K) / 32u) * 4u + 15u) & ~15u;
-    bar_off = (xperm_off + (static_cast<uint32_t>(K) / 8u) * 16u + 7u) & ~7u;
+    xperm_off = (cst_off + (static_cast<uint32_t>(K) / 32u) * 4u + 127u) & ~127u;
+    const uint32_t xchunk = sb == 32 ? kFXChunkNV : kFXChunkMX;
+    bar_off = (xperm_off + (static_cast<uint32_t>(K) / 512u) * xchunk + 7u) & ~7u;
     total = bar_off + 2u * kFMaxStages * 8u + 16u;
   }
 };
@@ -65,7 +73,9 @@ __device__ __forceinline__ void f_consumer_bar() {
 
 struct FMaps {
   CUtensorMap codes;   // uint8 [N, K/2], box {128, 16 T}, 128-byte swizzle
-  CUtensorMap scales;  // uint8 [N, K/16] (NVFP4) or [N, K/32] (MXFP4), box {32 or 16, 16 T}
+  // uint8 [N, K/16] (NVFP4, box {32, 16 T}, 32-byte swizzle) or [N, K/32] (MXFP4, box
+  // {16, 16 T}, no swizzle)
+  CUtensorMap scales;
 };
 
 template <bool MX, int T, int P>
@@ -86,7 +96,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   const FLayout L(T, K, stages, SB);
   float* sRed = reinterpret_cast<float*>(smem + L.red_off);  // [P][ROWS]
   float* sCst = reinterpret_cast<float*>(smem + L.cst_off);  // [K/32] 2^-e (NVFP4: [0] only)
-  uint4* sX = reinterpret_cast<uint4*>(smem + L.xperm_off);  // [K/8] FP16, natural order
+  uint4* sX = reinterpret_cast<uint4*>(smem + L.xperm_off);  // FP16, natural order per chunk
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kFMaxStages;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + kFMaxStages);
@@ -167,7 +177,8 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   } else {
     // x (BF16) -> FP16 in natural order under one power of two for the whole vector (largest
     // |x| in [2^14, 2^15)). Pass 1 finds the largest |x|, pass 2 converts; with one segment
-    // per thread (K <= 8 NC) the segment stays in registers between the passes.
+    // per thread (K <= 8 NC) the segment stays in registers between the passes. Segment R
+    // goes to slot 72 (R / 64) + R % 64.
     float amax = 0.f;
     const bool one = segs <= NC;
     float v1[8] = {};
@@ -193,14 +204,16 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
     const int e = f_x_exponent(amax);
     const float sc = f_pow2(e);
     if (one) {
-      if (tid < segs) sX[tid] = f_f16x8(v1, sc);
+      if (tid < segs) sX[(tid >> 6) * 72 + (tid & 63)] = f_f16x8(v1, sc);
     } else {
       for (int R = tid; R < segs; R += NC) {
         float v[8];
         f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
-        sX[R] = f_f16x8(v, sc);
+        sX[(R >> 6) * 72 + (R & 63)] = f_f16x8(v, sc);
       }
     }
+    for (int z = tid; z < 2 * kchunks; z += NC)
+      sX[(z >> 1) * 72 + 64 + 4 * (z & 1)] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) sCst[0] = f_pow2(-e);
   }
   f_consumer_bar<NC>();
@@ -208,9 +221,14 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   const int gq = lane >> 2, c = lane & 3;
   const int t = warp % T, p = warp / T;  // tile in the unit, first 32-k block in a chunk
   const uint32_t rowA = static_cast<uint32_t>(16 * t + gq);  // rowB = rowA + 8
+  // Blocks per fold group: MXFP4 folds each block's sum, NVFP4 each 16-k block's (both by
+  // lane c for the group's c-th block).
+  constexpr int G = NB < 4 ? NB : 4;
   // Per block r of this warp (block p + P r of a chunk): the offset of row rowA's word c in
-  // a stage (rows gq and gq + 8 share the 128-byte swizzle phase gq = row mod 8), and of
-  // this lane's 16 bytes of x in a chunk.
+  // a stage (rows gq and gq + 8 share the 128-byte swizzle phase gq = row mod 8) and of this
+  // lane's 16 bytes of x in a chunk. NVFP4: words c = 0, 1 of a 32-k block hold its first
+  // 16-k block and c = 2, 3 its second, so lane (gq, c) carries x for column gq exactly when
+  // gq = 2 (r mod G) + c / 2, and otherwise the zero segment on the other half of the banks.
   uint32_t code_off[NB], x_off[NB];
 #pragma unroll
   for (int r = 0; r < NB; ++r) {
@@ -218,10 +236,18 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
     code_off[r] = (j >> 3) * (L.code_bytes / 2) + rowA * 128u +
                   (((j & 7u) ^ static_cast<uint32_t>(gq)) << 4) + 4u * static_cast<uint32_t>(c);
     x_off[r] = (j * 4u + static_cast<uint32_t>(c)) * 16u;
+    if (!MX && gq != 2 * (r % G) + (c >> 1)) x_off[r] = (j & 1u) ? 64u * 16u : 68u * 16u;
   }
-  // NVFP4: words c = 0, 1 of a 32-k block hold its first 16-k block, c = 2, 3 its second;
-  // this selector duplicates the lane's byte of a block's two scale bytes.
-  const uint32_t ssel = static_cast<uint32_t>(c >> 1) * 0x11u;
+  // NVFP4: the offset of row rowA's two scale bytes of the block this lane folds in each
+  // group (the scale box comes with the 32-byte swizzle: the 16-byte halves of a row swap
+  // where bit 2 of the row is set).
+  constexpr int NG = NB / G;
+  uint32_t s_off[NG];
+#pragma unroll
+  for (int i = 0; i < NG; ++i) {
+    const uint32_t j = static_cast<uint32_t>(p + P * (G * i + (c < G ? c : 0)));
+    s_off[i] = rowA * SB + ((2u * j) ^ ((static_cast<uint32_t>(gq) & 4u) << 2));
+  }
   const uint32_t ring_base = smem_addr(smem);
   const uint32_t xbase = smem_addr(sX);
   const float S = MX ? 1.0f : __ldg(tensor_scale) * sCst[0];
@@ -229,44 +255,48 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   uint32_t phase = 0u;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
     const int row0 = u * ROWS;
-    float accA = 0.f, accB = 0.f;  // MX: rows rowA, rowB, this lane's blocks
-    // NVFP4: the unit's sums (every lane), in four independent MMA chains (block parity x
-    // first / second MMA of a block), added at the end
-    float dacc[4][4] = {};
+    float accA = 0.f, accB = 0.f;  // rows rowA, rowB: this lane's blocks
     for (int kc = 0; kc < kchunks; ++kc) {
       // On an expired wait every warp keeps walking without computing, so all consumer
       // warps still meet at the per-unit barriers below.
       const bool landed = mbar_wait_bounded(&full[s], phase, abort_flag, status, limit_ns);
       const uint32_t buf = ring_base + static_cast<uint32_t>(s) * L.stage_bytes;
       const uint32_t sbox = buf + L.code_bytes;  // [16 T rows][SB bytes]
-      const uint32_t xk = xbase + static_cast<uint32_t>(kc) * (kFBlocks * 64u);
+      const uint32_t xk = xbase + static_cast<uint32_t>(kc) * (MX ? kFXChunkMX : kFXChunkNV);
       if (landed) {
         if constexpr (!MX) {
 #pragma unroll
-          for (int r = 0; r < NB; ++r) {
-            const uint32_t j = static_cast<uint32_t>(p + P * r);
-            const uint32_t w0 = f_lds32(buf + code_off[r]);
-            const uint32_t w1 = f_lds32(buf + code_off[r] + 1024u);
-            const uint4 e = f_lds128(xk + x_off[r]);
-            const uint32_t qa = f_lds_u16(sbox + rowA * SB + 2u * j);
-            const uint32_t qb = f_lds_u16(sbox + (rowA + 8u) * SB + 2u * j);
-            const uint32_t sA = f_e4m3_pair(__byte_perm(qa, 0u, ssel));
-            const uint32_t sB = f_e4m3_pair(__byte_perm(qb, 0u, ssel));
-            uint32_t p0[4], p1[4];
-            f_e2m1_pairs(w0, p0);
-            f_e2m1_pairs(w1, p1);
+          for (int i = 0; i < NG; ++i) {
+            // two chains: the first and the second MMA of each block
+            float d0[4] = {}, d1[4] = {};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              p0[i] = f_hmul2(p0[i], sA);
-              p1[i] = f_hmul2(p1[i], sB);
+            for (int g = 0; g < G; ++g) {
+              const int r = G * i + g;
+              const uint32_t w0 = f_lds32(buf + code_off[r]);
+              const uint32_t w1 = f_lds32(buf + code_off[r] + 1024u);
+              const uint4 e = f_lds128(xk + x_off[r]);
+              uint32_t p0[4], p1[4];
+              f_e2m1_pairs(w0, p0);
+              f_e2m1_pairs(w1, p1);
+              // k-slots (2c, 2c + 1) and (2c + 8, 2c + 9) of an MMA hold k = 8c + 0, 1 and
+              // 8c + 2, 3 (first MMA) or 8c + 4, 5 and 8c + 6, 7 (second): x in natural order.
+              f_mma(d0, p0[0], p1[0], p0[1], p1[1], e.x, e.y);
+              f_mma(d1, p0[2], p1[2], p0[3], p1[3], e.z, e.w);
             }
-            // k-slots (2c, 2c + 1) and (2c + 8, 2c + 9) of an MMA hold k = 8c + 0, 1 and
-            // 8c + 2, 3 (first MMA) or 8c + 4, 5 and 8c + 6, 7 (second): x in natural order.
-            f_mma(dacc[2 * (r & 1)], p0[0], p1[0], p0[1], p1[1], e.x, e.y);
-            f_mma(dacc[2 * (r & 1) + 1], p0[2], p1[2], p0[3], p1[3], e.z, e.w);
+            // Lane c: columns 2c, 2c + 1 = the two 16-k halves of the group's block c (the
+            // lanes past the group's blocks hold zero columns and fold nothing).
+            if (c < G) {
+              const uint32_t qa = f_e4m3_pair(f_lds_u16(sbox + s_off[i]));
+              const uint32_t qb = f_e4m3_pair(f_lds_u16(sbox + s_off[i] + 8u * SB));
+              const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&qa));
+              const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&qb));
+              accA = fmaf(fa.x, d0[0] + d1[0], accA);
+              accA = fmaf(fa.y, d0[1] + d1[1], accA);
+              accB = fmaf(fb.x, d0[2] + d1[2], accB);
+              accB = fmaf(fb.y, d0[3] + d1[3], accB);
+            }
           }
         } else {
-          constexpr int G = NB < 4 ? NB : 4;  // blocks per fold group
 #pragma unroll
           for (int i = 0; i < NB / G; ++i) {
             float d[G][4];
@@ -312,17 +342,11 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
         phase ^= 1u;
       }
     }
-    if constexpr (MX) {
-      // Row sums: the 4 lanes of a row group (fixed order).
-      accA += __shfl_xor_sync(0xffffffffu, accA, 1);
-      accA += __shfl_xor_sync(0xffffffffu, accA, 2);
-      accB += __shfl_xor_sync(0xffffffffu, accB, 1);
-      accB += __shfl_xor_sync(0xffffffffu, accB, 2);
-    } else {
-      // column 2c of D; every column holds the same sums
-      accA = (dacc[0][0] + dacc[1][0]) + (dacc[2][0] + dacc[3][0]);
-      accB = (dacc[0][2] + dacc[1][2]) + (dacc[2][2] + dacc[3][2]);
-    }
+    // Row sums: the 4 lanes of a row group (fixed order).
+    accA += __shfl_xor_sync(0xffffffffu, accA, 1);
+    accA += __shfl_xor_sync(0xffffffffu, accA, 2);
+    accB += __shfl_xor_sync(0xffffffffu, accB, 1);
+    accB += __shfl_xor_sync(0xffffffffu, accB, 2);
     if (c == 0) {
       sRed[p * ROWS + static_cast<int>(rowA)] = accA;
       sRed[p * ROWS + static_cast<int>(rowA) + 8] = accB;
@@ -393,7 +417,8 @@ cudaError_t launch_fp4(const uint16_t* x, const uint8_t* codes, const uint8_t* s
   const uint64_t srow = MX ? static_cast<uint64_t>(K) / 32 : static_cast<uint64_t>(K) / 16;
   e = encode_tensor_map(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, srow,
                         static_cast<uint64_t>(N), srow, static_cast<uint32_t>(SB),
-                        static_cast<uint32_t>(16 * T), CU_TENSOR_MAP_SWIZZLE_NONE);
+                        static_cast<uint32_t>(16 * T),
+                        MX ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_32B);
   if (e != cudaSuccess) return e;
   const uint32_t smem = FLayout(T, K, plan.stages, SB).total + 1024u;
   auto kern = fp4_gemv_tc_kernel<MX, T, P>;
