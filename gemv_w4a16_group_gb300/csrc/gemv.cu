@@ -238,7 +238,9 @@ __global__ void __launch_bounds__(Shape<QW, CW>::kThreads, Shape<QW, CW>::kMinBl
   const int half = (r_hi - r_lo) >> 1;
   const int items = MR * half;
   const int items_pad = (items + 31) & ~31;  // warp-uniform trip count for the shuffles
-  constexpr int kBatch = 2;  // items per thread whose loads are issued together
+  // items per thread whose loads are issued together (with 12 consumer warps and K = 4096,
+  // all of x in one round up to MR = 4; more would spill at MR = 8)
+  constexpr int kBatch = MR >= 4 ? 3 : 2;
   int im0[kBatch], ip0[kBatch];
 #pragma unroll
   for (int t = 0; t < kBatch; ++t) {
