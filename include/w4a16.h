@@ -323,8 +323,8 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
  *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. For
  *   K % 512 == 0 the tensor-pipe kernel runs: x is held in shared memory in FP16 under one
  *   power of two (its largest magnitude in [2^14, 2^15)), so elements more than 29 binades
- *   below the largest lose bits (their terms lie far below the tolerance); K up to about
- *   100,000. Other K take a kernel with x in FP16 per 128-k chunk: K up to about 110,000
+ *   below the largest lose bits (their terms lie far below the tolerance); K up to 92,160.
+ *   Other K take a kernel with x in FP16 per 128-k chunk: K up to about 110,000
  *   (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0, K % 128 == 0.
  */
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
@@ -348,11 +348,12 @@ w4a16_status mxfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
 /*
  * mxfp4_gemv -- y[n] = sum_b 2^(s[n, b] - 127) * sum_j e2m1(q[n, 32 b + j]) x[32 b + j]:
  *   x bf16 [K]; codes, scales as above; y bf16 [N] (fp32 accumulation, rounded to nearest
- *   even). The tolerance of w4a16_matmul applies. For K % 512 == 0 the tensor-pipe kernel
- *   runs (x in FP16 under a power of two per 32-k block, each block's sum times its scale in
- *   fp32); other K take a kernel in which, within a 128-k chunk of a row, a block more than
- *   2^24 below the chunk's largest block scale adds nothing (its terms are below the
- *   tolerance). K limits as for nvfp4_gemv. Requires N > 0, K > 0, K % 128 == 0.
+ *   even). The tolerance of w4a16_matmul applies. For K % 512 == 0 up to 102,912 the
+ *   tensor-pipe kernel runs (x in FP16 under a power of two per 32-k block, each block's sum
+ *   times its scale in fp32); other K take a kernel in which, within a 128-k chunk of a row,
+ *   a block more than 2^24 below the chunk's largest block scale adds nothing (its terms are
+ *   below the tolerance): K up to about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires
+ *   N > 0, K > 0, K % 128 == 0.
  */
 w4a16_status mxfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         uint16_t* y, int N, int K, w4a16_stream_t stream);

@@ -82,12 +82,13 @@ def test_nvfp4_quantize_hand_worked_tensors(w4):
 # K % 512 == 0 takes the ring kernel, units of T tiles of 16 rows split over P k-parts (on
 # 152 SMs): N = 13, 40, 333, 1000 (T = 1, P = 16), 4096 (2, 8), 6000 (3, 8), 9000 (4, 4),
 # 14336 (6, 4), 12008 (6, 4; the last unit one ragged tile), 16384 (8, 2), 28672 (12, 2);
-# x up to 64 k long. P = 16 and 8 fold groups of one and two 32-k blocks, P = 4 one group of
-# four, P = 2 two groups of four per chunk.
+# x up to 64 k long, and the longest K the ring takes (NVFP4 92,160) beside the next multiple
+# of 512, which falls back to the plain-load kernel. P = 16 and 8 fold groups of one and two
+# 32-k blocks, P = 4 one group of four, P = 2 two groups of four per chunk.
 @pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (13, 512), (333, 1024), (1000, 4224),
                                  (1000, 4608), (4096, 4096), (6000, 2048), (9000, 1536),
                                  (14336, 4096), (12008, 1536), (16384, 1024), (28672, 1024),
-                                 (40, 65536)])
+                                 (40, 65536), (16, 92160), (16, 92672)])
 def test_nvfp4_gemv_every_output(w4, fp4_variant, N, K):
     w = special_weights(N, K, seed=N * 5 + K)
     c_np, s_np, S = oracle.nvfp4_quantize(w)
@@ -167,7 +168,7 @@ def test_mxfp4_quantize_hand_worked_blocks(w4):
 @pytest.mark.parametrize("N,K", [(16, 128), (17, 256), (13, 512), (333, 1024), (1000, 4224),
                                  (1000, 4608), (4096, 4096), (6000, 2048), (9000, 1536),
                                  (14336, 4096), (12008, 1536), (16384, 1024), (28672, 1024),
-                                 (40, 65536)])
+                                 (40, 65536), (16, 102912), (16, 103424)])
 def test_mxfp4_gemv_every_output(w4, fp4_variant, N, K):
     w = mx_special_weights(N, K, seed=N * 7 + K)
     c_np, s_np = oracle.mxfp4_quantize(w)
