@@ -17,17 +17,17 @@
 //     it). Per unit the P partial sums of a row are added in a fixed order; no atomics.
 //   * A byte of two codes becomes an FP16 pair in one cvt.rn.f16x2.e2m1x2 (natural k order,
 //     so x waits in shared memory in natural order, 8 k per 16 bytes).
-//   * NVFP4: x is FP16 under one power of two for the whole vector (largest |x| in
-//     [2^14, 2^15)). The n8 columns of the MMAs keep the 16-k blocks apart: over a group of
+//   * x is FP16 under a power of two per 32-k block (its largest |x| in [2^14, 2^15)).
+//   * NVFP4: the n8 columns of the MMAs keep the 16-k blocks apart: over a group of
 //     up to four 32-k blocks of a warp, column 2g + h of B is x on the h-th 16-k half of the
 //     group's g-th block and zero elsewhere (a lane whose column is not the block's reads a
 //     zero segment instead of x; the choice is made once, in its per-block x offset). After
 //     the group, column n of D holds the rows' sums over 16-k block n alone, and lane c,
 //     which holds columns 2c and 2c + 1, multiplies the two sums of block c by their E4M3
-//     scales in fp32. The tensor scale and the power of two multiply each output once.
-//   * MXFP4: x is FP16 under a power of two per 32-k block, each 32-k block's MMAs start
-//     from zero, and the block's power-of-two scale times the x scale multiplies its fp32 sum
-//     (lane c folds the c-th block of each group of four, like the Q4 scale).
+//     scales and the block's x scale in fp32. The tensor scale multiplies each output once.
+//   * MXFP4: each 32-k block's MMAs start from zero, and the block's power-of-two scale times
+//     the x scale multiplies its fp32 sum (lane c folds the c-th block of each group of four,
+//     like the Q4 scale).
 //   * The codes carry no offset, so there is no correction term.
 #include "common.cuh"
 #include "fp4_common.cuh"
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
                                              ~static_cast<uintptr_t>(1023));
   const FLayout L(T, K, stages, SB);
   float* sRed = reinterpret_cast<float*>(smem + L.red_off);  // [P][ROWS]
-  float* sCst = reinterpret_cast<float*>(smem + L.cst_off);  // [K/32] 2^-e (NVFP4: [0] only)
+  float* sCst = reinterpret_cast<float*>(smem + L.cst_off);  // [K/32] 2^-e per 32-k block
   uint4* sX = reinterpret_cast<uint4*>(smem + L.xperm_off);  // FP16, natural order per chunk
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kFMaxStages;
@@ -156,65 +156,27 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   // ---------------- consumer warps ----------------
   pdl_wait();  // x and y may belong to the previous kernel on the stream
   const int segs = K / 8;  // segment R = 8 k
-  if constexpr (MX) {
-    // x (BF16) -> FP16 in natural order with a power-of-two scale per 32-k block, the 4
-    // segments of a block on 4 adjacent lanes (segs and the thread count are multiples of
-    // 32, so a warp is either wholly inside x or wholly past it).
-    for (int base = 0; base < segs; base += NC) {
-      const int R = base + tid;
-      if (R >= segs) break;  // warp-uniform
-      float v[8];
-      f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
-      float amax = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const int e = f_x_exponent(amax);
-      sX[R] = f_f16x8(v, f_pow2(e));
-      if ((R & 3) == 0) sCst[R >> 2] = f_pow2(-e);
-    }
-  } else {
-    // x (BF16) -> FP16 in natural order under one power of two for the whole vector (largest
-    // |x| in [2^14, 2^15)). Pass 1 finds the largest |x|, pass 2 converts; with one segment
-    // per thread (K <= 8 NC) the segment stays in registers between the passes. Segment R
-    // goes to slot 72 (R / 64) + R % 64.
+  // x (BF16) -> FP16 in natural order with a power-of-two scale per 32-k block (its largest
+  // |x| in [2^14, 2^15)), the 4 segments of a block on 4 adjacent lanes (segs and the thread
+  // count are multiples of 32, so a warp is either wholly inside x or wholly past it).
+  // NVFP4 puts segment R at slot 72 (R / 64) + R % 64, beside each chunk's zero segments.
+  for (int base = 0; base < segs; base += NC) {
+    const int R = base + tid;
+    if (R >= segs) break;  // warp-uniform
+    float v[8];
+    f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
     float amax = 0.f;
-    const bool one = segs <= NC;
-    float v1[8] = {};
-    if (one) {
-      if (tid < segs) f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + tid), v1);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v1[q]));
-    } else {
-      for (int R = tid; R < segs; R += NC) {
-        float v[8];
-        f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
+    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
 #pragma unroll
-        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) sRed[warp] = amax;
-    f_consumer_bar<NC>();
-    amax = sRed[0];
-#pragma unroll
-    for (int w = 1; w < W; ++w) amax = fmaxf(amax, sRed[w]);
+    for (int o = 1; o < 4; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const int e = f_x_exponent(amax);
-    const float sc = f_pow2(e);
-    if (one) {
-      if (tid < segs) sX[(tid >> 6) * 72 + (tid & 63)] = f_f16x8(v1, sc);
-    } else {
-      for (int R = tid; R < segs; R += NC) {
-        float v[8];
-        f_bf16x8(__ldg(reinterpret_cast<const uint4*>(x) + R), v);
-        sX[(R >> 6) * 72 + (R & 63)] = f_f16x8(v, sc);
-      }
-    }
+    sX[MX ? R : (R >> 6) * 72 + (R & 63)] = f_f16x8(v, f_pow2(e));
+    if ((R & 3) == 0) sCst[R >> 2] = f_pow2(-e);
+  }
+  if constexpr (!MX) {
     for (int z = tid; z < 2 * kchunks; z += NC)
       sX[(z >> 1) * 72 + 64 + 4 * (z & 1)] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid == 0) sCst[0] = f_pow2(-e);
   }
   f_consumer_bar<NC>();
 
@@ -250,7 +212,7 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
   }
   const uint32_t ring_base = smem_addr(smem);
   const uint32_t xbase = smem_addr(sX);
-  const float S = MX ? 1.0f : __ldg(tensor_scale) * sCst[0];
+  const float S = MX ? 1.0f : __ldg(tensor_scale);
   int s = 0;
   uint32_t phase = 0u;
   for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
@@ -284,16 +246,17 @@ __global__ void __launch_bounds__(T * P * 32 + 32, 1)
               f_mma(d1, p0[2], p1[2], p0[3], p1[3], e.z, e.w);
             }
             // Lane c: columns 2c, 2c + 1 = the two 16-k halves of the group's block c (the
-            // lanes past the group's blocks hold zero columns and fold nothing).
+            // lanes past the group's blocks hold zero columns and fold nothing), times their
+            // E4M3 scales and the block's x scale 2^-e.
             if (c < G) {
+              const uint32_t j = static_cast<uint32_t>(p + P * (G * i + c));
+              const float u2 = sCst[kc * kFBlocks + static_cast<int>(j)];
               const uint32_t qa = f_e4m3_pair(f_lds_u16(sbox + s_off[i]));
               const uint32_t qb = f_e4m3_pair(f_lds_u16(sbox + s_off[i] + 8u * SB));
               const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&qa));
               const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&qb));
-              accA = fmaf(fa.x, d0[0] + d1[0], accA);
-              accA = fmaf(fa.y, d0[1] + d1[1], accA);
-              accB = fmaf(fb.x, d0[2] + d1[2], accB);
-              accB = fmaf(fb.y, d0[3] + d1[3], accB);
+              accA = fmaf(u2, fmaf(fa.x, d0[0] + d1[0], fa.y * (d0[1] + d1[1])), accA);
+              accB = fmaf(u2, fmaf(fb.x, d0[2] + d1[2], fb.y * (d0[3] + d1[3])), accB);
             }
           }
         } else {

@@ -321,11 +321,11 @@ w4a16_status nvfp4_quantize(const float* w, int N, int K, uint8_t* codes, uint8_
  * nvfp4_gemv -- y[n] = S * sum_b e4m3(s[n, b]) * sum_j e2m1(q[n, 16 b + j]) x[16 b + j]:
  *   x bf16 [K]; codes, scales, tensor_scale as above (device memory); y bf16 [N] (fp32
  *   accumulation, rounded to nearest even). The tolerance of w4a16_matmul applies. For
- *   K % 512 == 0 the tensor-pipe kernel runs: x is held in shared memory in FP16 under one
- *   power of two (its largest magnitude in [2^14, 2^15)), so elements more than 29 binades
- *   below the largest lose bits (their terms lie far below the tolerance); K up to 92,160.
- *   Other K take a kernel with x in FP16 per 128-k chunk: K up to about 110,000
- *   (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0, K % 128 == 0.
+ *   K % 512 == 0 up to 92,160 the tensor-pipe kernel runs: x is held in shared memory in
+ *   FP16 under a power of two per 32-k block (its largest magnitude in [2^14, 2^15)), so
+ *   elements more than 29 binades below their block's largest lose bits (their terms lie
+ *   far below the tolerance). Other K take a kernel with x in FP16 per 128-k chunk: K up to
+ *   about 110,000 (W4A16_ERR_UNSUPPORTED beyond). Requires N > 0, K > 0, K % 128 == 0.
  */
 w4a16_status nvfp4_gemv(const uint16_t* x, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, uint16_t* y, int N, int K,
