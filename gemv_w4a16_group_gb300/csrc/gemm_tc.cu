@@ -7,10 +7,13 @@
 // cores with fp32 sums, store BF16. The BF16 weights never reach global memory.
 //
 // GB300 design (not the Triton kernel's):
-//   * Roles: warp 4 issues TMA loads (x tile, packed-word tile, scale and min rows) into
-//     a 4-stage shared-memory ring; warps 0-3 rebuild the weight tile and write it into
-//     TMEM with tcgen05.st (each warp owns the 32 TMEM lanes of its quadrant); warp 5
-//     issues tcgen05.mma from one thread; warps 0-3 then drain the accumulator.
+//   * Roles: the dequantising warps (4, or 8 for BM = 256: two per TMEM lane quarter, each
+//     taking half of every 64-k block) rebuild the weight tile and write it into TMEM with
+//     tcgen05.st (a warp owns the 32 TMEM lanes of its quarter); the next warp issues TMA
+//     loads (x tile, packed-word tile, scale and min rows) into a shared-memory ring of 4 to
+//     12 stages (deeper for narrow tiles); the last issues tcgen05.mma from one thread; the
+//     dequantising warps then drain the accumulator (with split K: fp32 partials, summed by
+//     the last CTA of the tile to arrive, in split order).
 //   * The weight tile is the MMA's A operand straight from TMEM (128 weight columns =
 //     128 TMEM lanes, 16 k = 8 columns of BF16 pairs), so the dequantised tile costs no
 //     shared-memory bandwidth; x is the B operand (K-major, 128-byte swizzle) from
