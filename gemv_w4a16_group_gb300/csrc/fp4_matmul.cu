@@ -15,9 +15,11 @@
 //     taking tile t and the 32-k blocks p, p + P, ... of every chunk) with each chunk's slice
 //     of x (8 KB per 8 rows) copied beside the weights, so that a weight fragment is decoded
 //     once and feeds the m16n8k16 MMAs of every 8 rows of x (the n8 columns). NVFP4 scales the
-//     FP16 code pairs by their E4M3 block scale before the MMAs (exact, as in the GEMV) and
-//     accumulates over all of K; MXFP4 starts each 32-k block's MMAs from zero and adds the
-//     block's fp32 sums times its power-of-two scale. The P k-parts of a unit are added in a
+//     FP16 code pairs by their E4M3 block scale before the MMAs (exact: an E2M1 value times an
+//     E4M3 scale lies inside FP16's normal range; the GEMV instead keeps the 16-k blocks apart
+//     in the n8 columns, which here hold the rows of x) and accumulates over all of K; MXFP4
+//     starts each 32-k block's MMAs from zero and adds the block's fp32 sums times its
+//     power-of-two scale. The P k-parts of a unit are added in a
 //     fixed order through shared memory; y = S 2^-e_m (sum) in BF16.
 // Rows of x beyond 32 take further passes (the weights stream again; a larger M belongs on a
 // tcgen05 tile kernel).

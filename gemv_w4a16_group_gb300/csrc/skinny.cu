@@ -6,10 +6,11 @@
 // Same per-group factorised form as the M = 1 kernel ("Low-Precision Kernels: INT4, INT8 and
 // FP8 Matmuls, Measured", "How the measurements were taken"). Between one row and the
 // tensor-core tile GEMM the pages measure the weight-only kernel's gain holding to about 16
-// rows and shrinking past that ("Batch size: where the 4-bit advantage ends"): the batch is
-// still too small to fill a 128-row tcgen05 tile, and a tcgen05.mma of 128 x 16 costs the
-// same for any N up to 256 (measured), so at 16 rows it runs at 1/16 of its rate. mma.sync
-// keeps n8 granularity: 4 MMAs per 256 codes and n8 tile.
+// rows and shrinking past that ("Batch size: where the 4-bit advantage ends"). With so few
+// rows as tcgen05's N, every 128 x 16 weight tile would be rebuilt into tensor memory for
+// only those rows (the tcgen05 kernel measured about twice this kernel's time at 16 rows).
+// mma.sync keeps n8 granularity and the weights in registers: 4 MMAs per 256 codes and n8
+// tile.
 //
 // Two kernels per call, chained by programmatic dependent launch:
 //   * skinny_xprep_kernel converts x once per call into the caller's workspace: FP16 B
