@@ -99,8 +99,9 @@ w4a16_status w4a16_pack(const uint8_t* codes, int N, int K, int32_t* qw,
  * Kernel choice is by M: for 5 <= M <= 32 a skinny kernel (FP16 mma.sync with the batch in
  * n8 tiles) when the caller's workspace holds its converted activations; otherwise a GEMV for
  * M <= 8 and a TMA + tcgen05 tensor-core kernel above. Accuracy:
- * |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k| per output, y_ref the exact product on the same 4-bit weights. Results are
- * deterministic (no floating-point atomics).
+ * |y - y_ref| <= 4e-3 |y_ref| + 1e-3 sum_k |x_k w_hat_k| per output, y_ref the exact
+ * product on the same 4-bit weights. Results are deterministic (no floating-point
+ * atomics).
  *   workspace / workspace_bytes: optional caller-owned device scratch that lets small-N
  *   shapes split K across thread blocks and lets 5 <= M <= 32 use the skinny kernel; size
  *   it with w4a16_matmul_workspace_bytes(). NULL (with 0 bytes) is always accepted. The
