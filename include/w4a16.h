@@ -388,8 +388,8 @@ w4a16_status mxfp4_matmul(const uint16_t* x, const uint8_t* codes, const uint8_t
  * device's status word. Returns W4A16_ERR_TIMEOUT if any kernel of this library gave
  * up a bounded wait since the last query, W4A16_ERR_LAYOUT if a kernel found its
  * dynamic shared memory less than 128-byte aligned and skipped its work (its output is
- * then not written), W4A16_ERR_CUDA if the synchronization failed, W4A16_OK otherwise. (The pages have no counterpart; this is the library's
- * failure-detection hook.)
+ * then not written), W4A16_ERR_CUDA if the synchronization failed, W4A16_OK otherwise.
+ * (The pages have no counterpart; this is the library's failure-detection hook.)
  */
 w4a16_status w4a16_device_status(w4a16_stream_t stream);
 
